@@ -1,0 +1,312 @@
+"""Pins of the CPU oracle to things other than itself.
+
+Each ``check_*`` takes a loaded oracle library (``oracle.load(path)``) and raises
+AssertionError when the oracle disagrees with what the pages, the mathematics or
+an independent library routine fix.  ``test_oracle_pins.py`` runs them on the
+oracle; ``test_oracle_mutants.py`` runs them on copies of the oracle with a
+planted mistake and expects at least one to fail.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle
+from ulysses_sequence_attention_tf_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def ordered16(bits: torch.Tensor) -> torch.Tensor:
+    """Map 16-bit float patterns to integers whose difference counts ulps."""
+    b = bits.to(torch.int32) & 0xFFFF
+    mag = b & 0x7FFF
+    return torch.where(b >= 0x8000, -mag, mag)
+
+
+def ulp_diff(a: torch.Tensor, b: torch.Tensor) -> torch.Tensor:
+    return (ordered16(a.view(torch.int16)) - ordered16(b.view(torch.int16))).abs()
+
+
+# ----------------------------------------------------------------------------
+# 16-bit codecs vs the library conversions (torch for bfloat16, numpy for binary16)
+# ----------------------------------------------------------------------------
+
+def check_codec_decode(lib):
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    ref_bf = bits.view(torch.bfloat16).double().numpy()
+    ref_h = bits.numpy().view(np.float16).astype(np.float64)
+    for fmt, ref in ((1, ref_bf), (0, ref_h)):
+        step = 7 if fmt == 1 else 5  # a spread of patterns over every exponent
+        for i in list(range(0, 65536, step)) + [0x0000, 0x8000, 0x0001, 0x7F7F, 0x7F80, 0xFF80, 0x7BFF, 0x7C00, 0x03FF]:
+            got = lib.tfo_decode16(fmt, i)
+            want = ref[i]
+            assert (math.isnan(got) and math.isnan(want)) or got == want, (fmt, hex(i), got, want)
+
+
+def _fp32_probe_values(n=60000, seed=3):
+    rng = np.random.default_rng(seed)
+    bits = rng.integers(0, 2**32, size=n, dtype=np.uint64).astype(np.uint32)
+    vals = bits.view(np.float32)
+    vals = vals[np.isfinite(vals)]
+    # exact ties for bf16 (low 16 bits 0x8000) and for fp16 (13 low bits at the half point)
+    ties_bf = (rng.integers(0, 2**16, size=4000, dtype=np.uint64).astype(np.uint32) << 16 | 0x8000).view(np.float32)
+    mant = rng.integers(0, 2**10, size=4000, dtype=np.uint64).astype(np.uint32)
+    exps = rng.integers(100, 143, size=4000, dtype=np.uint64).astype(np.uint32)  # around fp16 range
+    ties_h = ((exps << 23) | (mant << 13) | (1 << 12)).view(np.float32)
+    normal = rng.standard_normal(20000).astype(np.float32) * np.float32(3.0)
+    tiny = (rng.standard_normal(4000) * 1e-6).astype(np.float32)  # fp16 subnormal range
+    big = np.array([65504.0, 65519.99, 65520.0, 65536.0, 3.3895314e38, 3.4e38, -65520.0, 0.0, -0.0,
+                    5.96e-8, 2.98e-8, 2.99e-8, 1e-40, -1e-45], dtype=np.float32)
+    allv = np.concatenate([vals, ties_bf[np.isfinite(ties_bf)], ties_h, normal, tiny, big])
+    return allv.astype(np.float32)
+
+
+def check_codec_encode(lib):
+    vals = _fp32_probe_values()
+    want_bf = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
+    with np.errstate(over="ignore"):  # overflow to infinity is part of what is checked
+        want_h = vals.astype(np.float16).view(np.uint16)
+    for i, x in enumerate(vals.tolist()):
+        gb = lib.tfo_encode16(1, x)
+        assert gb == want_bf[i], ("bf16", x, hex(gb), hex(want_bf[i]))
+        gh = lib.tfo_encode16(0, x)
+        assert gh == want_h[i], ("fp16", x, hex(gh), hex(want_h[i]))
+
+
+# ----------------------------------------------------------------------------
+# Relayout
+# ----------------------------------------------------------------------------
+
+def check_relayout_golden(lib):
+    with open(os.path.join(GOLDEN, "relayout_handworked.json")) as f:
+        gold = json.load(f)
+    for case in gold["cases"]:
+        P = case["P"]
+        srcs = [torch.tensor(s, dtype=torch.int32).unsqueeze(0) for s in case["sources"]]
+        tgts = [torch.tensor(s, dtype=torch.int32).unsqueeze(0) for s in case["targets"]]
+        got = oracle.scatter(srcs, P, lib=lib)
+        for g in range(P):
+            assert torch.equal(got[g], tgts[g]), (case, g, got[g])
+        back = oracle.gather(tgts, P, lib=lib)
+        for r in range(P):
+            assert torch.equal(back[r], srcs[r]), (case, r)
+
+
+def _allgather_scatter_reference(srcs, P):
+    """The all-gather formulation: concatenate the shards along the sequence in
+    rank order, then take head band g (library routines only)."""
+    full = torch.cat([s.contiguous() for s in srcs], dim=1)
+    Hl = full.shape[2] // P
+    return [full[:, :, g * Hl:(g + 1) * Hl, :].contiguous() for g in range(P)]
+
+
+def _allgather_gather_reference(attn, P):
+    """Inverse: concatenate the head groups along heads, then take shard r's tokens."""
+    full = torch.cat([a.contiguous() for a in attn], dim=2)
+    Sl = full.shape[1] // P
+    return [full[:, r * Sl:(r + 1) * Sl].contiguous() for r in range(P)]
+
+
+RELAYOUT_SHAPES = [
+    # P, B, Sl, H, D, layout, dtype
+    (1, 1, 3, 2, 4, "contiguous", torch.int16),
+    (2, 1, 5, 4, 8, "contiguous", torch.bfloat16),
+    (3, 2, 3, 6, 2, "fused", torch.float16),
+    (4, 2, 1, 8, 3, "v_strided", torch.bfloat16),
+    (2, 3, 4, 6, 1, "fused", torch.float32),
+    (5, 1, 2, 10, 5, "contiguous", torch.int8),
+    (4, 1, 6, 4, 16, "v_strided", torch.float64),
+]
+
+
+def _shards(P, B, Sl, H, D, layout, dtype, seed):
+    if dtype in (torch.int8, torch.int16):
+        d = synth.qkv_shards(P, B, Sl, H, D, torch.float32, seed=seed, layout=layout)
+        cast = lambda x: (x * 50).to(dtype)  # noqa: E731  (views keep their strides below)
+        out = {}
+        for key in ("q", "k", "v"):
+            out[key] = [cast(x) for x in d[key]]
+        return out
+    return synth.qkv_shards(P, B, Sl, H, D, dtype, seed=seed, layout=layout)
+
+
+def check_relayout_allgather(lib):
+    for i, (P, B, Sl, H, D, layout, dtype) in enumerate(RELAYOUT_SHAPES):
+        d = _shards(P, B, Sl, H, D, layout, dtype, seed=11 + i)
+        for key in ("q", "v"):
+            srcs = d[key]
+            got = oracle.scatter(srcs, P, lib=lib)
+            want = _allgather_scatter_reference(srcs, P)
+            for g in range(P):
+                assert torch.equal(got[g].view(torch.uint8), want[g].view(torch.uint8)), (P, B, Sl, H, D, layout, key, g)
+            back = oracle.gather(got, P, lib=lib)
+            want_back = _allgather_gather_reference(got, P)
+            for r in range(P):
+                assert torch.equal(back[r].view(torch.uint8), want_back[r].view(torch.uint8)), ("gather", P, key, r)
+
+
+def check_relayout_invariants(lib):
+    # exactly once: distinct ids land once each; gather(scatter(x)) == x; P = 1 is the identity layout
+    for P, B, Sl, H, D in [(2, 1, 4, 4, 2), (3, 2, 2, 6, 4), (4, 1, 3, 8, 2), (1, 2, 5, 3, 4), (8, 1, 2, 8, 8)]:
+        srcs = synth.unique_id_shards(P, B, Sl, H, D)
+        tg = oracle.scatter(srcs, P, lib=lib)
+        src_ids = torch.cat([s.flatten() for s in srcs]).sort().values
+        tgt_ids = torch.cat([t.flatten() for t in tg]).sort().values
+        assert torch.equal(src_ids, tgt_ids), "an element was lost or duplicated"
+        back = oracle.gather(tg, P, lib=lib)
+        for r in range(P):
+            assert torch.equal(back[r], srcs[r]), ("round trip", P, r)
+        if P == 1:
+            assert torch.equal(tg[0], srcs[0]), "P = 1 must be the identity layout"
+
+
+# ----------------------------------------------------------------------------
+# RMSNorm + RoPE
+# ----------------------------------------------------------------------------
+
+def _table_row(lib, theta, S, D, p):
+    return oracle.rope_table(theta, S, D, lib=lib)[p]
+
+
+def check_rope_table_textbook(lib):
+    with open(os.path.join(GOLDEN, "rope_textbook.json")) as f:
+        gold = json.load(f)
+    c1, s1 = np.float32(gold["cos_1"]), np.float32(gold["sin_1"])
+    for case in gold["cases"]:
+        tab = oracle.rope_table(case["theta"], case["p"] + 1, case["D"], lib=lib)
+        c, s = tab[case["p"], case["i"]].tolist()
+        assert np.float32(c) == c1 and np.float32(s) == s1, (case, c, s)
+    # position 0 is the identity rotation
+    tab = oracle.rope_table(10000.0, 3, 128, lib=lib)
+    assert torch.all(tab[0, :, 0] == 1.0) and torch.all(tab[0, :, 1] == 0.0)
+    # pair 0 rotates by exactly p radians; every entry lies on the unit circle
+    tab = oracle.rope_table(10000.0, 4096, 64, lib=lib).double()
+    r2 = tab[..., 0] ** 2 + tab[..., 1] ** 2
+    assert torch.all((r2 - 1).abs() < 4e-7)
+    # angle addition: rot((p+q) f) = rot(p f) rot(q f) for a frequency f of the table
+    p, q = 1234, 987
+    cp, sp = tab[p, :, 0], tab[p, :, 1]
+    cq, sq = tab[q, :, 0], tab[q, :, 1]
+    assert torch.all((cp * cq - sp * sq - tab[p + q, :, 0]).abs() < 2e-6)
+    assert torch.all((sp * cq + cp * sq - tab[p + q, :, 1]).abs() < 2e-6)
+
+
+def _rms_norm_torch(x: torch.Tensor, w: torch.Tensor, eps: float):
+    """Library reference of the normalise step: fp32 rms_norm, cast, then 16-bit weight scale."""
+    y = torch.nn.functional.rms_norm(x.float(), (x.shape[-1],), eps=eps).to(x.dtype)
+    return y * w  # 16-bit x 16-bit product, rounded to the 16-bit type
+
+
+def check_rmsnorm_vs_torch(lib):
+    eps = 1e-6
+    for dtype in (torch.bfloat16, torch.float16):
+        for D in (64, 128):
+            gen = synth.make_generator(5, "cpu")
+            x = torch.randn((400, D), generator=gen).to(dtype)
+            x[0] = 0  # zero row: 0 * 1/sqrt(eps) = 0
+            x[1] = 3.0  # constant row
+            x[2] *= 1e-3  # tiny row, where eps matters
+            wq, _ = synth.norm_weights(D, dtype, seed=9)
+            ones = torch.ones(D, dtype=dtype)
+            ident = oracle.rope_table(10000.0, 1, D, lib=lib)[0]  # p = 0: no rotation
+            for w in (ones, wq):
+                want = _rms_norm_torch(x, w, eps)
+                got = torch.stack([oracle.rmsnorm_rope_row(x[i], w, eps, ident, lib=lib) for i in range(x.shape[0])])
+                ud = ulp_diff(got, want)
+                # torch's fp32 reduction order may flip an isolated value by one ulp
+                assert int(ud.max()) <= 1, (dtype, D, int(ud.max()))
+                assert int((ud > 0).sum()) <= max(2, x.numel() // 2000), (dtype, D, int((ud > 0).sum()))
+
+
+def check_rmsnorm_closed_forms(lib):
+    eps = 1e-6
+    D = 64
+    ident = oracle.rope_table(10000.0, 1, D, lib=lib)[0]
+    for dtype in (torch.bfloat16, torch.float16):
+        ones = torch.ones(D, dtype=dtype)
+        for c in (3.0, -0.5, 1e-3, 2e-4):
+            x = torch.full((D,), c, dtype=dtype)
+            cx = float(x[0])
+            # mean(x^2) = c^2 exactly; y = c / sqrt(c^2 + eps), one rounding to the 16-bit type
+            exact = cx / math.sqrt(cx * cx + eps)
+            got = oracle.rmsnorm_rope_row(x, ones, eps, ident, lib=lib)
+            want = torch.tensor([exact], dtype=torch.float64).to(dtype)
+            assert int(ulp_diff(got, want.expand(D)).max()) <= 1, (dtype, c, got[0], exact)
+        # weight 1, no rotation: the output has rms 1 up to 16-bit rounding
+        gen = synth.make_generator(21, "cpu")
+        x = torch.randn((D,), generator=gen).to(dtype)
+        got = oracle.rmsnorm_rope_row(x, ones, eps, ident, lib=lib).double()
+        assert abs(float(got.pow(2).mean().sqrt()) - 1.0) < 2 ** -7
+
+
+def _rotate_complex(z: torch.Tensor, angles: torch.Tensor) -> torch.Tensor:
+    """Interleaved RoPE as multiplication of (z[2i] + j z[2i+1]) by exp(j angle_i), complex128."""
+    zc = torch.view_as_complex(z.double().reshape(-1, 2).contiguous())
+    out = zc * torch.polar(torch.ones_like(angles), angles)
+    return torch.view_as_real(out).reshape(-1)
+
+
+def check_rope_vs_complex(lib):
+    eps = 1e-6
+    theta = 10000.0
+    for dtype in (torch.bfloat16, torch.float16):
+        for D in (64, 128):
+            S = 300
+            tab = oracle.rope_table(theta, S, D, lib=lib)
+            ident = tab[0]
+            gen = synth.make_generator(33, "cpu")
+            wq, _ = synth.norm_weights(D, dtype, seed=2)
+            worst = 0
+            for p in (1, 2, 17, 123, 299):
+                x = torch.randn((D,), generator=gen).to(dtype)
+                z = oracle.rmsnorm_rope_row(x, wq, eps, ident, lib=lib)  # normalised + scaled, unrotated
+                got = oracle.rmsnorm_rope_row(x, wq, eps, tab[p], lib=lib)
+                angles = torch.tensor([p * theta ** (-2.0 * i / D) for i in range(D // 2)], dtype=torch.float64)
+                want = _rotate_complex(z, angles)
+                err = (got.double() - want).abs()
+                # one rounding of the output plus the fp32 table rounding
+                bound = want.abs() * 2.0 ** (-7 if dtype == torch.bfloat16 else -10) + 2e-6 * z.double().abs().max()
+                assert torch.all(err <= bound + 1e-12), (dtype, D, p, float((err - bound).max()))
+                worst = max(worst, int((err > 0).sum()))
+                # rotation keeps each pair's length
+                n_in = z.double().reshape(-1, 2).pow(2).sum(-1).sqrt()
+                n_out = got.double().reshape(-1, 2).pow(2).sum(-1).sqrt()
+                rel = 2.0 ** (-6 if dtype == torch.bfloat16 else -9)
+                assert torch.all((n_in - n_out).abs() <= rel * n_in + 1e-6), (dtype, D, p)
+
+
+def check_fused_scatter_composition(lib):
+    """The fused scatter equals the plain scatter followed by the row operation at
+    target row index p (global position), so the two oracle entry points agree."""
+    P, B, Sl, H, D = 3, 2, 5, 6, 64
+    dtype = torch.bfloat16
+    d = synth.qkv_shards(P, B, Sl, H, D, dtype, seed=4, layout="fused")
+    wq, _ = synth.norm_weights(D, dtype, seed=4)
+    tab = oracle.rope_table(10000.0, P * Sl, D, lib=lib)
+    fused = oracle.scatter_norm_rope(d["q"], P, wq, 1e-6, tab, lib=lib)
+    plain = oracle.scatter(d["q"], P, lib=lib)
+    for g in range(P):
+        for b in range(B):
+            for p in range(P * Sl):
+                for h in range(H // P):
+                    row = oracle.rmsnorm_rope_row(plain[g][b, p, h], wq, 1e-6, tab[p], lib=lib)
+                    assert torch.equal(row.view(torch.int16), fused[g][b, p, h].view(torch.int16)), (g, b, p, h)
+
+
+ALL_CHECKS = [
+    check_codec_decode,
+    check_codec_encode,
+    check_relayout_golden,
+    check_relayout_allgather,
+    check_relayout_invariants,
+    check_rope_table_textbook,
+    check_rmsnorm_vs_torch,
+    check_rmsnorm_closed_forms,
+    check_rope_vs_complex,
+    check_fused_scatter_composition,
+]
