@@ -1,0 +1,390 @@
+#!/usr/bin/env python3
+"""Benchmark of the Ulysses sequence<->head relayout on GB300.
+
+One step = the whole hot path on the video-DiT workload (P=4 logical shards,
+B=1, S=32760 = 21x30x52 tokens, H=40, D=128, bf16): one grouped scatter of Q, K
+and V into the cached final-layout targets, with RMSNorm + interleaved RoPE at
+global positions fused on Q/K and V read as a strided view of a fused
+projection, then the head->sequence gather of a synthetic attention output.
+
+Metric: relayout GB/s = algorithmic payload bytes (every element read once and
+written once: 3 x 2 x 335.5 MB for the scatter, 2 x 335.5 MB for the gather)
+per second, plus tokens/s.  Timing: CUDA events on the launching stream around
+K steps after W warm-up steps, synchronised on both sides, max over ranks.
+Inputs rotate over two sets of ~2 GB each, so every step reads from HBM (the
+inputs are larger than the 129 MB L2).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the CPU oracle (the reference arm of this build) on
+a bounded token-sample of the same workload.  N>1 (torchrun) runs independent
+replicas, one per GPU ("replicas only": the path has no cross-GPU exchange on
+one box).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "relayout GB/s (read+write) and % of GB300 HBM peak; fused Q/K/V tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = dict(name="video_dit_p4_s32760", P=4, B=1, S=32760, H=40, D=128, eps=1e-6, theta=10000.0)
+PROFILE = os.path.join(ROOT, "profiles", "fused_scatter_video_dit_p4_s32760.txt")
+KERNEL_SOURCES = [os.path.join(ROOT, "ulysses_sequence_attention_tf_gb300", "csrc", f)
+                  for f in ("relayout_kernels.cu", "relayout.h")]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=1024, help="tokens per shard in the CPU-baseline sample")
+    return ap.parse_args()
+
+
+def step_bytes(w, S=None):
+    """Algorithmic bytes of one step: (scatter payload, scatter extra, gather payload)."""
+    S = w["S"] if S is None else S
+    tensor = w["B"] * S * w["H"] * w["D"] * 2  # one of Q/K/V over all shards, bf16
+    scatter_payload = 3 * 2 * tensor  # Q, K, V each read once and written once
+    scatter_extra = S * w["D"] * 4 + 2 * w["D"] * 2  # fp32 (cos, sin) rows + two RMSNorm weights
+    gather_payload = 2 * tensor
+    return scatter_payload, scatter_extra, gather_payload
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, torch copy)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the fused scatter from the committed ncu summary,
+    or None if the summary is missing or the kernel changed since it was taken."""
+    try:
+        fields = {}
+        with open(PROFILE) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("kernel_source_sha256_16") != kernel_source_hash():
+            return None
+        return int(float(fields["dram_bytes_per_full_launch"]))
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+               "-lms", "50"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons, n = [], [], set(), 0
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            n += 1
+            for name, val in zip(self.NAMES, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+def gpu_id_for_smi(torch, dev):
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if uuid:
+            return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:  # noqa: BLE001
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    return vis.split(",")[dev] if vis else str(dev)
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+def oracle_step(w, Sl, seed=0):
+    """One step of the workload on the CPU oracle with S_local = Sl tokens per
+    shard; returns seconds."""
+    import torch
+
+    import oracle
+    from ulysses_sequence_attention_tf_gb300 import synth
+    P, B, H, D = w["P"], w["B"], w["H"], w["D"]
+    d = synth.qkv_shards(P, B, Sl, H, D, torch.bfloat16, seed=seed, layout="v_strided")
+    wq, wk = synth.norm_weights(D, torch.bfloat16, seed=0)
+    attn = synth.attn_outputs(P, B, P * Sl, H // P, D, torch.bfloat16, seed=seed)
+    oracle.load()
+    t0 = time.perf_counter()
+    table = oracle.rope_table(w["theta"], P * Sl, D)
+    oracle.scatter(d["v"], P)
+    oracle.scatter_norm_rope(d["q"], P, wq, w["eps"], table)
+    oracle.scatter_norm_rope(d["k"], P, wk, w["eps"], table)
+    oracle.gather(attn, P)
+    return time.perf_counter() - t0
+
+
+def cpu_cores_used():
+    return 1  # the oracle is single-threaded C
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle, as it stands, on a bounded token-sample per step."""
+    w = WORKLOAD
+    # calibrate: seconds per token per shard, then size each step's sample so the
+    # whole --warmup + --steps run stays within about two and a half minutes
+    cal = oracle_step(w, 4) / 4
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    Sl = max(1, min(w["S"] // w["P"], int(budget / cal)))
+    for i in range(args.warmup):
+        oracle_step(w, Sl, seed=i)
+    times = [oracle_step(w, Sl, seed=100 + i) for i in range(args.steps)]
+    t = sum(times) / len(times)
+    sp, _, gp = step_bytes(w, S=w["P"] * Sl)
+    value = (sp + gp) / t / 1e9
+    sample = (f"S_local={Sl} tokens per shard (of {w['S'] // w['P']}), every other size as the workload; "
+              f"one oracle step = fused Q/K scatter, V scatter, cos/sin table, output gather")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w["name"], "P": w["P"], "B": w["B"], "S": w["S"], "H": w["H"], "D": w["D"],
+                   "parallelism": "replicas", "l2": "CPU oracle; no GPU"},
+        "tokens_per_s": w["P"] * Sl * w["B"] / t,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cpu_cores_used(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    from ulysses_sequence_attention_tf_gb300 import binding, build, synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    build.build()
+    binding.lib()
+    binding.use_torch_allocator(True)
+
+    w = WORKLOAD
+    P, B, S, H, D = w["P"], w["B"], w["S"], w["H"], w["D"]
+    Sl, Hl = S // P, H // P
+    dtype = torch.bfloat16
+    nsets = 2
+    sets = []
+    for s in range(nsets):
+        g = synth.qkv_shards(P, B, Sl, H, D, dtype, seed=1000 * rank + s, layout="v_strided", device=dev)
+        g["attn"] = synth.attn_outputs(P, B, S, Hl, D, dtype, seed=1000 * rank + s, device=dev)
+        sets.append(g)
+    wq, wk = synth.norm_weights(D, dtype, seed=0, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(g):
+        binding.scatter_qkv("bench_qkv", g["q"], g["k"], g["v"], norm_rope=True, q_weight=wq, k_weight=wk,
+                            eps=w["eps"], theta=w["theta"], stream=stream)
+        binding.gather_out("bench_out", g["attn"], stream=stream)
+
+    for i in range(args.warmup):
+        step(sets[i % nsets])
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_id_for_smi(torch, local_rank))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    n_launch0 = binding.launch_count()
+    start.record(stream)
+    for k in range(K):
+        g = sets[k % nsets]
+        ev[k][0].record(stream)
+        binding.scatter_qkv("bench_qkv", g["q"], g["k"], g["v"], norm_rope=True, q_weight=wq, k_weight=wk,
+                            eps=w["eps"], theta=w["theta"], stream=stream)
+        ev[k][1].record(stream)
+        binding.gather_out("bench_out", g["attn"], stream=stream)
+        ev[k][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = binding.launch_count() - n_launch0
+    clocks = sampler.stop()
+    total_ms = start.elapsed_time(end)
+    scat_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    gath_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        dist.barrier()
+
+    sp, sx, gp = step_bytes(w)
+    ms_per_step = total_ms / K
+    value = world * (sp + gp) * K / (total_ms / 1e3) / 1e9
+    scat_avg = sum(scat_ms) / K
+    gath_avg = sum(gath_ms) / K
+    peak, peak_src = measured_peak()
+    achieved = (sp + sx) / (scat_avg / 1e3) / 1e9
+
+    # ---------------- end to end through the public API with host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        src = sets[0]
+        h_in = {key: [x.contiguous().cpu().pin_memory() for x in src[key]] for key in ("q", "k", "v", "attn")}
+        d_in = {key: [torch.empty_like(x, device=dev) for x in h_in[key]] for key in h_in}
+        tq, tk, tv, _ = binding.scatter_qkv("bench_e2e", d_in["q"], d_in["k"], d_in["v"], norm_rope=True,
+                                            q_weight=wq, k_weight=wk, eps=w["eps"], theta=w["theta"], stream=stream)
+        outs, _ = binding.gather_out("bench_e2e", d_in["attn"], stream=stream)
+        h_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (tq + tk + tv + outs)]
+        torch.cuda.synchronize(dev)
+        h2d = sum(x.numel() * x.element_size() for key in h_in for x in h_in[key])
+        d2h = sum(x.numel() * x.element_size() for x in h_out)
+
+        def e2e_step():
+            for key in h_in:
+                for dx, hx in zip(d_in[key], h_in[key]):
+                    dx.copy_(hx, non_blocking=True)
+            a, b_, c, _ = binding.scatter_qkv("bench_e2e", d_in["q"], d_in["k"], d_in["v"], norm_rope=True,
+                                              q_weight=wq, k_weight=wk, eps=w["eps"], theta=w["theta"],
+                                              stream=stream)
+            o, _ = binding.gather_out("bench_e2e", d_in["attn"], stream=stream)
+            for hx, dx in zip(h_out, a + b_ + c + o):
+                hx.copy_(dx, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * (sp + gp) * args.e2e_steps / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms / args.e2e_steps,
+               "note": "pinned host Q/K/V/attention inputs copied in, all targets and outputs copied out, "
+                       "every step; V uploaded contiguous"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        Sl_cpu = min(args.cpu_tokens, Sl)
+        t_cpu = oracle_step(w, Sl_cpu, seed=7)
+        sp_c, _, gp_c = step_bytes(w, S=P * Sl_cpu)
+        cpu = {"value": (sp_c + gp_c) / t_cpu / 1e9, "unit": "GB/s", "cores": cpu_cores_used(), "kind": "oracle",
+               "sample": f"one step at S_local={Sl_cpu} tokens per shard (of {Sl}), other sizes as the workload: "
+                         f"fused Q/K scatter, V scatter, cos/sin table, output gather; {t_cpu:.2f} s",
+               "host_cpu_count": os.cpu_count()}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w["name"], "P": P, "B": B, "S": S, "H": H, "D": D,
+                       "step": "fused Q/K/V scatter (RMSNorm+RoPE on Q/K, V strided view of a fused "
+                               "projection) into cached targets + head->sequence output gather",
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2: 2 rotating input sets of ~2 GB"},
+            "tokens_per_s": world * B * S * K / (total_ms / 1e3),
+            "pct_of_hbm_measured": 100.0 * value / world / peak,
+            "pct_of_hbm_nominal_8000": 100.0 * value / world / NOMINAL_HBM_GBS,
+            "kernels": {
+                "scatter_fused": {"ms": scat_avg, "GB/s": achieved, "bytes": sp + sx},
+                "gather": {"ms": gath_avg, "GB/s": gp / (gath_avg / 1e3) / 1e9, "bytes": gp},
+            },
+            "tolerance": {"relayout": "bit-exact", "fused_qk": "max-abs 1e-2 (bf16) / 2e-3 (fp16); an element "
+                          "above that must differ by exactly 1 ulp (checked by the -m gpu tests)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": profiled_traffic(), "peak_source": peak_src,
+                         "kernel": "relayout_kernel<scatter, bf16 fused, D=128> (one launch per step)"},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": clocks,
+            "gpu_launches": launches,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,52 @@
+"""Comparison helpers for the GPU parity tests (no method arithmetic here)."""
+from __future__ import annotations
+
+import torch
+
+# Tolerance of the fused RMSNorm + RoPE path: max-abs 1e-2 for bf16 and 2e-3 for
+# fp16; an element above it passes only if it differs from the oracle by exactly
+# one unit in the last place of the output type (an isolated rounding flip, the
+# classification of flashinfer PR #6332, "Assumptions / Tolerance").
+FUSED_ATOL = {torch.bfloat16: 1e-2, torch.float16: 2e-3}
+
+
+def ordered16(bits: torch.Tensor) -> torch.Tensor:
+    b = bits.to(torch.int32) & 0xFFFF
+    mag = b & 0x7FFF
+    return torch.where(b >= 0x8000, -mag, mag)
+
+
+def ulp_diff(a: torch.Tensor, b: torch.Tensor) -> torch.Tensor:
+    return (ordered16(a.view(torch.int16)) - ordered16(b.view(torch.int16))).abs()
+
+
+def bits_equal(a: torch.Tensor, b: torch.Tensor) -> bool:
+    if a.shape != b.shape:
+        return False
+    return torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8))
+
+
+def fused_compare(got: torch.Tensor, want: torch.Tensor) -> dict:
+    """Classify the differences of a fused (normalised + rotated) output."""
+    got, want = got.cpu(), want.cpu()
+    assert got.shape == want.shape and got.dtype == want.dtype
+    tol = FUSED_ATOL[got.dtype]
+    diff = (got.float() - want.float()).abs()
+    ulp = ulp_diff(got, want)
+    over = diff > tol
+    return dict(
+        n=got.numel(),
+        n_bit_diff=int((ulp > 0).sum()),
+        max_abs=float(diff.max()) if got.numel() else 0.0,
+        max_ulp=int(ulp.max()) if got.numel() else 0,
+        n_over_tol=int(over.sum()),
+        tol=tol,
+        ok=bool((ulp[over] == 1).all()),
+    )
+
+
+def assert_fused_ok(got, want, max_flip_fraction=1e-5):
+    st = fused_compare(got, want)
+    assert st["ok"], st
+    assert st["n_bit_diff"] <= max(2, int(st["n"] * max_flip_fraction)), st
+    return st

@@ -1,0 +1,298 @@
+"""Thin ctypes binding of ``libtf_ulysses.so`` (the C ABI in include/tf_ulysses.h).
+
+Argument marshalling only: torch supplies device memory, streams and the
+tensors' data pointers/strides; every step of the relayout runs in the
+library's CUDA kernels.  There is no fallback: if the library is missing or a
+call fails, a ``TfUlyssesError`` is raised.
+
+Names follow the C ABI: ``scatter_qkv`` / ``scatter_qkv_into`` / ``gather_out``
+/ ``rope_table`` / ``cache_clear`` ...
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtf_ulysses.so")
+
+TF_OK, TF_ERR_INVALID, TF_ERR_DIVISIBILITY, TF_ERR_ALIGNMENT = 0, 1, 2, 3
+TF_ERR_UNSUPPORTED, TF_ERR_OOM, TF_ERR_CUDA, TF_ERR_BUSY = 4, 5, 6, 7
+STATUS_NAMES = {0: "TF_OK", 1: "TF_ERR_INVALID", 2: "TF_ERR_DIVISIBILITY", 3: "TF_ERR_ALIGNMENT",
+                4: "TF_ERR_UNSUPPORTED", 5: "TF_ERR_OOM", 6: "TF_ERR_CUDA", 7: "TF_ERR_BUSY"}
+TF_MODE_SCATTER, TF_MODE_SCATTER_NORM_ROPE, TF_MODE_GATHER = 0, 1, 2
+MAX_SHARDS = 8
+CACHE_CAPACITY = 12
+
+_DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2, torch.int32: 2,
+               torch.uint8: 3, torch.int8: 3}
+for _name in ("float8_e4m3fn", "float8_e5m2"):
+    if hasattr(torch, _name):
+        _DTYPE_CODE[getattr(torch, _name)] = 3
+
+
+class TfUlyssesError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class Strides(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_int64), ("t", ctypes.c_int64), ("h", ctypes.c_int64)]
+
+
+class NormRope(ctypes.Structure):
+    _fields_ = [("q_weight", ctypes.c_void_p), ("k_weight", ctypes.c_void_p), ("eps", ctypes.c_float),
+                ("theta", ctypes.c_float), ("cos_sin", ctypes.c_void_p)]
+
+
+class Targets(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p * MAX_SHARDS), ("k", ctypes.c_void_p * MAX_SHARDS),
+                ("v", ctypes.c_void_p * MAX_SHARDS), ("done", ctypes.c_void_p)]
+
+
+ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p)
+FREE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p)
+
+_lock = threading.Lock()
+_lib = None
+
+
+def _declare(lib):
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    PP = ctypes.POINTER(ctypes.c_void_p)
+    lib.tf_ulysses_scatter_qkv.argtypes = [ctypes.c_char_p, PP, PP, PP, ctypes.POINTER(Strides),
+                                           i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(NormRope),
+                                           vp, ctypes.POINTER(Targets)]
+    lib.tf_ulysses_scatter_qkv_into.argtypes = [PP, PP, PP, ctypes.POINTER(Strides), i32, i32, i32, i32, i32,
+                                                i32, i32, ctypes.POINTER(NormRope), PP, PP, PP, vp]
+    lib.tf_ulysses_gather_out.argtypes = [ctypes.c_char_p, PP, ctypes.POINTER(Strides), i32, i32, i32, i32, i32,
+                                          i32, PP, ctypes.POINTER(Strides), vp, ctypes.POINTER(Targets)]
+    lib.tf_ulysses_rope_table.argtypes = [ctypes.c_float, i32, i32, vp, ctypes.POINTER(ctypes.c_void_p)]
+    for name in ("tf_ulysses_scatter_qkv", "tf_ulysses_scatter_qkv_into", "tf_ulysses_gather_out",
+                 "tf_ulysses_rope_table", "tf_ulysses_cache_clear"):
+        getattr(lib, name).restype = i32
+    lib.tf_ulysses_cache_clear.argtypes = []
+    lib.tf_ulysses_cache_entries.argtypes = []
+    lib.tf_ulysses_cache_entries.restype = i32
+    lib.tf_ulysses_set_allocator.argtypes = [ALLOC_FN, FREE_FN, vp]
+    lib.tf_ulysses_set_allocator.restype = None
+    lib.tf_ulysses_last_error.argtypes = []
+    lib.tf_ulysses_last_error.restype = ctypes.c_char_p
+    lib.tf_ulysses_launch_count.argtypes = []
+    lib.tf_ulysses_launch_count.restype = ctypes.c_uint64
+    lib.tf_ulysses_abi_version.argtypes = []
+    lib.tf_ulysses_abi_version.restype = i32
+    del i64
+    return lib
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise TfUlyssesError(TF_ERR_INVALID, f"{LIB_PATH} is not built (run __graft_entry__.build())")
+                _lib = _declare(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def _check(status: int):
+    if status != TF_OK:
+        raise TfUlyssesError(status, lib().tf_ulysses_last_error().decode(errors="replace"))
+
+
+# ---------------------------------------------------------------- marshalling
+def _ptr_array(ts):
+    if ts is None:
+        return None
+    return (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+
+
+def _strides_of(ts, ndim_names="[B, tokens, heads, D]"):
+    s = ts[0].stride()
+    if ts[0].dim() != 4:
+        raise ValueError(f"expected 4-d views {ndim_names}")
+    if ts[0].shape[-1] > 1 and s[3] != 1:
+        raise ValueError("the D dimension must have stride 1")
+    for t in ts[1:]:
+        if t.stride() != s or t.shape != ts[0].shape or t.dtype != ts[0].dtype:
+            raise ValueError("all shards of a tensor must share shape, dtype and strides")
+    return Strides(s[0], s[1], s[2])
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+class _DeviceBuffer:
+    """Zero-copy view of library-owned device memory for torch.as_tensor."""
+
+    def __init__(self, ptr, shape, typestr):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (ptr, False),
+                                         "version": 2, "strides": None}
+
+
+def _wrap(ptr, shape, dtype, device):
+    if not ptr or 0 in shape:
+        return torch.empty(shape, dtype=dtype, device=device)
+    esize = torch.empty((), dtype=dtype).element_size()
+    typestr = {1: "|u1", 2: "<i2", 4: "<i4", 8: "<i8"}[esize]
+    with torch.cuda.device(device):
+        t = torch.as_tensor(_DeviceBuffer(ptr, shape, typestr), device=device)
+    return t.view(dtype)
+
+
+def _dtype_code(dtype):
+    if dtype not in _DTYPE_CODE:
+        raise ValueError(f"unsupported dtype {dtype}")
+    return _DTYPE_CODE[dtype]
+
+
+def _norm_rope(q_weight, k_weight, eps, theta, cos_sin):
+    nr = NormRope()
+    nr.q_weight = q_weight.data_ptr() if q_weight is not None else None
+    nr.k_weight = k_weight.data_ptr() if k_weight is not None else None
+    nr.eps = float(eps)
+    nr.theta = float(theta)
+    nr.cos_sin = cos_sin.data_ptr() if cos_sin is not None else None
+    return nr
+
+
+def _scatter_args(q, k, v):
+    P = len(q)
+    if not 1 <= P <= MAX_SHARDS:
+        raise ValueError(f"P={P} outside [1, {MAX_SHARDS}]")
+    B, Sl, H, D = q[0].shape
+    strides = (Strides * 3)()
+    for i, ts in enumerate((q, k, v)):
+        if ts is None:
+            continue
+        if len(ts) != P or ts[0].shape != q[0].shape or ts[0].dtype != q[0].dtype:
+            raise ValueError("q, k and v must have P shards of the same shape and dtype")
+        strides[i] = _strides_of(ts)
+    return P, B, Sl, H, D, strides
+
+
+# ---------------------------------------------------------------- public API
+def scatter_qkv(tag, q, k=None, v=None, *, norm_rope=False, q_weight=None, k_weight=None, eps=1e-6,
+                theta=10000.0, cos_sin=None, stream=None):
+    """Sequence->head scatter of P shards ``[B, S_local, H, D]`` of Q (and K, V)
+    into cached final-layout targets, in one launch.
+
+    Returns ``(q_targets, k_targets, v_targets, done_event_handle)``: lists of P
+    ``[B, P*S_local, H/P, D]`` tensors viewing library-owned memory (valid until the
+    next call with the same key, eviction or ``cache_clear``), ``None`` for absent
+    tensors.  With ``norm_rope=True``, Q and K get RMSNorm (eps, q_weight/k_weight)
+    and interleaved RoPE at global positions (theta, or an fp32 ``cos_sin`` table
+    ``[>= S, D/2, 2]``); V is copied bit for bit.
+    """
+    P, B, Sl, H, D, strides = _scatter_args(q, k, v)
+    mode = TF_MODE_SCATTER_NORM_ROPE if norm_rope else TF_MODE_SCATTER
+    nr = _norm_rope(q_weight, k_weight, eps, theta, cos_sin) if norm_rope else None
+    out = Targets()
+    _check(lib().tf_ulysses_scatter_qkv(
+        tag.encode() if isinstance(tag, str) else tag, _ptr_array(q), _ptr_array(k), _ptr_array(v), strides,
+        P, B, Sl, H, D, _dtype_code(q[0].dtype), mode, ctypes.byref(nr) if nr is not None else None,
+        _stream_handle(stream), ctypes.byref(out)))
+    shape = (B, P * Sl, H // P, D)
+    dev = q[0].device
+    res = []
+    for arr, ts in ((out.q, q), (out.k, k), (out.v, v)):
+        res.append(None if ts is None else [_wrap(arr[g], shape, q[0].dtype, dev) for g in range(P)])
+    return res[0], res[1], res[2], out.done
+
+
+def scatter_qkv_into(q, k, v, q_out, k_out=None, v_out=None, *, norm_rope=False, q_weight=None, k_weight=None,
+                     eps=1e-6, theta=10000.0, cos_sin=None, stream=None):
+    """Same scatter into caller-owned contiguous targets ``[B, P*S_local, H/P, D]``."""
+    P, B, Sl, H, D, strides = _scatter_args(q, k, v)
+    for outs in (q_out, k_out, v_out):
+        if outs is not None and any(not o.is_contiguous() for o in outs):
+            raise ValueError("targets must be contiguous [B, S, H/P, D]")
+    mode = TF_MODE_SCATTER_NORM_ROPE if norm_rope else TF_MODE_SCATTER
+    nr = _norm_rope(q_weight, k_weight, eps, theta, cos_sin) if norm_rope else None
+    _check(lib().tf_ulysses_scatter_qkv_into(
+        _ptr_array(q), _ptr_array(k), _ptr_array(v), strides, P, B, Sl, H, D, _dtype_code(q[0].dtype), mode,
+        ctypes.byref(nr) if nr is not None else None, _ptr_array(q_out), _ptr_array(k_out), _ptr_array(v_out),
+        _stream_handle(stream)))
+    return q_out, k_out, v_out
+
+
+def gather_out(tag, attn, out=None, *, stream=None):
+    """Head->sequence gather of P head-group outputs ``[B, S, H/P, D]`` into P shard
+    outputs ``[B, S/P, H, D]`` -- cached library buffers, or ``out`` (P caller tensors,
+    any strides with unit D stride).  Returns ``(outputs, done_event_handle)``."""
+    P = len(attn)
+    B, S, Hl, D = attn[0].shape
+    if S % P:
+        raise ValueError(f"S={S} is not divisible by P={P}")
+    Sl, H = S // P, Hl * P
+    a_str = _strides_of(attn)
+    o_str = _strides_of(out) if out is not None else None
+    res = Targets()
+    _check(lib().tf_ulysses_gather_out(
+        tag.encode() if isinstance(tag, str) else tag, _ptr_array(attn), ctypes.byref(a_str), P, B, Sl, H, D,
+        _dtype_code(attn[0].dtype), _ptr_array(out), ctypes.byref(o_str) if o_str is not None else None,
+        _stream_handle(stream), ctypes.byref(res)))
+    if out is not None:
+        return list(out), res.done
+    return [_wrap(res.q[r], (B, Sl, H, D), attn[0].dtype, attn[0].device) for r in range(P)], res.done
+
+
+def rope_table(theta, S, D, *, stream=None, device=None):
+    """The library's resident fp32 cos/sin table ``[S, D/2, 2]`` (a view)."""
+    ptr = ctypes.c_void_p()
+    _check(lib().tf_ulysses_rope_table(float(theta), int(S), int(D), _stream_handle(stream), ctypes.byref(ptr)))
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    return _wrap(ptr.value, (S, D // 2, 2), torch.float32, dev)
+
+
+def cache_clear():
+    _check(lib().tf_ulysses_cache_clear())
+
+
+def cache_entries() -> int:
+    return lib().tf_ulysses_cache_entries()
+
+
+def launch_count() -> int:
+    return int(lib().tf_ulysses_launch_count())
+
+
+def abi_version() -> int:
+    return lib().tf_ulysses_abi_version()
+
+
+# torch-backed allocator: cached targets and tables come from torch's caching allocator
+_alloc_refs = None
+
+
+def _torch_alloc(nbytes, stream, ctx):
+    try:
+        return torch.cuda.caching_allocator_alloc(int(nbytes), stream=int(stream or 0))
+    except Exception:  # noqa: BLE001 -- the library reports TF_ERR_OOM
+        return None
+
+
+def _torch_free(ptr, nbytes, stream, ctx):
+    torch.cuda.caching_allocator_delete(ptr)
+
+
+def use_torch_allocator(enable: bool = True):
+    """Route the library's device allocations through torch's caching allocator
+    (default: cudaMallocAsync on the calling stream)."""
+    global _alloc_refs
+    if enable:
+        _alloc_refs = (ALLOC_FN(_torch_alloc), FREE_FN(_torch_free))
+        lib().tf_ulysses_set_allocator(_alloc_refs[0], _alloc_refs[1], None)
+    else:
+        lib().tf_ulysses_set_allocator(ALLOC_FN(), FREE_FN(), None)
+        _alloc_refs = None

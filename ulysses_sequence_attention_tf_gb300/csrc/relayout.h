@@ -1,0 +1,77 @@
+// relayout.h -- internal interface between the C-ABI host code and the CUDA kernels.
+// Not part of the public ABI (that is include/tf_ulysses.h).
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace tfu {
+
+constexpr int kMaxShards = 8;
+constexpr int kMaxSlots = 3;      // Q, K, V
+constexpr int kThreads = 256;     // threads per CTA
+constexpr int kChunkVecs = 2048;  // 16-byte vectors per work unit (32 KiB)
+
+// Unsigned 32-bit division by an invariant divisor as multiply-high, add and
+// shift (Granlund & Montgomery, "Division by invariant integers using
+// multiplication", PLDI 1994, section 4, figure 4.1).  Exact for every n < 2^32.
+struct FastDiv {
+    uint32_t d, m, s1, s2;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f{};
+    f.d = d;
+    uint32_t l = 0;
+    while ((uint64_t(1) << l) < d) ++l;  // l = ceil(log2 d)
+    uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1;
+    f.m = uint32_t(m);
+    f.s1 = l < 1 ? l : 1;
+    f.s2 = l > 1 ? l - 1 : 0;
+    return f;
+}
+
+__host__ __device__ inline uint32_t fastdiv(uint32_t n, const FastDiv& f) {
+#ifdef __CUDA_ARCH__
+    uint32_t t = __umulhi(n, f.m);
+#else
+    uint32_t t = uint32_t((uint64_t(n) * f.m) >> 32);
+#endif
+    return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+
+enum class Dir : int { kScatter = 0, kGather = 1 };
+enum class Fused : int { kNone = 0, kBF16 = 1, kFP16 = 2 };
+
+// One grouped launch.  A "slot" is one tensor (V, Q, K in that order when present);
+// a "plane" is one (batch b, shard r, slot x, head group g) block of
+// S_local * Hl * D elements; a "unit" is one 32 KiB chunk of a plane.
+struct RelayoutParams {
+    // scatter: src[x][r] = shard r, dst[x][g] = head-group target g
+    // gather:  src[x][g] = head-group buffer g, dst[x][r] = shard output r
+    const uint8_t* src[kMaxSlots][kMaxShards];
+    uint8_t* dst[kMaxSlots][kMaxShards];
+    int64_t s_b[kMaxSlots], s_t[kMaxSlots], s_h[kMaxSlots];  // byte strides
+    int64_t d_b[kMaxSlots], d_t[kMaxSlots], d_h[kMaxSlots];  // byte strides
+    const void* weight[kMaxSlots];  // per slot RMSNorm weight [D] (fused slots only)
+    const float* table;             // [>= P*S_local][D/2][2] fp32 (fused only)
+    float eps;
+    uint32_t fused_mask;  // bit x set: slot x gets RMSNorm + RoPE
+    uint32_t nx, P, B, Sl, Hl;
+    uint32_t vpr;       // 16-byte vectors per head row = D * esize / 16
+    uint32_t nv;        // vectors per plane = Sl * Hl * vpr
+    uint32_t n_planes;  // B * P * nx * P
+    uint32_t n_chunks;  // ceil(nv / kChunkVecs)
+    uint32_t n_units;   // n_chunks * n_planes
+    FastDiv div_vpr, div_hl, div_planes;
+};
+
+// Launch the relayout of every plane in `p`.  vpr_fused is the head row length
+// in vectors for the fused kernels (4, 8, 16 or 32); ignored otherwise.
+cudaError_t launch_relayout(const RelayoutParams& p, Dir dir, Fused fused, cudaStream_t stream);
+
+// Fill table[S][D/2][2] with (cos, sin) of p * inv_freq[i] evaluated in double.
+cudaError_t launch_rope_table(float* table, const double* inv_freq_host, int S, int D, cudaStream_t stream);
+
+}  // namespace tfu

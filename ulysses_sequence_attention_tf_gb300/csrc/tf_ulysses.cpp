@@ -1,0 +1,592 @@
+// tf_ulysses.cpp -- host side of the C ABI declared in include/tf_ulysses.h:
+// argument validation (all of it before any CUDA call), the tagged target cache,
+// the resident RoPE tables, the allocator hook and the launches.
+//
+// Sources: TeleFuser PR #27 "Add CUDA IPC Ulysses overlap and lossless LingBot
+// streaming", "Changes Made" (final-layout targets, up to 12 cached targets keyed
+// by tag, shape, dtype, mode and device, one grouped completion for tagged
+// Q/K/V) and "Additional Notes" (no protocol switch once a grouped transfer
+// started -- here: nothing is launched unless every check passed); TeleFuser PR
+// #22 (RoPE tables kept resident); TeleFuser docs "Communication Architecture",
+// "Cross-Worker Tensor Channel" (slot reuse ordered by an event, no device-wide
+// synchronisation) for how cache reuse and eviction are ordered.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "relayout.h"
+#include "tf_ulysses.h"
+
+namespace {
+
+using tfu::RelayoutParams;
+
+thread_local std::string g_last_error;
+std::atomic<uint64_t> g_launches{0};
+std::mutex g_mu;  // guards the cache, the tables and the allocator
+
+tf_status fail(tf_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+tf_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(TF_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------- allocator
+struct Allocator {
+    tf_alloc_fn alloc = nullptr;
+    tf_free_fn release = nullptr;
+    void* ctx = nullptr;
+};
+Allocator g_alloc;
+
+void* dev_alloc(const Allocator& a, size_t bytes, cudaStream_t s) {
+    if (bytes == 0) return nullptr;
+    if (a.alloc) return a.alloc(bytes, s, a.ctx);
+    void* p = nullptr;
+    if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return p;
+}
+
+// Release memory whose last use is `last_use` (an event recorded after it).
+void dev_release(const Allocator& a, void* ptr, size_t bytes, cudaEvent_t last_use, cudaStream_t s) {
+    if (!ptr) return;
+    if (a.release) {
+        if (last_use) cudaEventSynchronize(last_use);
+        a.release(ptr, bytes, s, a.ctx);
+    } else {
+        if (last_use) cudaStreamWaitEvent(s, last_use, 0);
+        cudaFreeAsync(ptr, s);
+    }
+}
+
+// ---------------------------------------------------------------- validation
+int elem_size(tf_dtype d) {
+    switch (d) {
+        case TF_FP16: return 2;
+        case TF_BF16: return 2;
+        case TF_FP32: return 4;
+        case TF_BYTE: return 1;
+    }
+    return 0;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Shape {
+    int P, B, Sl, H, D, Hl, esize;
+    tf_dtype dtype;
+};
+
+tf_status check_shape(int P, int B, int Sl, int H, int D, tf_dtype dtype, Shape* sh) {
+    if (P < 1 || P > TF_ULYSSES_MAX_SHARDS) return fail(TF_ERR_INVALID, "P=%d outside [1, %d]", P, TF_ULYSSES_MAX_SHARDS);
+    if (B < 0 || Sl < 0) return fail(TF_ERR_INVALID, "B=%d, S_local=%d must be >= 0", B, Sl);
+    if (H < 1 || D < 1) return fail(TF_ERR_INVALID, "H=%d, D=%d must be >= 1", H, D);
+    const int e = elem_size(dtype);
+    if (e == 0) return fail(TF_ERR_INVALID, "unknown dtype %d", int(dtype));
+    if (H % P != 0) return fail(TF_ERR_DIVISIBILITY, "H=%d is not divisible by P=%d", H, P);
+    if ((int64_t(D) * e) % 16 != 0)
+        return fail(TF_ERR_ALIGNMENT, "a head row (D=%d x %d B) must be a multiple of 16 bytes", D, e);
+    if (int64_t(P) * Sl > INT32_MAX) return fail(TF_ERR_UNSUPPORTED, "P*S_local too large");
+    *sh = Shape{P, B, Sl, H, D, H / P, e, dtype};
+    return TF_OK;
+}
+
+tf_status check_ptrs(const char* what, const void* const* a, int P) {
+    for (int i = 0; i < P; ++i) {
+        if (!a[i]) return fail(TF_ERR_INVALID, "%s[%d] is NULL", what, i);
+        if (!aligned16(a[i])) return fail(TF_ERR_ALIGNMENT, "%s[%d] is not 16-byte aligned", what, i);
+    }
+    return TF_OK;
+}
+
+// strides of a [nb, nt, nh, D] view; a stride of an extent-1 dimension is never used
+tf_status check_strides(const char* what, const tf_strides& s, int esize, int64_t nb, int64_t nt, int64_t nh) {
+    const int64_t v[3] = {s.b, s.t, s.h};
+    const int64_t n[3] = {nb, nt, nh};
+    const char* name[3] = {"b", "t", "h"};
+    for (int i = 0; i < 3; ++i) {
+        if (n[i] <= 1) continue;
+        if (v[i] < 0) return fail(TF_ERR_UNSUPPORTED, "%s stride %s=%lld is negative", what, name[i], (long long)v[i]);
+        if ((v[i] * esize) % 16 != 0)
+            return fail(TF_ERR_ALIGNMENT, "%s stride %s=%lld elements is not a multiple of 16 bytes", what, name[i],
+                        (long long)v[i]);
+    }
+    return TF_OK;
+}
+
+// Sizes of the unit grid; everything indexed in 32 bits must fit.
+tf_status plan_units(RelayoutParams& p, const Shape& sh) {
+    p.P = uint32_t(sh.P);
+    p.B = uint32_t(sh.B);
+    p.Sl = uint32_t(sh.Sl);
+    p.Hl = uint32_t(sh.Hl);
+    p.vpr = uint32_t(int64_t(sh.D) * sh.esize / 16);
+    const uint64_t nv = uint64_t(sh.Sl) * uint64_t(sh.Hl) * p.vpr;
+    if (nv > (uint64_t(1) << 31)) return fail(TF_ERR_UNSUPPORTED, "one shard/head-group block exceeds 2^31 vectors");
+    p.nv = uint32_t(nv);
+    const uint64_t planes = uint64_t(sh.B) * sh.P * p.nx * sh.P;
+    const uint64_t chunks = (nv + tfu::kChunkVecs - 1) / tfu::kChunkVecs;
+    if (planes * chunks >= (uint64_t(1) << 31)) return fail(TF_ERR_UNSUPPORTED, "problem exceeds 2^31 work units");
+    p.n_planes = uint32_t(planes);
+    p.n_chunks = uint32_t(chunks);
+    p.n_units = uint32_t(planes * chunks);
+    p.div_vpr = tfu::make_fastdiv(p.vpr);
+    p.div_hl = tfu::make_fastdiv(p.Hl);
+    p.div_planes = tfu::make_fastdiv(p.n_planes ? p.n_planes : 1);
+    return TF_OK;
+}
+
+// ---------------------------------------------------------------- RoPE tables
+constexpr int kMaxTables = 4;
+struct Table {
+    float theta = 0;
+    int S = 0, D = 0, device = -1;
+    float* ptr = nullptr;
+    size_t bytes = 0;
+    Allocator alloc;
+    cudaEvent_t last_use = nullptr;  // recorded after the build and after every launch that reads it
+    uint64_t stamp = 0;
+};
+std::vector<Table> g_tables;
+uint64_t g_clock = 0;
+
+// Caller holds g_mu.  Returns a table with >= S rows for (theta, D) on `device`,
+// ordered on `stream` after its build.
+tf_status get_table(float theta, int S, int D, int device, cudaStream_t stream, Table** out) {
+    for (auto& t : g_tables) {
+        if (t.device == device && t.D == D && t.S >= S && std::memcmp(&t.theta, &theta, sizeof theta) == 0) {
+            t.stamp = ++g_clock;
+            cudaError_t e = cudaStreamWaitEvent(stream, t.last_use, 0);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(table)");
+            *out = &t;
+            return TF_OK;
+        }
+    }
+    if (int(g_tables.size()) >= kMaxTables) {  // evict the least recently used table
+        size_t lru = 0;
+        for (size_t i = 1; i < g_tables.size(); ++i)
+            if (g_tables[i].stamp < g_tables[lru].stamp) lru = i;
+        Table& t = g_tables[lru];
+        dev_release(t.alloc, t.ptr, t.bytes, t.last_use, stream);
+        cudaEventDestroy(t.last_use);
+        g_tables.erase(g_tables.begin() + lru);
+    }
+    Table t;
+    t.theta = theta;
+    t.S = S;
+    t.D = D;
+    t.device = device;
+    t.bytes = size_t(S) * size_t(D) * sizeof(float);
+    t.alloc = g_alloc;
+    t.ptr = static_cast<float*>(dev_alloc(t.alloc, t.bytes, stream));
+    if (t.bytes && !t.ptr) return fail(TF_ERR_OOM, "allocating a %zu-byte RoPE table failed", t.bytes);
+    cudaError_t e = cudaEventCreateWithFlags(&t.last_use, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        dev_release(t.alloc, t.ptr, t.bytes, nullptr, stream);
+        return cuda_fail(e, "cudaEventCreate");
+    }
+    // frequencies of the interleaved pairs, theta^(-2i/D), in double on the host
+    std::vector<double> inv_freq(size_t(D / 2));
+    for (int i = 0; i < D / 2; ++i) inv_freq[size_t(i)] = std::pow(double(theta), -2.0 * i / D);
+    e = tfu::launch_rope_table(t.ptr, inv_freq.data(), S, D, stream);
+    if (e == cudaSuccess && S > 0) g_launches.fetch_add(1);
+    if (e == cudaSuccess) e = cudaEventRecord(t.last_use, stream);
+    if (e != cudaSuccess) {
+        dev_release(t.alloc, t.ptr, t.bytes, nullptr, stream);
+        cudaEventDestroy(t.last_use);
+        return cuda_fail(e, "building the RoPE table");
+    }
+    t.stamp = ++g_clock;
+    g_tables.push_back(t);
+    *out = &g_tables.back();
+    return TF_OK;
+}
+
+// ---------------------------------------------------------------- target cache
+struct Entry {
+    std::string tag;
+    int mode = 0, present = 0, P = 0, B = 0, Sl = 0, H = 0, D = 0, dtype = 0, device = -1;
+    void* slab = nullptr;
+    size_t bytes = 0;
+    Allocator alloc;
+    void* buf[3][TF_ULYSSES_MAX_SHARDS] = {};
+    cudaEvent_t done = nullptr;
+    cudaStream_t last_stream = nullptr;
+    uint64_t stamp = 0;
+};
+std::vector<Entry> g_entries;
+
+void reclaim_entry(Entry& e, cudaStream_t stream) {
+    dev_release(e.alloc, e.slab, e.bytes, e.done, stream);
+    if (e.done) cudaEventDestroy(e.done);
+    e.slab = nullptr;
+    e.done = nullptr;
+}
+
+size_t round_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
+
+// Caller holds g_mu.  buffer_bytes: size of one target; counts[x]: buffers of tensor x.
+tf_status get_entry(const std::string& tag, int mode, int present, const Shape& sh, int device, size_t buffer_bytes,
+                    const int counts[3], cudaStream_t stream, Entry** out) {
+    for (auto& e : g_entries) {
+        if (e.tag == tag && e.mode == mode && e.present == present && e.P == sh.P && e.B == sh.B && e.Sl == sh.Sl &&
+            e.H == sh.H && e.D == sh.D && e.dtype == int(sh.dtype) && e.device == device) {
+            if (e.last_stream != stream) {  // order the rewrite after the previous one
+                cudaError_t err = cudaStreamWaitEvent(stream, e.done, 0);
+                if (err != cudaSuccess) return cuda_fail(err, "cudaStreamWaitEvent(entry)");
+            }
+            e.stamp = ++g_clock;
+            *out = &e;
+            return TF_OK;
+        }
+    }
+    if (int(g_entries.size()) >= TF_ULYSSES_CACHE_CAPACITY) {
+        size_t lru = 0;
+        for (size_t i = 1; i < g_entries.size(); ++i)
+            if (g_entries[i].stamp < g_entries[lru].stamp) lru = i;
+        reclaim_entry(g_entries[lru], stream);
+        g_entries.erase(g_entries.begin() + lru);
+    }
+    Entry e;
+    e.tag = tag;
+    e.mode = mode;
+    e.present = present;
+    e.P = sh.P;
+    e.B = sh.B;
+    e.Sl = sh.Sl;
+    e.H = sh.H;
+    e.D = sh.D;
+    e.dtype = int(sh.dtype);
+    e.device = device;
+    e.alloc = g_alloc;
+    const size_t stride = round_up(buffer_bytes, 256);
+    e.bytes = stride * size_t(counts[0] + counts[1] + counts[2]);
+    e.slab = dev_alloc(e.alloc, e.bytes, stream);
+    if (e.bytes && !e.slab) return fail(TF_ERR_OOM, "allocating %zu bytes of targets failed", e.bytes);
+    size_t off = 0;
+    for (int x = 0; x < 3; ++x)
+        for (int i = 0; i < counts[x]; ++i, off += stride)
+            e.buf[x][i] = buffer_bytes ? static_cast<uint8_t*>(e.slab) + off : nullptr;
+    cudaError_t err = cudaEventCreateWithFlags(&e.done, cudaEventDisableTiming);
+    if (err != cudaSuccess) {
+        dev_release(e.alloc, e.slab, e.bytes, nullptr, stream);
+        return cuda_fail(err, "cudaEventCreate");
+    }
+    e.last_stream = stream;
+    e.stamp = ++g_clock;
+    g_entries.push_back(e);
+    *out = &g_entries.back();
+    return TF_OK;
+}
+
+// ---------------------------------------------------------------- scatter core
+struct ScatterPlan {
+    Shape sh;
+    RelayoutParams p{};
+    tfu::Fused fused = tfu::Fused::kNone;
+    int slot_of[3] = {-1, -1, -1};  // tensor (q=0, k=1, v=2) -> slot
+    int present = 0;                // bit per tensor
+    bool empty = false;
+};
+
+tf_status plan_scatter(const void* const* q, const void* const* k, const void* const* v, const tf_strides* strides,
+                       int P, int B, int Sl, int H, int D, tf_dtype dtype, tf_mode mode, const tf_norm_rope* nr,
+                       ScatterPlan* plan) {
+    ScatterPlan& pl = *plan;
+    tf_status s = check_shape(P, B, Sl, H, D, dtype, &pl.sh);
+    if (s != TF_OK) return s;
+    if (mode != TF_MODE_SCATTER && mode != TF_MODE_SCATTER_NORM_ROPE)
+        return fail(TF_ERR_INVALID, "mode %d is not a scatter mode", int(mode));
+    if (!q) return fail(TF_ERR_INVALID, "q is NULL");
+    if (!strides) return fail(TF_ERR_INVALID, "strides is NULL");
+    const void* const* src[3] = {q, k, v};
+    const char* names[3] = {"q", "k", "v"};
+    for (int x = 0; x < 3; ++x) {
+        if (!src[x]) continue;
+        pl.present |= 1 << x;
+        if (B > 0 && Sl > 0 && (s = check_ptrs(names[x], src[x], P)) != TF_OK) return s;
+        if ((s = check_strides(names[x], strides[x], pl.sh.esize, B, Sl, H)) != TF_OK) return s;
+    }
+    if (mode == TF_MODE_SCATTER_NORM_ROPE) {
+        if (dtype != TF_FP16 && dtype != TF_BF16)
+            return fail(TF_ERR_UNSUPPORTED, "the fused mode needs fp16 or bf16 (dtype %d)", int(dtype));
+        if (D != 32 && D != 64 && D != 128 && D != 256)
+            return fail(TF_ERR_UNSUPPORTED, "the fused mode is built for D in {32, 64, 128, 256}, not %d", D);
+        if (!nr) return fail(TF_ERR_INVALID, "the fused mode needs norm/rope parameters");
+        if (!nr->q_weight || !aligned16(nr->q_weight)) return fail(TF_ERR_ALIGNMENT, "q_weight NULL or misaligned");
+        if (k && (!nr->k_weight || !aligned16(nr->k_weight)))
+            return fail(TF_ERR_ALIGNMENT, "k_weight NULL or misaligned");
+        if (!std::isfinite(nr->eps) || nr->eps < 0) return fail(TF_ERR_INVALID, "eps must be finite and >= 0");
+        if (nr->cos_sin) {
+            if (!aligned16(nr->cos_sin)) return fail(TF_ERR_ALIGNMENT, "cos_sin is not 16-byte aligned");
+        } else if (!std::isfinite(nr->theta) || nr->theta <= 0) {
+            return fail(TF_ERR_INVALID, "theta must be finite and > 0");
+        }
+        pl.fused = dtype == TF_BF16 ? tfu::Fused::kBF16 : tfu::Fused::kFP16;
+    }
+    // slots in launch order: V first, then Q, then K
+    RelayoutParams& p = pl.p;
+    const int order[3] = {2, 0, 1};
+    uint32_t nx = 0;
+    for (int j = 0; j < 3; ++j) {
+        const int x = order[j];
+        if (!src[x]) continue;
+        const int slot = int(nx++);
+        pl.slot_of[x] = slot;
+        for (int r = 0; r < P; ++r) p.src[slot][r] = static_cast<const uint8_t*>(src[x][r]);
+        p.s_b[slot] = strides[x].b * pl.sh.esize;
+        p.s_t[slot] = strides[x].t * pl.sh.esize;
+        p.s_h[slot] = strides[x].h * pl.sh.esize;
+        const int64_t rowb = int64_t(D) * pl.sh.esize;  // targets: contiguous [B, S, Hl, D]
+        p.d_h[slot] = rowb;
+        p.d_t[slot] = rowb * pl.sh.Hl;
+        p.d_b[slot] = rowb * pl.sh.Hl * int64_t(P) * Sl;
+        if (mode == TF_MODE_SCATTER_NORM_ROPE && x != 2) {
+            p.fused_mask |= 1u << slot;
+            p.weight[slot] = x == 0 ? nr->q_weight : nr->k_weight;
+        }
+    }
+    p.nx = nx;
+    p.eps = nr ? nr->eps : 0.f;
+    p.table = nr ? nr->cos_sin : nullptr;
+    if ((s = plan_units(p, pl.sh)) != TF_OK) return s;
+    pl.empty = B == 0 || Sl == 0;
+    return TF_OK;
+}
+
+// Caller holds g_mu when the plan needs a library table.
+tf_status launch_scatter(ScatterPlan& pl, const tf_norm_rope* nr, int device, cudaStream_t stream, Table** used) {
+    *used = nullptr;
+    if (pl.empty) return TF_OK;
+    if (pl.fused != tfu::Fused::kNone && !nr->cos_sin) {
+        Table* t = nullptr;
+        tf_status s = get_table(nr->theta, pl.sh.P * pl.sh.Sl, pl.sh.D, device, stream, &t);
+        if (s != TF_OK) return s;
+        pl.p.table = t->ptr;
+        *used = t;
+    }
+    cudaError_t e = tfu::launch_relayout(pl.p, tfu::Dir::kScatter, pl.fused, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the scatter kernel");
+    g_launches.fetch_add(1);
+    if (*used) cudaEventRecord((*used)->last_use, stream);
+    return TF_OK;
+}
+
+tf_status current_device(int* dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    return TF_OK;
+}
+
+tf_status check_tag(const char* tag, std::string* out) {
+    if (!tag) tag = "";
+    const size_t n = strnlen(tag, 64);
+    if (n > 63) return fail(TF_ERR_INVALID, "tag longer than 63 bytes");
+    out->assign(tag, n);
+    return TF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+TF_API tf_status tf_ulysses_scatter_qkv(const char* tag, const void* const* q, const void* const* k,
+                                        const void* const* v, const tf_strides* strides, int P, int B, int S_local,
+                                        int H, int D, tf_dtype dtype, tf_mode mode, const tf_norm_rope* nr,
+                                        void* stream, tf_targets* out) {
+    std::string key;
+    tf_status s = check_tag(tag, &key);
+    if (s != TF_OK) return s;
+    if (!out) return fail(TF_ERR_INVALID, "out is NULL");
+    ScatterPlan pl;
+    if ((s = plan_scatter(q, k, v, strides, P, B, S_local, H, D, dtype, mode, nr, &pl)) != TF_OK) return s;
+    int device = 0;
+    if ((s = current_device(&device)) != TF_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    const size_t target_bytes = size_t(B) * size_t(P) * size_t(S_local) * size_t(pl.sh.Hl) * size_t(D) * pl.sh.esize;
+    int counts[3] = {0, 0, 0};
+    for (int x = 0; x < 3; ++x)
+        if (pl.present & (1 << x)) counts[x] = P;
+    Entry* e = nullptr;
+    if ((s = get_entry(key, int(mode), pl.present, pl.sh, device, target_bytes, counts, st, &e)) != TF_OK) return s;
+    for (int x = 0; x < 3; ++x) {
+        const int slot = pl.slot_of[x];
+        if (slot < 0) continue;
+        for (int g = 0; g < P; ++g) pl.p.dst[slot][g] = static_cast<uint8_t*>(e->buf[x][g]);
+    }
+    Table* used = nullptr;
+    if ((s = launch_scatter(pl, nr, device, st, &used)) != TF_OK) return s;
+    cudaError_t err = cudaEventRecord(e->done, st);
+    if (err != cudaSuccess) return cuda_fail(err, "cudaEventRecord");
+    e->last_stream = st;
+    std::memset(out, 0, sizeof *out);
+    for (int g = 0; g < P; ++g) {
+        out->q[g] = e->buf[0][g];
+        out->k[g] = e->buf[1][g];
+        out->v[g] = e->buf[2][g];
+    }
+    out->done = e->done;
+    return TF_OK;
+}
+
+TF_API tf_status tf_ulysses_scatter_qkv_into(const void* const* q, const void* const* k, const void* const* v,
+                                             const tf_strides* strides, int P, int B, int S_local, int H, int D,
+                                             tf_dtype dtype, tf_mode mode, const tf_norm_rope* nr,
+                                             void* const* q_out, void* const* k_out, void* const* v_out,
+                                             void* stream) {
+    ScatterPlan pl;
+    tf_status s = plan_scatter(q, k, v, strides, P, B, S_local, H, D, dtype, mode, nr, &pl);
+    if (s != TF_OK) return s;
+    void* const* dsts[3] = {q_out, k_out, v_out};
+    const char* names[3] = {"q_out", "k_out", "v_out"};
+    for (int x = 0; x < 3; ++x) {
+        if (!(pl.present & (1 << x))) continue;
+        if (!dsts[x]) return fail(TF_ERR_INVALID, "%s is NULL for a present source", names[x]);
+        if (!pl.empty && (s = check_ptrs(names[x], dsts[x], P)) != TF_OK) return s;
+        for (int g = 0; g < P; ++g) pl.p.dst[pl.slot_of[x]][g] = static_cast<uint8_t*>(dsts[x][g]);
+    }
+    int device = 0;
+    if ((s = current_device(&device)) != TF_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Table* used = nullptr;
+    if (pl.fused != tfu::Fused::kNone && !nr->cos_sin) {  // the resident table lives under the lock
+        std::lock_guard<std::mutex> lock(g_mu);
+        return launch_scatter(pl, nr, device, st, &used);
+    }
+    return launch_scatter(pl, nr, device, st, &used);
+}
+
+TF_API tf_status tf_ulysses_gather_out(const char* tag, const void* const* attn, const tf_strides* attn_strides,
+                                       int P, int B, int S_local, int H, int D, tf_dtype dtype, void* const* dst,
+                                       const tf_strides* dst_strides, void* stream, tf_targets* out) {
+    std::string key;
+    tf_status s = check_tag(tag, &key);
+    if (s != TF_OK) return s;
+    if (!out) return fail(TF_ERR_INVALID, "out is NULL");
+    Shape sh;
+    if ((s = check_shape(P, B, S_local, H, D, dtype, &sh)) != TF_OK) return s;
+    if (!attn) return fail(TF_ERR_INVALID, "attn is NULL");
+    const bool empty = B == 0 || S_local == 0;  // nothing is dereferenced then
+    if (!empty && (s = check_ptrs("attn", attn, P)) != TF_OK) return s;
+    const int64_t S = int64_t(P) * S_local;
+    const tf_strides a_def{S * sh.Hl * D, int64_t(sh.Hl) * D, D};
+    const tf_strides o_def{int64_t(S_local) * H * D, int64_t(H) * D, D};
+    const tf_strides as = attn_strides ? *attn_strides : a_def;
+    const tf_strides os = dst_strides ? *dst_strides : o_def;
+    if ((s = check_strides("attn", as, sh.esize, B, S, sh.Hl)) != TF_OK) return s;
+    if (dst) {
+        if (!empty && (s = check_ptrs("dst", dst, P)) != TF_OK) return s;
+        if ((s = check_strides("dst", os, sh.esize, B, S_local, H)) != TF_OK) return s;
+    }
+    RelayoutParams p{};
+    p.nx = 1;
+    for (int g = 0; g < P; ++g) p.src[0][g] = static_cast<const uint8_t*>(attn[g]);
+    p.s_b[0] = as.b * sh.esize;
+    p.s_t[0] = as.t * sh.esize;
+    p.s_h[0] = as.h * sh.esize;
+    p.d_b[0] = os.b * sh.esize;
+    p.d_t[0] = os.t * sh.esize;
+    p.d_h[0] = os.h * sh.esize;
+    if ((s = plan_units(p, sh)) != TF_OK) return s;
+    int device = 0;
+    if ((s = current_device(&device)) != TF_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    const size_t out_bytes = size_t(B) * size_t(S_local) * size_t(H) * size_t(D) * sh.esize;
+    int counts[3] = {dst ? 0 : P, 0, 0};
+    Entry* e = nullptr;
+    const int present = dst ? 0 : 1;  // caller-owned outputs and cached outputs are different keys
+    if ((s = get_entry(key, int(TF_MODE_GATHER), present, sh, device, dst ? 0 : out_bytes, counts, st, &e)) != TF_OK)
+        return s;
+    for (int r = 0; r < P; ++r) p.dst[0][r] = static_cast<uint8_t*>(dst ? dst[r] : e->buf[0][r]);
+    if (!empty) {
+        cudaError_t err = tfu::launch_relayout(p, tfu::Dir::kGather, tfu::Fused::kNone, st);
+        if (err != cudaSuccess) return cuda_fail(err, "launching the gather kernel");
+        g_launches.fetch_add(1);
+    }
+    cudaError_t err = cudaEventRecord(e->done, st);
+    if (err != cudaSuccess) return cuda_fail(err, "cudaEventRecord");
+    e->last_stream = st;
+    std::memset(out, 0, sizeof *out);
+    for (int r = 0; r < P; ++r) out->q[r] = p.dst[0][r];
+    if (empty)
+        for (int r = 0; r < P; ++r) out->q[r] = dst ? dst[r] : nullptr;
+    out->done = e->done;
+    return TF_OK;
+}
+
+TF_API tf_status tf_ulysses_rope_table(float theta, int S, int D, void* stream, const float** table) {
+    if (!table) return fail(TF_ERR_INVALID, "table is NULL");
+    if (S < 0) return fail(TF_ERR_INVALID, "S must be >= 0");
+    if (D < 2 || D > 256 || D % 2) return fail(TF_ERR_UNSUPPORTED, "D must be even and in [2, 256]");
+    if (!std::isfinite(theta) || theta <= 0) return fail(TF_ERR_INVALID, "theta must be finite and > 0");
+    int device = 0;
+    tf_status s = current_device(&device);
+    if (s != TF_OK) return s;
+    std::lock_guard<std::mutex> lock(g_mu);
+    Table* t = nullptr;
+    if ((s = get_table(theta, S, D, device, static_cast<cudaStream_t>(stream), &t)) != TF_OK) return s;
+    *table = t->ptr;
+    return TF_OK;
+}
+
+TF_API tf_status tf_ulysses_cache_clear(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_entries.empty() && g_tables.empty()) return TF_OK;
+    for (auto& e : g_entries) {
+        if (e.done) cudaEventSynchronize(e.done);
+        reclaim_entry(e, nullptr);
+    }
+    g_entries.clear();
+    for (auto& t : g_tables) {
+        dev_release(t.alloc, t.ptr, t.bytes, t.last_use, nullptr);
+        if (t.last_use) cudaEventDestroy(t.last_use);
+    }
+    g_tables.clear();
+    cudaError_t e = cudaStreamSynchronize(nullptr);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    return TF_OK;
+}
+
+TF_API int tf_ulysses_cache_entries(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    return int(g_entries.size());
+}
+
+TF_API void tf_ulysses_set_allocator(tf_alloc_fn alloc, tf_free_fn release, void* ctx) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (alloc && release) {
+        g_alloc = Allocator{alloc, release, ctx};
+    } else {
+        g_alloc = Allocator{};
+    }
+}
+
+TF_API const char* tf_ulysses_last_error(void) { return g_last_error.c_str(); }
+
+TF_API uint64_t tf_ulysses_launch_count(void) { return g_launches.load(); }
+
+TF_API int tf_ulysses_abi_version(void) { return TF_ULYSSES_ABI_VERSION; }
+
+}  // extern "C"

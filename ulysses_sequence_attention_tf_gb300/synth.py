@@ -123,3 +123,26 @@ def unique_id_shards(P, B, S_local, H, D, *, device="cpu"):
         raise ValueError("too many elements for distinct 16-bit ids")
     ids = torch.arange(P * n, dtype=torch.int32, device=device) - 32768
     return [ids[r * n:(r + 1) * n].to(torch.int16).view(B, S_local, H, D).clone() for r in range(P)]
+
+
+def move(d, device):
+    """Copy a ``qkv_shards`` result to ``device`` keeping every view's strides
+    (views into a fused projection stay views into the copied projection)."""
+    backing = [b.to(device) for b in d["backing"]]
+    ptrs = [b.data_ptr() for b in d["backing"]]
+    out = {"backing": backing}
+    for key in ("q", "k", "v"):
+        if d[key] is None:
+            out[key] = None
+            continue
+        res = []
+        for x in d[key]:
+            base = x._base
+            if base is None or base.data_ptr() not in ptrs:
+                res.append(x.to(device))
+                continue
+            i = ptrs.index(base.data_ptr())
+            off = x.storage_offset() - base.storage_offset()
+            res.append(backing[i].as_strided(x.shape, x.stride(), backing[i].storage_offset() + off))
+        out[key] = res
+    return out
