@@ -40,18 +40,23 @@ def _stale() -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile the library if it is missing or older than its sources."""
-    if not force and not _stale():
+def build(force: bool = False, verbose: bool = False, defines=(), out: str | None = None) -> str:
+    """Compile the library if it is missing or older than its sources.
+
+    ``defines``: extra ``-D`` macros (tuning constants); ``out``: library path
+    (default: the in-tree ``libtf_ulysses.so``)."""
+    lib = out or LIB
+    if not force and not defines and out is None and not _stale():
         return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    build_dir = BUILD_DIR if out is None else os.path.join(os.path.dirname(lib), "_obj")
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src + ".o")
+        obj = os.path.join(build_dir, src + ".o")
         objs.append(obj)
-        cmd = [cc, *ARCH, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [cc, *ARCH, *NVCC_FLAGS, *[f"-D{d}" for d in defines], "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
@@ -64,10 +69,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
             failed.append(" ".join(cmd))
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -10,8 +10,9 @@ namespace tfu {
 
 constexpr int kMaxShards = 8;
 constexpr int kMaxSlots = 3;      // Q, K, V
-constexpr int kThreads = 256;     // threads per CTA
-constexpr int kChunkVecs = 2048;  // 16-byte vectors per work unit (32 KiB)
+constexpr int kThreads = 256;          // threads per CTA
+constexpr int kChunkBytes = 32768;     // payload bytes per work unit
+__host__ __device__ constexpr int chunk_vecs(int vec_bytes) { return kChunkBytes / vec_bytes; }
 
 // Unsigned 32-bit division by an invariant divisor as multiply-high, add and
 // shift (Granlund & Montgomery, "Division by invariant integers using
@@ -59,16 +60,18 @@ struct RelayoutParams {
     float eps;
     uint32_t fused_mask;  // bit x set: slot x gets RMSNorm + RoPE
     uint32_t nx, P, B, Sl, Hl;
-    uint32_t vpr;       // 16-byte vectors per head row = D * esize / 16
-    uint32_t nv;        // vectors per plane = Sl * Hl * vpr
-    uint32_t n_planes;  // B * P * nx * P
-    uint32_t n_chunks;  // ceil(nv / kChunkVecs)
+    uint32_t vec_bytes;  // bytes each lane moves per access: 32, or 16 when rows/strides/bases are
+                         // only 16-byte aligned
+    uint32_t vpr;        // vectors per head row = D * esize / vec_bytes
+    uint32_t nv;         // vectors per plane = Sl * Hl * vpr
+    uint32_t n_planes;   // B * P * nx * P
+    uint32_t n_chunks;   // ceil(nv / chunk_vecs(vec_bytes))
     uint32_t n_units;   // n_chunks * n_planes
     FastDiv div_vpr, div_hl, div_planes;
 };
 
-// Launch the relayout of every plane in `p`.  vpr_fused is the head row length
-// in vectors for the fused kernels (4, 8, 16 or 32); ignored otherwise.
+// Launch the relayout of every plane in `p` (vector width p.vec_bytes; for the
+// fused kernels the head row holds p.vpr vectors, D in {32, 64, 128, 256}).
 cudaError_t launch_relayout(const RelayoutParams& p, Dir dir, Fused fused, cudaStream_t stream);
 
 // Fill table[S][D/2][2] with (cos, sin) of p * inv_freq[i] evaluated in double.

@@ -9,23 +9,25 @@
 // fused mode the per-head RMSNorm + interleaved RoPE of flashinfer PR #6332,
 // "Assumptions / Operator math" (see tf_ulysses.h for the formula).
 //
-// Design (HBM-bound data movement, no tensor cores):
-//  * One grouped launch per call.  Work is split into units of 32 KiB (2048
-//    16-byte vectors) of one plane = (batch b, shard r, tensor slot x, head group
-//    g).  Units are ordered chunk-major with g innermost, so CTAs that run at the
-//    same time read whole source token rows (all head groups) and the P head
-//    groups of one token block -- and, in the fused mode, reuse the same RoPE
-//    table rows from L2.  V (slot 0) comes first within each token block.
-//  * A persistent grid (SM count x resident CTAs) walks the units; each thread
-//    issues 8 (copy) or 4 (fused) independent 16-byte loads before any store,
-//    keeping ~64 KiB+ in flight per SM.  Loads bypass L1 (read-once data);
-//    stores are streaming (evict-first) since targets are not re-read here.
-//  * Fused rows: D/8 consecutive lanes hold one head row (8 elements each).
-//    The sum of squares is accumulated as an unevaluated float pair (TwoSum,
-//    Knuth, TAOCP vol. 2, 4.2.2) and reduced with xor-shuffles, so the fp32 mean
-//    is the correctly rounded mean for ordinary inputs; all other steps use
-//    IEEE-rounded fp32 intrinsics with no contraction, so results match a
-//    step-by-step fp32 evaluation bit for bit.
+// Design (HBM-bound data movement plus light fp32 math; no tensor cores):
+//  * One grouped launch per call.  Work is split into units of 32 KiB of one
+//    plane = (batch b, shard r, tensor slot x, head group g).  Units are ordered
+//    chunk-major with g innermost, so CTAs running at the same time read whole
+//    source token rows (all head groups), write the P head groups of one token
+//    block, and in the fused mode share the same RoPE table rows through L2.
+//    V (slot 0) comes first within each token block.
+//  * A persistent grid (SM count x resident CTAs) walks the units.  Each lane
+//    moves 32-byte vectors (16-byte when rows, strides or bases are only 16-byte
+//    aligned) and issues all of its loads of a batch before any store.  Loads
+//    skip L1 allocation (read once); stores are evict-first (not re-read here).
+//  * Fused rows: a head row of D 16-bit values is spread over D*2/VW consecutive
+//    lanes.  The sum of squares is carried as an unevaluated float pair (TwoSum)
+//    through the lane and an xor-shuffle tree, so the fp32 mean is the correctly
+//    rounded mean for ordinary inputs; then 1/sqrt(ms + eps) with IEEE-rounded
+//    sqrt and reciprocal, the product rounded to the 16-bit type, the weight
+//    scale as a packed 16-bit multiply (exactly the rounded product), and the
+//    rotation with separately rounded fp32 products (no contraction), as a
+//    step-by-step fp32 evaluation does.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -34,17 +36,45 @@
 namespace tfu {
 namespace {
 
-__device__ __forceinline__ uint4 ld_stream(const uint8_t* p) {
-    uint4 v;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p));
+// ---------------------------------------------------------------- vectors
+template <int VW>
+struct Vec;
+template <>
+struct Vec<16> {
+    uint32_t w[4];
+};
+template <>
+struct Vec<32> {
+    uint32_t w[8];
+};
+
+template <int VW>
+__device__ __forceinline__ Vec<VW> ld_stream(const uint8_t* p) {
+    Vec<VW> v;
+    if constexpr (VW == 16) {
+        asm("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
+            : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+            : "l"(p));
+    } else {
+        asm("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+            : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]),
+              "=r"(v.w[7])
+            : "l"(p));
+    }
     return v;
 }
 
-__device__ __forceinline__ void st_stream(uint8_t* p, const uint4& v) {
-    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
+template <int VW>
+__device__ __forceinline__ void st_stream(uint8_t* p, const Vec<VW>& v) {
+    if constexpr (VW == 16) {
+        asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]),
+                     "r"(v.w[3])
+                     : "memory");
+    } else {
+        asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v.w[0]),
+                     "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
+                     : "memory");
+    }
 }
 
 __device__ __forceinline__ float4 ld_table(const float* p) {
@@ -53,6 +83,7 @@ __device__ __forceinline__ float4 ld_table(const float* p) {
     return v;
 }
 
+// ---------------------------------------------------------------- planes
 struct Plane {
     const uint8_t* src;
     uint8_t* dst;
@@ -89,43 +120,44 @@ __device__ __forceinline__ Plane decode_plane(const RelayoutParams& p, uint32_t 
 }
 
 // vector v of a plane -> (token t, head h, vector-in-row dv) -> byte offset
+template <int VW>
 __device__ __forceinline__ int64_t vec_offset(const RelayoutParams& p, uint32_t v, int64_t st, int64_t sh) {
     const uint32_t row = fastdiv(v, p.div_vpr);
     const uint32_t dv = v - row * p.vpr;
     const uint32_t t = fastdiv(row, p.div_hl);
     const uint32_t h = row - t * p.Hl;
-    return int64_t(t) * st + int64_t(h) * sh + int64_t(dv) * 16;
+    return int64_t(t) * st + int64_t(h) * sh + int64_t(dv) * VW;
 }
 
-// Scatter targets are contiguous [B, S, Hl, D]: vector v of a plane lands at v * 16.
-template <Dir kDir>
+// Scatter targets are contiguous [B, S, Hl, D]: vector v of a plane lands at v * VW.
+template <Dir kDir, int VW>
 __device__ __forceinline__ int64_t dst_offset(const RelayoutParams& p, const Plane& pl, uint32_t v) {
     if constexpr (kDir == Dir::kScatter) {
-        return int64_t(v) * 16;
+        return int64_t(v) * VW;
     } else {
-        return vec_offset(p, v, pl.dt, pl.dh);
+        return vec_offset<VW>(p, v, pl.dt, pl.dh);
     }
 }
 
-template <Dir kDir, int VB>
+template <Dir kDir, int VW, int VB>
 __device__ __forceinline__ void copy_range(const RelayoutParams& p, const Plane& pl, uint32_t v0, uint32_t v1) {
 #pragma unroll 1
     for (uint32_t base = v0; base < v1; base += kThreads * VB) {
-        uint4 buf[VB];
+        Vec<VW> buf[VB];
 #pragma unroll
         for (int i = 0; i < VB; ++i) {
             const uint32_t v = base + i * kThreads + threadIdx.x;
-            if (v < v1) buf[i] = ld_stream(pl.src + vec_offset(p, v, pl.st, pl.sh));
+            if (v < v1) buf[i] = ld_stream<VW>(pl.src + vec_offset<VW>(p, v, pl.st, pl.sh));
         }
 #pragma unroll
         for (int i = 0; i < VB; ++i) {
             const uint32_t v = base + i * kThreads + threadIdx.x;
-            if (v < v1) st_stream(pl.dst + dst_offset<kDir>(p, pl, v), buf[i]);
+            if (v < v1) st_stream<VW>(pl.dst + dst_offset<kDir, VW>(p, pl, v), buf[i]);
         }
     }
 }
 
-// ---- 16-bit <-> fp32 helpers (round to nearest even) ----
+// ---------------------------------------------------------------- 16-bit helpers (RN-even)
 template <Fused kF>
 __device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
     if constexpr (kF == Fused::kBF16) {
@@ -149,39 +181,63 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
-// s + e == a + b exactly, s = fl(a + b)  (TwoSum)
+// round16(a * b) for two pairs of 16-bit values: the exact product of two 16-bit
+// values fits fp32, so the packed multiply's single rounding equals rounding
+// the fp32 product.
+template <Fused kF>
+__device__ __forceinline__ uint32_t mul2(uint32_t a, uint32_t b) {
+    if constexpr (kF == Fused::kBF16) {
+        const __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                                         *reinterpret_cast<const __nv_bfloat162*>(&b));
+        return *reinterpret_cast<const uint32_t*>(&r);
+    } else {
+        const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+        return *reinterpret_cast<const uint32_t*>(&r);
+    }
+}
+
+// s + e == a + b exactly, s = fl(a + b)  (TwoSum, Knuth, TAOCP vol. 2, 4.2.2)
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
     s = __fadd_rn(a, b);
     const float bb = __fsub_rn(s, a);
     e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
-// One lane's 8 elements of a head row: RMSNorm (row reduced over kVpr lanes),
-// weight scale, interleaved RoPE with this lane's 4 (cos, sin) pairs tab[0..8).
-template <Fused kF, int kVpr>
-__device__ __forceinline__ uint4 norm_rope_vec(const uint4& xin, const float (&w)[8], const float* tab, bool valid,
-                                               float eps) {
-    float4 c0 = make_float4(1.f, 0.f, 1.f, 0.f), c1 = c0;
-    if (valid) {  // issued first: the reduction below hides its latency
-        c0 = ld_table(tab);
-        c1 = ld_table(tab + 4);
-    }
-    float x[8];
-    unpack2<kF>(xin.x, x[0], x[1]);
-    unpack2<kF>(xin.y, x[2], x[3]);
-    unpack2<kF>(xin.z, x[4], x[5]);
-    unpack2<kF>(xin.w, x[6], x[7]);
-    // squares of 16-bit values are exact in fp32; accumulate them as hi + lo
-    float hi = __fmul_rn(x[0], x[0]), lo = 0.f;
+// TFU_EXACT_SUMSQ 1: the row's sum of squares is carried as an unevaluated pair
+// hi + lo (TwoSum), so its fp32 rounding is the correctly rounded sum for
+// ordinary inputs and the whole fused path matches a step-by-step evaluation
+// bit for bit.  0: a plain fp32 FMA chain (rare 1-ulp output differences).
+#ifndef TFU_EXACT_SUMSQ
+#define TFU_EXACT_SUMSQ 1
+#endif
+
+// One lane's NP element pairs of a head row spread over kLanes lanes: RMSNorm,
+// weight scale (wpk: the lane's weights as packed pairs) and interleaved RoPE
+// with the lane's NP (cos, sin) pairs at tab[0 .. 2*NP).
+template <Fused kF, int kLanes, int NP>
+__device__ __forceinline__ void norm_rope_lane(uint32_t (&xw)[NP], const uint32_t (&wpk)[NP], const float* tab,
+                                               bool valid, float eps) {
+    constexpr float kInvD = 1.0f / float(kLanes * NP * 2);  // D is a power of two: exact scaling
+    float4 cs[NP / 2];
 #pragma unroll
-    for (int j = 1; j < 8; ++j) {
-        float s, e;
-        two_sum(hi, __fmul_rn(x[j], x[j]), s, e);
-        hi = s;
+    for (int k = 0; k < NP / 2; ++k) cs[k] = make_float4(1.f, 0.f, 1.f, 0.f);
+    if (valid) {  // issued first: the reduction below hides its latency
+#pragma unroll
+        for (int k = 0; k < NP / 2; ++k) cs[k] = ld_table(tab + 4 * k);
+    }
+#if TFU_EXACT_SUMSQ
+    float hi = 0.f, lo = 0.f;  // squares of 16-bit values are exact in fp32
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        float a, b, s, e;
+        unpack2<kF>(xw[j], a, b);
+        two_sum(hi, __fmul_rn(a, a), s, e);
+        lo = __fadd_rn(lo, e);
+        two_sum(s, __fmul_rn(b, b), hi, e);
         lo = __fadd_rn(lo, e);
     }
 #pragma unroll
-    for (int m = 1; m < kVpr; m <<= 1) {
+    for (int m = 1; m < kLanes; m <<= 1) {  // both partners compute the same pair
         const float ohi = __shfl_xor_sync(0xffffffffu, hi, m);
         const float olo = __shfl_xor_sync(0xffffffffu, lo, m);
         float s, e;
@@ -190,85 +246,118 @@ __device__ __forceinline__ uint4 norm_rope_vec(const uint4& xin, const float (&w
         hi = s;
     }
     const float ss = __fadd_rn(hi, lo);
-    const float ms = __fmul_rn(ss, 1.0f / float(kVpr * 8));  // D is a power of two: exact scaling
-    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
-    float z[8];
+#else
+    float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-        float y0, y1;
-        unpack2<kF>(pack2<kF>(__fmul_rn(x[j], inv), __fmul_rn(x[j + 1], inv)), y0, y1);
-        unpack2<kF>(pack2<kF>(__fmul_rn(y0, w[j]), __fmul_rn(y1, w[j + 1])), z[j], z[j + 1]);
+    for (int j = 0; j < NP; ++j) {
+        float a, b;
+        unpack2<kF>(xw[j], a, b);
+        acc0 = __fmaf_rn(a, a, acc0);  // squares of 16-bit values are exact in fp32
+        acc1 = __fmaf_rn(b, b, acc1);
     }
-    const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    uint32_t o[4];
+    float ss = __fadd_rn(acc0, acc1);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float a = z[2 * k], b = z[2 * k + 1], c = cs[2 * k], s = cs[2 * k + 1];
-        o[k] = pack2<kF>(__fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s)), __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c)));
+    for (int m = 1; m < kLanes; m <<= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, m));
+#endif
+    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(ss, kInvD), eps)));
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        float a, b;
+        unpack2<kF>(xw[j], a, b);
+        const uint32_t y = pack2<kF>(__fmul_rn(a, inv), __fmul_rn(b, inv));
+        unpack2<kF>(mul2<kF>(y, wpk[j]), a, b);
+        const float4 c4 = cs[j / 2];
+        const float c = (j & 1) ? c4.z : c4.x;
+        const float s = (j & 1) ? c4.w : c4.y;
+        xw[j] = pack2<kF>(__fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s)), __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c)));
     }
-    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-template <Fused kF, int kVpr>
+template <Fused kF, int VW, int kLanes, int VB>
 __device__ __forceinline__ void norm_rope_range(const RelayoutParams& p, const Plane& pl, uint32_t v0, uint32_t v1) {
-    constexpr int VB = 4;
-    constexpr int kRowFloats = kVpr * 8;  // D floats per table row: D/2 (cos, sin) pairs
-    const uint32_t dv = threadIdx.x % kVpr;  // v0 and kThreads are multiples of kVpr
-    float w[8];
+    constexpr int NP = VW / 4;                    // element pairs per lane
+    constexpr int kRowFloats = kLanes * NP * 2;  // D floats per table row: D/2 (cos, sin) pairs
+    const uint32_t dv = threadIdx.x % kLanes;    // v0 and kThreads are multiples of kLanes
+    uint32_t wpk[NP];
     {
-        const uint4 wv = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.weight[pl.x]) + dv * 16);
-        unpack2<kF>(wv.x, w[0], w[1]);
-        unpack2<kF>(wv.y, w[2], w[3]);
-        unpack2<kF>(wv.z, w[4], w[5]);
-        unpack2<kF>(wv.w, w[6], w[7]);
+        const Vec<VW> wv = *reinterpret_cast<const Vec<VW>*>(static_cast<const uint8_t*>(p.weight[pl.x]) + dv * VW);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) wpk[j] = wv.w[j];
     }
-    const float* tab_lane = p.table + size_t(pl.pos0) * kRowFloats + dv * 8;
+    const float* tab_lane = p.table + size_t(pl.pos0) * kRowFloats + dv * (2 * NP);
 #pragma unroll 1
     for (uint32_t base = v0; base < v1; base += kThreads * VB) {
-        uint4 buf[VB];
+        Vec<VW> buf[VB];
 #pragma unroll
         for (int i = 0; i < VB; ++i) {
             const uint32_t v = base + i * kThreads + threadIdx.x;
-            buf[i] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int j = 0; j < NP; ++j) buf[i].w[j] = 0u;
             if (v < v1) {
-                const uint32_t row = v / kVpr;
+                const uint32_t row = v / kLanes;
                 const uint32_t t = fastdiv(row, p.div_hl);
                 const uint32_t h = row - t * p.Hl;
-                buf[i] = ld_stream(pl.src + int64_t(t) * pl.st + int64_t(h) * pl.sh + int64_t(dv) * 16);
+                buf[i] = ld_stream<VW>(pl.src + int64_t(t) * pl.st + int64_t(h) * pl.sh + int64_t(dv) * VW);
             }
         }
 #pragma unroll
         for (int i = 0; i < VB; ++i) {
             const uint32_t v = base + i * kThreads + threadIdx.x;
-            const uint32_t t = fastdiv(v / kVpr, p.div_hl);
+            const uint32_t t = fastdiv(v / kLanes, p.div_hl);
             // every lane runs the row reduction (it shuffles); only valid lanes load and store
-            const uint4 o = norm_rope_vec<kF, kVpr>(buf[i], w, tab_lane + size_t(t) * kRowFloats, v < v1, p.eps);
-            if (v < v1) st_stream(pl.dst + int64_t(v) * 16, o);
+            norm_rope_lane<kF, kLanes, NP>(buf[i].w, wpk, tab_lane + size_t(t) * kRowFloats, v < v1, p.eps);
+            if (v < v1) st_stream<VW>(pl.dst + int64_t(v) * VW, buf[i]);
         }
     }
 }
 
-// Resident CTAs per SM the register budget is sized for: 4 x 256 threads for the
-// plain copy (<= 64 registers), 3 x 256 for the fused kernels (<= 85 registers).
-template <Fused kF>
-constexpr int min_blocks() { return kF == Fused::kNone ? 4 : 3; }
+// Tuning constants (compile-time; overridable with -D for measurement sweeps).
+// TFU_COPY_MIN_BLOCKS / TFU_FUSED_MIN_BLOCKS: resident 256-thread CTAs per SM the
+// register budget is sized for.  TFU_COPY_BATCH / TFU_FUSED_BATCH: 32-byte
+// vectors each lane loads before storing (twice as many 16-byte vectors).
+#ifndef TFU_COPY_MIN_BLOCKS
+#define TFU_COPY_MIN_BLOCKS 4
+#endif
+#ifndef TFU_FUSED_MIN_BLOCKS
+#define TFU_FUSED_MIN_BLOCKS 2
+#endif
+#ifndef TFU_COPY_BATCH
+#define TFU_COPY_BATCH 4
+#endif
+#ifndef TFU_FUSED_BATCH
+#define TFU_FUSED_BATCH 4
+#endif
 
-template <Dir kDir, Fused kF, int kVpr>
+template <Fused kF>
+__host__ __device__ constexpr int min_blocks() {
+    return kF == Fused::kNone ? TFU_COPY_MIN_BLOCKS : TFU_FUSED_MIN_BLOCKS;
+}
+template <int VW>
+__host__ __device__ constexpr int copy_batch() {
+    return VW == 32 ? TFU_COPY_BATCH : 2 * TFU_COPY_BATCH;
+}
+template <int VW>
+__host__ __device__ constexpr int fused_batch() {
+    return VW == 32 ? TFU_FUSED_BATCH : 2 * TFU_FUSED_BATCH;
+}
+
+template <Dir kDir, Fused kF, int VW, int kLanes>
 __global__ void __launch_bounds__(kThreads, min_blocks<kF>()) relayout_kernel(const __grid_constant__ RelayoutParams p) {
+    constexpr uint32_t kChunk = uint32_t(chunk_vecs(VW));
 #pragma unroll 1
     for (uint32_t u = blockIdx.x; u < p.n_units; u += gridDim.x) {
         const uint32_t c = fastdiv(u, p.div_planes);
         const uint32_t q = u - c * p.n_planes;
         const Plane pl = decode_plane<kDir>(p, q);
-        const uint32_t v0 = c * uint32_t(kChunkVecs);
-        const uint32_t v1 = min(v0 + uint32_t(kChunkVecs), p.nv);
+        const uint32_t v0 = c * kChunk;
+        const uint32_t v1 = min(v0 + kChunk, p.nv);
         if constexpr (kF != Fused::kNone) {
             if ((p.fused_mask >> pl.x) & 1u) {
-                norm_rope_range<kF, kVpr>(p, pl, v0, v1);
+                norm_rope_range<kF, VW, kLanes, fused_batch<VW>()>(p, pl, v0, v1);
                 continue;
             }
         }
-        copy_range<kDir, 8>(p, pl, v0, v1);
+        copy_range<kDir, VW, copy_batch<VW>()>(p, pl, v0, v1);
     }
 }
 
@@ -297,45 +386,54 @@ int device_sms() {
     return sms > 0 ? sms : 1;
 }
 
-template <Dir kDir, Fused kF, int kVpr>
+template <Dir kDir, Fused kF, int VW, int kLanes>
 cudaError_t launch_one(const RelayoutParams& p, cudaStream_t stream) {
     static int blocks_per_sm = 0;  // same for every device of one architecture
     if (blocks_per_sm == 0) {
         int b = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, relayout_kernel<kDir, kF, kVpr>, kThreads, 0);
+        cudaError_t e =
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, relayout_kernel<kDir, kF, VW, kLanes>, kThreads, 0);
         if (e != cudaSuccess) return e;
         blocks_per_sm = b > 0 ? b : 1;
     }
     const int64_t want = int64_t(device_sms()) * blocks_per_sm;
     const unsigned grid = unsigned(want < int64_t(p.n_units) ? want : int64_t(p.n_units));
-    relayout_kernel<kDir, kF, kVpr><<<grid, kThreads, 0, stream>>>(p);
+    relayout_kernel<kDir, kF, VW, kLanes><<<grid, kThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
-template <Fused kF>
+template <Fused kF, int VW>
 cudaError_t launch_fused(const RelayoutParams& p, cudaStream_t stream) {
-    switch (p.vpr) {
-        case 4: return launch_one<Dir::kScatter, kF, 4>(p, stream);
-        case 8: return launch_one<Dir::kScatter, kF, 8>(p, stream);
-        case 16: return launch_one<Dir::kScatter, kF, 16>(p, stream);
-        case 32: return launch_one<Dir::kScatter, kF, 32>(p, stream);
+    switch (p.vpr) {  // lanes per head row
+        case 2: return launch_one<Dir::kScatter, kF, VW, 2>(p, stream);
+        case 4: return launch_one<Dir::kScatter, kF, VW, 4>(p, stream);
+        case 8: return launch_one<Dir::kScatter, kF, VW, 8>(p, stream);
+        case 16: return launch_one<Dir::kScatter, kF, VW, 16>(p, stream);
+        case 32: return launch_one<Dir::kScatter, kF, VW, 32>(p, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+template <int VW>
+cudaError_t launch_width(const RelayoutParams& p, Dir dir, Fused fused, cudaStream_t stream) {
+    if (dir == Dir::kGather) {
+        if (fused != Fused::kNone) return cudaErrorInvalidValue;
+        return launch_one<Dir::kGather, Fused::kNone, VW, 0>(p, stream);
+    }
+    switch (fused) {
+        case Fused::kNone: return launch_one<Dir::kScatter, Fused::kNone, VW, 0>(p, stream);
+        case Fused::kBF16: return launch_fused<Fused::kBF16, VW>(p, stream);
+        case Fused::kFP16: return launch_fused<Fused::kFP16, VW>(p, stream);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_relayout(const RelayoutParams& p, Dir dir, Fused fused, cudaStream_t stream) {
     if (p.n_units == 0) return cudaSuccess;
-    if (dir == Dir::kGather) {
-        if (fused != Fused::kNone) return cudaErrorInvalidValue;
-        return launch_one<Dir::kGather, Fused::kNone, 0>(p, stream);
-    }
-    switch (fused) {
-        case Fused::kNone: return launch_one<Dir::kScatter, Fused::kNone, 0>(p, stream);
-        case Fused::kBF16: return launch_fused<Fused::kBF16>(p, stream);
-        case Fused::kFP16: return launch_fused<Fused::kFP16>(p, stream);
-    }
+    if (p.vec_bytes == 32) return launch_width<32>(p, dir, fused, stream);
+    if (p.vec_bytes == 16) return launch_width<16>(p, dir, fused, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -132,18 +132,42 @@ tf_status check_strides(const char* what, const tf_strides& s, int esize, int64_
     return TF_OK;
 }
 
-// Sizes of the unit grid; everything indexed in 32 bits must fit.
+// 32-byte vectors when every address the kernel forms is 32-byte aligned
+// (bases, strides of dimensions longer than 1, weights, the head row), else 16.
+#ifndef TFU_MAX_VEC_BYTES
+#define TFU_MAX_VEC_BYTES 32
+#endif
+uint32_t pick_vec_bytes(const RelayoutParams& p, const Shape& sh, int64_t src_tokens, int64_t dst_tokens) {
+    if (TFU_MAX_VEC_BYTES < 32) return 16;
+    auto ok = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 31u) == 0; };
+    auto ok_stride = [](int64_t st, int64_t extent) { return extent <= 1 || st % 32 == 0; };
+    if ((int64_t(sh.D) * sh.esize) % 32 != 0) return 16;
+    for (uint32_t x = 0; x < p.nx; ++x) {
+        for (int i = 0; i < sh.P; ++i)
+            if (!ok(p.src[x][i]) || !ok(p.dst[x][i])) return 16;
+        if (!ok_stride(p.s_b[x], sh.B) || !ok_stride(p.s_t[x], src_tokens) || !ok_stride(p.s_h[x], sh.H) ||
+            !ok_stride(p.d_b[x], sh.B) || !ok_stride(p.d_t[x], dst_tokens) || !ok_stride(p.d_h[x], sh.H))
+            return 16;
+        if (((p.fused_mask >> x) & 1u) && !ok(p.weight[x])) return 16;
+    }
+    return 32;
+}
+
+// Sizes of the unit grid for vectors of p.vec_bytes; everything indexed in 32
+// bits must fit.
 tf_status plan_units(RelayoutParams& p, const Shape& sh) {
     p.P = uint32_t(sh.P);
     p.B = uint32_t(sh.B);
     p.Sl = uint32_t(sh.Sl);
     p.Hl = uint32_t(sh.Hl);
-    p.vpr = uint32_t(int64_t(sh.D) * sh.esize / 16);
+    if (p.vec_bytes != 16 && p.vec_bytes != 32) p.vec_bytes = 16;
+    p.vpr = uint32_t(int64_t(sh.D) * sh.esize / p.vec_bytes);
     const uint64_t nv = uint64_t(sh.Sl) * uint64_t(sh.Hl) * p.vpr;
     if (nv > (uint64_t(1) << 31)) return fail(TF_ERR_UNSUPPORTED, "one shard/head-group block exceeds 2^31 vectors");
     p.nv = uint32_t(nv);
+    const uint64_t cv = uint64_t(tfu::chunk_vecs(int(p.vec_bytes)));
     const uint64_t planes = uint64_t(sh.B) * sh.P * p.nx * sh.P;
-    const uint64_t chunks = (nv + tfu::kChunkVecs - 1) / tfu::kChunkVecs;
+    const uint64_t chunks = (nv + cv - 1) / cv;
     if (planes * chunks >= (uint64_t(1) << 31)) return fail(TF_ERR_UNSUPPORTED, "problem exceeds 2^31 work units");
     p.n_planes = uint32_t(planes);
     p.n_chunks = uint32_t(chunks);
@@ -367,6 +391,7 @@ tf_status plan_scatter(const void* const* q, const void* const* k, const void* c
     p.nx = nx;
     p.eps = nr ? nr->eps : 0.f;
     p.table = nr ? nr->cos_sin : nullptr;
+    p.vec_bytes = 16;  // size limits checked for the larger vector count; re-planned at launch
     if ((s = plan_units(p, pl.sh)) != TF_OK) return s;
     pl.empty = B == 0 || Sl == 0;
     return TF_OK;
@@ -383,6 +408,9 @@ tf_status launch_scatter(ScatterPlan& pl, const tf_norm_rope* nr, int device, cu
         pl.p.table = t->ptr;
         *used = t;
     }
+    pl.p.vec_bytes = pick_vec_bytes(pl.p, pl.sh, pl.sh.Sl, int64_t(pl.sh.P) * pl.sh.Sl);
+    tf_status s = plan_units(pl.p, pl.sh);
+    if (s != TF_OK) return s;
     cudaError_t e = tfu::launch_relayout(pl.p, tfu::Dir::kScatter, pl.fused, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launching the scatter kernel");
     g_launches.fetch_add(1);
@@ -507,6 +535,7 @@ TF_API tf_status tf_ulysses_gather_out(const char* tag, const void* const* attn,
     p.d_b[0] = os.b * sh.esize;
     p.d_t[0] = os.t * sh.esize;
     p.d_h[0] = os.h * sh.esize;
+    p.vec_bytes = 16;
     if ((s = plan_units(p, sh)) != TF_OK) return s;
     int device = 0;
     if ((s = current_device(&device)) != TF_OK) return s;
@@ -521,6 +550,8 @@ TF_API tf_status tf_ulysses_gather_out(const char* tag, const void* const* attn,
         return s;
     for (int r = 0; r < P; ++r) p.dst[0][r] = static_cast<uint8_t*>(dst ? dst[r] : e->buf[0][r]);
     if (!empty) {
+        p.vec_bytes = pick_vec_bytes(p, sh, S, S_local);
+        if ((s = plan_units(p, sh)) != TF_OK) return s;
         cudaError_t err = tfu::launch_relayout(p, tfu::Dir::kGather, tfu::Fused::kNone, st);
         if (err != cudaSuccess) return cuda_fail(err, "launching the gather kernel");
         g_launches.fetch_add(1);
