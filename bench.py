@@ -52,6 +52,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--sets", type=int, default=2, help="rotating input sets (each ~2 GB)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=1024, help="tokens per shard in the CPU-baseline sample")
     return ap.parse_args()
@@ -241,7 +242,7 @@ def main():
     P, B, S, H, D = w["P"], w["B"], w["S"], w["H"], w["D"]
     Sl, Hl = S // P, H // P
     dtype = torch.bfloat16
-    nsets = 2
+    nsets = max(1, args.sets)
     sets = []
     for s in range(nsets):
         g = synth.qkv_shards(P, B, Sl, H, D, dtype, seed=1000 * rank + s, layout="v_strided", device=dev)
@@ -363,7 +364,7 @@ def main():
                        "step": "fused Q/K/V scatter (RMSNorm+RoPE on Q/K, V strided view of a fused "
                                "projection) into cached targets + head->sequence output gather",
                        "parallelism": "replicas" if world > 1 else "single GPU",
-                       "l2": "inputs larger than L2: 2 rotating input sets of ~2 GB"},
+                       "l2": f"inputs larger than L2: {nsets} rotating input set(s) of ~2 GB"},
             "tokens_per_s": world * B * S * K / (total_ms / 1e3),
             "pct_of_hbm_measured": 100.0 * value / world / peak,
             "pct_of_hbm_nominal_8000": 100.0 * value / world / NOMINAL_HBM_GBS,
