@@ -178,6 +178,35 @@ TF_API tf_status tf_ulysses_scatter_qkv_into(const void *const *q, const void *c
                                              void *stream);
 
 /*
+ * tf_ulysses_scatter_qkv_noalloc -- the scatter of tf_ulysses_scatter_qkv_into for
+ * callers that cannot allocate device memory: code running under a device-memory
+ * budget reserved up front (another allocator already owns the GPU's free
+ * memory, so a cudaMalloc may fail or break that accounting), and latency-bound
+ * loops where the implicit device synchronisation of cudaMalloc/cudaFree is not
+ * acceptable.  The paper has no counterpart; this is an interface of this
+ * library only.
+ *
+ * Arguments, layouts and errors are those of tf_ulysses_scatter_qkv_into; the
+ * caller passes the inputs and the targets.  When mode is
+ * TF_MODE_SCATTER_NORM_ROPE and nr->cos_sin is NULL, the cos/sin table is built
+ * on `stream`, on every call, into a fixed 16 MiB device array that is part of
+ * the library (file-scope, held by every GPU that loads the library until
+ * exit), so P * S_local * D must not exceed 4,194,304 (4 Mi floats); larger
+ * sizes return TF_ERR_UNSUPPORTED before any launch.  Nothing is allocated: no
+ * cudaMalloc, cudaFree or allocating library routine is called.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  All calls share the one array: calls whose work
+ * overlaps on the GPU (e.g. on two streams without ordering) race on it.
+ */
+TF_API tf_status tf_ulysses_scatter_qkv_noalloc(const void *const *q, const void *const *k, const void *const *v,
+                                                const tf_strides *strides,
+                                                int P, int B, int S_local, int H, int D,
+                                                tf_dtype dtype, tf_mode mode, const tf_norm_rope *nr,
+                                                void *const *q_out, void *const *k_out, void *const *v_out,
+                                                void *stream);
+
+/*
  * tf_ulysses_gather_out -- head->sequence gather of the attention output (the
  * inverse all-to-all of the Ulysses section; TeleFuser PR #27 keeps it for the
  * output path).

@@ -1,0 +1,105 @@
+"""The allocation-free scatter entry point (tf_ulysses_scatter_qkv_noalloc).
+
+It serves callers that cannot allocate device memory: code working inside a
+device-memory budget reserved up front, where another allocator already owns
+the free memory, and latency-bound loops that cannot take the device
+synchronisation of cudaMalloc/cudaFree.  Its cos/sin table lives in a fixed
+device array of the library instead of an allocation.
+
+Checked here through the C ABI: two calls in a row (different shapes and RoPE
+bases, so the fixed table is rebuilt) give the same targets as the existing
+caller-owned-target entry point, within the tolerance of the other fused
+tests; no allocation callback fires; a size beyond the fixed capacity is
+rejected.  This file is collected last so that a run stopping at its first
+failure has already run every other test.
+"""
+import pytest
+import torch
+
+from parity_util import assert_fused_ok, bits_equal
+from ulysses_sequence_attention_tf_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tf():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from ulysses_sequence_attention_tf_gb300 import binding, build
+    build.build()
+    binding.lib()
+    binding.use_torch_allocator(True)
+    return binding
+
+
+def _targets(P, B, S, Hl, D, dtype, fill):
+    return [torch.full((B, S, Hl, D), fill, dtype=dtype, device="cuda") for _ in range(P)]
+
+
+class _CountingAllocator:
+    """Allocation callbacks that count calls and refuse to allocate."""
+
+    def __init__(self, tf):
+        self.calls = 0
+        self.fns = (tf.ALLOC_FN(self._alloc), tf.FREE_FN(self._free))
+
+    def _alloc(self, nbytes, stream, ctx):
+        self.calls += 1
+        return None
+
+    def _free(self, ptr, nbytes, stream, ctx):
+        self.calls += 1
+
+
+CALLS = [
+    # P, B, S, H, D, dtype, theta, layout
+    (4, 1, 4096, 24, 128, torch.bfloat16, 10000.0, "fused"),
+    (2, 2, 998, 16, 64, torch.float16, 500000.0, "v_strided"),
+]
+
+
+def test_noalloc_matches_existing_entry_point_twice(tf):
+    counter = _CountingAllocator(tf)
+    for i, (P, B, S, H, D, dtype, theta, layout) in enumerate(CALLS):
+        Sl, Hl = S // P, H // P
+        g = synth.qkv_shards(P, B, Sl, H, D, dtype, seed=40 + i, layout=layout, device="cuda")
+        wq, wk = synth.norm_weights(D, dtype, seed=40 + i, device="cuda")
+        kw = dict(norm_rope=True, q_weight=wq, k_weight=wk, eps=1e-6, theta=theta)
+        ref = [_targets(P, B, S, Hl, D, dtype, 0.0) for _ in range(3)]
+        tf.scatter_qkv_into(g["q"], g["k"], g["v"], *ref, **kw)
+        out = [_targets(P, B, S, Hl, D, dtype, 9.0) for _ in range(3)]
+        torch.cuda.synchronize()
+        tf.lib().tf_ulysses_set_allocator(counter.fns[0], counter.fns[1], None)
+        try:
+            tf.scatter_qkv_noalloc(g["q"], g["k"], g["v"], *out, **kw)
+            torch.cuda.synchronize()
+        finally:
+            tf.use_torch_allocator(True)
+        assert counter.calls == 0, "the allocation-free entry point called the allocator"
+        for x in (0, 1):  # Q and K: the fused path, with the tolerance of the other fused tests
+            for gi in range(P):
+                assert_fused_ok(out[x][gi], ref[x][gi])
+        for gi in range(P):  # V: bit copy
+            assert bits_equal(out[2][gi], ref[2][gi])
+
+
+def test_noalloc_rejects_sizes_beyond_the_fixed_scratch(tf):
+    P, B, Sl, H, D = 2, 1, 16385, 4, 128  # P * S_local * D = 4,194,560 > 4 Mi floats
+    dtype = torch.bfloat16
+    g = synth.qkv_shards(P, B, Sl, H, D, dtype, seed=1, device="cuda", with_k=False, with_v=False)
+    wq, wk = synth.norm_weights(D, dtype, device="cuda")
+    out = _targets(P, B, P * Sl, H // P, D, dtype, 5.0)
+    with pytest.raises(tf.TfUlyssesError) as ei:
+        tf.scatter_qkv_noalloc(g["q"], None, None, out, norm_rope=True, q_weight=wq, k_weight=wk)
+    assert ei.value.status == tf.TF_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert all(torch.all(o == 5.0) for o in out), "a rejected call wrote its targets"
+    # with a caller table no scratch is needed, so the same size is accepted
+    table = torch.zeros((P * Sl, D // 2, 2), dtype=torch.float32, device="cuda")
+    table[..., 0] = 1.0
+    tf.scatter_qkv_noalloc(g["q"], None, None, out, norm_rope=True, q_weight=wq, k_weight=wk, cos_sin=table)
+    ref = _targets(P, B, P * Sl, H // P, D, dtype, 0.0)
+    tf.scatter_qkv_into(g["q"], None, None, ref, norm_rope=True, q_weight=wq, k_weight=wk, cos_sin=table)
+    for gi in range(P):
+        assert_fused_ok(out[gi], ref[gi])

@@ -69,10 +69,12 @@ def _declare(lib):
                                            vp, ctypes.POINTER(Targets)]
     lib.tf_ulysses_scatter_qkv_into.argtypes = [PP, PP, PP, ctypes.POINTER(Strides), i32, i32, i32, i32, i32,
                                                 i32, i32, ctypes.POINTER(NormRope), PP, PP, PP, vp]
+    lib.tf_ulysses_scatter_qkv_noalloc.argtypes = lib.tf_ulysses_scatter_qkv_into.argtypes
     lib.tf_ulysses_gather_out.argtypes = [ctypes.c_char_p, PP, ctypes.POINTER(Strides), i32, i32, i32, i32, i32,
                                           i32, PP, ctypes.POINTER(Strides), vp, ctypes.POINTER(Targets)]
     lib.tf_ulysses_rope_table.argtypes = [ctypes.c_float, i32, i32, vp, ctypes.POINTER(ctypes.c_void_p)]
-    for name in ("tf_ulysses_scatter_qkv", "tf_ulysses_scatter_qkv_into", "tf_ulysses_gather_out",
+    for name in ("tf_ulysses_scatter_qkv", "tf_ulysses_scatter_qkv_into", "tf_ulysses_scatter_qkv_noalloc",
+                 "tf_ulysses_gather_out",
                  "tf_ulysses_rope_table", "tf_ulysses_cache_clear"):
         getattr(lib, name).restype = i32
     lib.tf_ulysses_cache_clear.argtypes = []
@@ -220,6 +222,25 @@ def scatter_qkv_into(q, k, v, q_out, k_out=None, v_out=None, *, norm_rope=False,
     mode = TF_MODE_SCATTER_NORM_ROPE if norm_rope else TF_MODE_SCATTER
     nr = _norm_rope(q_weight, k_weight, eps, theta, cos_sin) if norm_rope else None
     _check(lib().tf_ulysses_scatter_qkv_into(
+        _ptr_array(q), _ptr_array(k), _ptr_array(v), strides, P, B, Sl, H, D, _dtype_code(q[0].dtype), mode,
+        ctypes.byref(nr) if nr is not None else None, _ptr_array(q_out), _ptr_array(k_out), _ptr_array(v_out),
+        _stream_handle(stream)))
+    return q_out, k_out, v_out
+
+
+def scatter_qkv_noalloc(q, k, v, q_out, k_out=None, v_out=None, *, norm_rope=False, q_weight=None, k_weight=None,
+                        eps=1e-6, theta=10000.0, cos_sin=None, stream=None):
+    """``scatter_qkv_into`` for callers that cannot allocate device memory: the
+    library allocates nothing; a needed cos/sin table is rebuilt on every call
+    in the library's fixed 16 MiB device scratch (P*S_local*D <= 4 Mi floats).
+    Calls that overlap on the GPU race on that scratch."""
+    P, B, Sl, H, D, strides = _scatter_args(q, k, v)
+    for outs in (q_out, k_out, v_out):
+        if outs is not None and any(not o.is_contiguous() for o in outs):
+            raise ValueError("targets must be contiguous [B, S, H/P, D]")
+    mode = TF_MODE_SCATTER_NORM_ROPE if norm_rope else TF_MODE_SCATTER
+    nr = _norm_rope(q_weight, k_weight, eps, theta, cos_sin) if norm_rope else None
+    _check(lib().tf_ulysses_scatter_qkv_noalloc(
         _ptr_array(q), _ptr_array(k), _ptr_array(v), strides, P, B, Sl, H, D, _dtype_code(q[0].dtype), mode,
         ctypes.byref(nr) if nr is not None else None, _ptr_array(q_out), _ptr_array(k_out), _ptr_array(v_out),
         _stream_handle(stream)))

@@ -21,6 +21,7 @@
 
 #include <cuda_runtime.h>
 
+#include "noalloc.h"
 #include "relayout.h"
 #include "tf_ulysses.h"
 
@@ -502,6 +503,54 @@ TF_API tf_status tf_ulysses_scatter_qkv_into(const void* const* q, const void* c
         return launch_scatter(pl, nr, device, st, &used);
     }
     return launch_scatter(pl, nr, device, st, &used);
+}
+
+// Allocation-free scatter: the library-built cos/sin table goes to the fixed
+// scratch of noalloc.cu, rebuilt on every call in stream order.
+TF_API tf_status tf_ulysses_scatter_qkv_noalloc(const void* const* q, const void* const* k, const void* const* v,
+                                                const tf_strides* strides, int P, int B, int S_local, int H, int D,
+                                                tf_dtype dtype, tf_mode mode, const tf_norm_rope* nr,
+                                                void* const* q_out, void* const* k_out, void* const* v_out,
+                                                void* stream) {
+    ScatterPlan pl;
+    tf_status s = plan_scatter(q, k, v, strides, P, B, S_local, H, D, dtype, mode, nr, &pl);
+    if (s != TF_OK) return s;
+    void* const* dsts[3] = {q_out, k_out, v_out};
+    const char* names[3] = {"q_out", "k_out", "v_out"};
+    for (int x = 0; x < 3; ++x) {
+        if (!(pl.present & (1 << x))) continue;
+        if (!dsts[x]) return fail(TF_ERR_INVALID, "%s is NULL for a present source", names[x]);
+        if (!pl.empty && (s = check_ptrs(names[x], dsts[x], P)) != TF_OK) return s;
+        for (int g = 0; g < P; ++g) pl.p.dst[pl.slot_of[x]][g] = static_cast<uint8_t*>(dsts[x][g]);
+    }
+    const bool own_table = pl.fused != tfu::Fused::kNone && !nr->cos_sin;
+    const uint64_t table_floats = uint64_t(P) * uint64_t(S_local) * uint64_t(D);
+    if (own_table && table_floats > tfu::kNoAllocTableFloats)
+        return fail(TF_ERR_UNSUPPORTED,
+                    "P*S_local*D = %llu exceeds the fixed cos/sin scratch of %llu floats of the allocation-free entry "
+                    "point",
+                    (unsigned long long)table_floats, (unsigned long long)tfu::kNoAllocTableFloats);
+    int device = 0;
+    if ((s = current_device(&device)) != TF_OK) return s;
+    if (pl.empty) return TF_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (own_table) {
+        float* table = nullptr;
+        cudaError_t e = tfu::noalloc_table_address(&table);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(cos/sin scratch)");
+        double inv_freq[128];  // D <= 256 in the fused mode
+        for (int i = 0; i < D / 2; ++i) inv_freq[i] = std::pow(double(nr->theta), -2.0 * i / D);
+        e = tfu::launch_rope_table(table, inv_freq, P * S_local, D, st);
+        if (e != cudaSuccess) return cuda_fail(e, "building the cos/sin table in the fixed scratch");
+        g_launches.fetch_add(1);
+        pl.p.table = table;
+    }
+    pl.p.vec_bytes = pick_vec_bytes(pl.p, pl.sh, pl.sh.Sl, int64_t(P) * S_local);
+    if ((s = plan_units(pl.p, pl.sh)) != TF_OK) return s;
+    cudaError_t e = tfu::launch_relayout(pl.p, tfu::Dir::kScatter, pl.fused, st);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the scatter kernel");
+    g_launches.fetch_add(1);
+    return TF_OK;
 }
 
 TF_API tf_status tf_ulysses_gather_out(const char* tag, const void* const* attn, const tf_strides* attn_strides,
