@@ -385,3 +385,9 @@ def test_padding_rows_normalise_to_zero(tf):
     for i in range(P):
         assert_fused_ok(tq[i], want[i])
     assert int(ulp_diff(tq[0].cpu(), want[0]).max()) <= 1
+
+
+def test_device_status_clean_after_all_launches(tf):
+    """No bounded in-kernel wait gave up during any launch of this module."""
+    torch.cuda.synchronize()
+    assert tf.device_status(clear=False) == 0

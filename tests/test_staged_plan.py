@@ -1,0 +1,75 @@
+"""Host check of the staged kernel's work decomposition (csrc/tma_plan.h), the
+same code the kernel runs: for many shapes and strides, every unit fits one
+shared-memory stage, its bulk-copy runs tile the unit's rows exactly and in
+order, every run is really contiguous under the strides, stays inside the
+plane, and has 16-byte aligned offsets and sizes."""
+import os
+import subprocess
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "ulysses_sequence_attention_tf_gb300", "csrc")
+
+HARNESS = r'''
+#include <cstdio>
+#include <cstdint>
+#include <vector>
+#include "tma_plan.h"
+using namespace tfu;
+static uint64_t x = 0x9E3779B97F4A7C15ull;
+static uint32_t rnd(uint32_t n) { x ^= x << 13; x ^= x >> 7; x ^= x << 17; return uint32_t(x % n); }
+int main() {
+  long bad = 0, cases = 0;
+  for (int it = 0; it < 4000; ++it) {
+    const uint32_t Sl = 1 + rnd(300), Hl = 1 + rnd(70);
+    const uint32_t rb = 16 * (1 + rnd(40));            // D * esize, a multiple of 16
+    // source-like strides: packed heads or spread heads, token stride >= band
+    const bool packed = rnd(3) != 0;
+    const int64_t sh = packed ? rb : int64_t(rb) + 16 * (1 + rnd(8));
+    const int64_t band = int64_t(Hl - 1) * sh + rb;
+    const int64_t st = rnd(3) == 0 && packed ? int64_t(Hl) * rb : band + 16 * rnd(64);
+    // fused units (16-bit payload) also stage D fp32 cos/sin values per token
+    const uint32_t table_row = (it & 1) ? rb * 2 : 0;
+    const uint32_t rpu = tma_rows_per_unit(Hl, rb, table_row);
+    const uint32_t rows = Sl * Hl;
+    if (table_row > kStageTableBytes / 2) { if (rpu != 0) ++bad; continue; }
+    if (rpu == 0 || uint64_t(rpu) * rb > kStageBytes) { ++bad; continue; }
+    if (uint64_t(Hl) * rb <= kStageBytes && rpu % Hl != 0) { ++bad; continue; }  // whole tokens
+    const int64_t extent = int64_t(Sl - 1) * st + band;
+    for (uint32_t R0 = 0; R0 < rows; R0 += rpu) {
+      const uint32_t R1 = R0 + rpu < rows ? R0 + rpu : rows;
+      uint32_t next = 0;
+      for_each_run(R0, R1, Hl, st, sh, rb, [&](uint32_t i, uint32_t n, int64_t off) {
+        ++cases;
+        if (i != next || n == 0 || i + n > R1 - R0) ++bad;
+        if (off % 16 != 0 || (uint64_t(n) * rb) % 16 != 0) ++bad;
+        for (uint32_t k = 0; k < n; ++k) {  // each row of the run where the strides put it
+          const uint32_t R = R0 + i + k, t = R / Hl, h = R % Hl;
+          if (off + int64_t(k) * rb != int64_t(t) * st + int64_t(h) * sh) ++bad;
+        }
+        if (off < 0 || off + int64_t(n) * rb > extent) ++bad;
+        next = i + n;
+      });
+      if (next != R1 - R0) ++bad;
+      uint32_t t0, t1;
+      unit_tokens(R0, R1, Hl, t0, t1);
+      if (t0 != R0 / Hl || t1 != (R1 - 1) / Hl || t1 >= Sl) ++bad;
+      if (table_row && uint64_t(t1 - t0 + 1) * table_row > kStageTableBytes) ++bad;  // table rows fit
+    }
+  }
+  // a row larger than a stage is refused
+  if (tma_rows_per_unit(4, kStageBytes + 16) != 0) ++bad;
+  std::printf("%ld %ld\n", bad, cases);
+  return bad != 0;
+}
+'''
+
+
+def test_staged_plan_runs_tile_units_exactly(tmp_path):
+    src = tmp_path / "plan.cpp"
+    src.write_text(HARNESS)
+    exe = tmp_path / "plan"
+    subprocess.run(["g++", "-O2", "-std=c++17", f"-I{CSRC}", str(src), "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    bad, cases = r.stdout.split()
+    assert r.returncode == 0 and bad == "0", r.stdout
+    assert int(cases) > 10000

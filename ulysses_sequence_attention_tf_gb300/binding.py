@@ -82,6 +82,8 @@ def _declare(lib):
     lib.tf_ulysses_cache_entries.restype = i32
     lib.tf_ulysses_set_allocator.argtypes = [ALLOC_FN, FREE_FN, vp]
     lib.tf_ulysses_set_allocator.restype = None
+    lib.tf_ulysses_device_status.argtypes = [i32, ctypes.POINTER(ctypes.c_uint)]
+    lib.tf_ulysses_device_status.restype = i32
     lib.tf_ulysses_last_error.argtypes = []
     lib.tf_ulysses_last_error.restype = ctypes.c_char_p
     lib.tf_ulysses_launch_count.argtypes = []
@@ -278,6 +280,13 @@ def rope_table(theta, S, D, *, stream=None, device=None):
 
 def cache_clear():
     _check(lib().tf_ulysses_cache_clear())
+
+
+def device_status(clear: bool = False) -> int:
+    """The staged kernels' device status word (0 = every in-kernel wait completed)."""
+    v = ctypes.c_uint()
+    _check(lib().tf_ulysses_device_status(1 if clear else 0, ctypes.byref(v)))
+    return int(v.value)
 
 
 def cache_entries() -> int:

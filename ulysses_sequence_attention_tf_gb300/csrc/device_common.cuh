@@ -1,0 +1,268 @@
+// device_common.cuh -- device helpers shared by the relayout kernels: vector
+// loads/stores, plane decoding, 16-bit conversions and the per-lane fused
+// RMSNorm + interleaved RoPE of a head row (flashinfer PR #6332 commit message,
+// "Assumptions / Operator math"; formula in tf_ulysses.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "relayout.h"
+
+namespace tfu {
+namespace dev {
+
+// ---------------------------------------------------------------- vectors
+template <int VW>
+struct Vec;
+template <>
+struct Vec<16> {
+    uint32_t w[4];
+};
+template <>
+struct Vec<32> {
+    uint32_t w[8];
+};
+
+template <int VW>
+__device__ __forceinline__ Vec<VW> ld_stream(const uint8_t* p) {
+    Vec<VW> v;
+    if constexpr (VW == 16) {
+        asm("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
+            : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+            : "l"(p));
+    } else {
+        asm("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+            : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]),
+              "=r"(v.w[7])
+            : "l"(p));
+    }
+    return v;
+}
+
+template <int VW>
+__device__ __forceinline__ void st_stream(uint8_t* p, const Vec<VW>& v) {
+    if constexpr (VW == 16) {
+        asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]),
+                     "r"(v.w[3])
+                     : "memory");
+    } else {
+        asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v.w[0]),
+                     "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
+                     : "memory");
+    }
+}
+
+__device__ __forceinline__ float4 ld_table(const float* p) {
+    float4 v;
+    asm("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+
+// ---------------------------------------------------------------- planes
+struct Plane {
+    const uint8_t* src;
+    uint8_t* dst;
+    int64_t st, sh, dt, dh;
+    uint32_t x;
+    uint32_t pos0;  // global position of the plane's first token (scatter)
+};
+
+// plane index q = ((b * P + r) * nx + x) * P + g
+template <Dir kDir>
+__device__ __forceinline__ Plane decode_plane(const RelayoutParams& p, uint32_t q) {
+    const uint32_t g = q % p.P;
+    uint32_t rest = q / p.P;
+    const uint32_t x = rest % p.nx;
+    rest /= p.nx;
+    const uint32_t r = rest % p.P;
+    const uint32_t b = rest / p.P;
+    Plane pl;
+    pl.x = x;
+    pl.st = p.s_t[x];
+    pl.sh = p.s_h[x];
+    pl.dt = p.d_t[x];
+    pl.dh = p.d_h[x];
+    if constexpr (kDir == Dir::kScatter) {
+        pl.src = p.src[x][r] + int64_t(b) * p.s_b[x] + int64_t(g) * p.Hl * pl.sh;
+        pl.dst = p.dst[x][g] + int64_t(b) * p.d_b[x] + int64_t(r) * p.Sl * pl.dt;
+        pl.pos0 = r * p.Sl;
+    } else {
+        pl.src = p.src[x][g] + int64_t(b) * p.s_b[x] + int64_t(r) * p.Sl * pl.st;
+        pl.dst = p.dst[x][r] + int64_t(b) * p.d_b[x] + int64_t(g) * p.Hl * pl.dh;
+        pl.pos0 = 0;
+    }
+    return pl;
+}
+
+// ---------------------------------------------------------------- 16-bit helpers (RN-even)
+template <Fused kF>
+__device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
+    if constexpr (kF == Fused::kBF16) {
+        lo = __uint_as_float(w << 16);
+        hi = __uint_as_float(w & 0xffff0000u);
+    } else {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+        lo = f.x;
+        hi = f.y;
+    }
+}
+
+template <Fused kF>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (kF == Fused::kBF16) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+}
+
+// round16(a * b) for two pairs of 16-bit values: the exact product of two 16-bit
+// values fits fp32, so the packed multiply's single rounding equals rounding
+// the fp32 product.
+template <Fused kF>
+__device__ __forceinline__ uint32_t mul2(uint32_t a, uint32_t b) {
+    if constexpr (kF == Fused::kBF16) {
+        const __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                                         *reinterpret_cast<const __nv_bfloat162*>(&b));
+        return *reinterpret_cast<const uint32_t*>(&r);
+    } else {
+        const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+        return *reinterpret_cast<const uint32_t*>(&r);
+    }
+}
+
+// s + e == a + b exactly, s = fl(a + b)  (TwoSum, Knuth, TAOCP vol. 2, 4.2.2)
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// TFU_EXACT_SUMSQ 1: the row's sum of squares is carried as an unevaluated pair
+// hi + lo (TwoSum), so its fp32 rounding is the correctly rounded sum for
+// ordinary inputs and the whole fused path matches a step-by-step evaluation
+// bit for bit.  0: a plain fp32 FMA chain (rare 1-ulp output differences).
+#ifndef TFU_EXACT_SUMSQ
+#define TFU_EXACT_SUMSQ 1
+#endif
+
+// ---- packed fp32 pairs (sm_100+ f32x2 arithmetic: each lane of the pair is an
+// ordinary IEEE round-to-nearest fp32 operation; one instruction issues both) ----
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// TwoSum on both lanes of a pair
+__device__ __forceinline__ void f2_two_sum(uint64_t a, uint64_t b, uint64_t& s, uint64_t& e) {
+    s = f2_add(a, b);
+    const uint64_t bb = f2_sub(s, a);
+    e = f2_add(f2_sub(a, f2_sub(s, bb)), f2_sub(b, bb));
+}
+
+// One lane's NP element pairs of a head row spread over kLanes lanes: RMSNorm,
+// weight scale (wpk: the lane's weights as packed pairs) and interleaved RoPE
+// with the lane's NP (cos, sin) pairs at tab[0 .. 2*NP) -- in shared memory when
+// kSmemTable, else read through the read-only global path.
+template <Fused kF, int kLanes, int NP, bool kSmemTable = false>
+__device__ __forceinline__ void norm_rope_lane(uint32_t (&xw)[NP], const uint32_t (&wpk)[NP], const float* tab,
+                                               bool valid, float eps) {
+    constexpr float kInvD = 1.0f / float(kLanes * NP * 2);  // D is a power of two: exact scaling
+    float4 cs[NP / 2];
+#pragma unroll
+    for (int k = 0; k < NP / 2; ++k) cs[k] = make_float4(1.f, 0.f, 1.f, 0.f);
+    if (valid) {  // issued first: the reduction below hides its latency
+#pragma unroll
+        for (int k = 0; k < NP / 2; ++k) {
+            if constexpr (kSmemTable) {
+                cs[k] = reinterpret_cast<const float4*>(tab)[k];
+            } else {
+                cs[k] = ld_table(tab + 4 * k);
+            }
+        }
+    }
+    uint64_t x2[NP];  // the lane's values as fp32 pairs
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        float a, b;
+        unpack2<kF>(xw[j], a, b);
+        x2[j] = f2_pack(a, b);
+    }
+#if TFU_EXACT_SUMSQ
+    // squares of 16-bit values are exact in fp32; two interleaved float-pair
+    // accumulators (even and odd elements), then one TwoSum to combine them
+    uint64_t hi2 = f2_mul(x2[0], x2[0]), lo2 = 0;
+#pragma unroll
+    for (int j = 1; j < NP; ++j) {
+        uint64_t s2, e2;
+        f2_two_sum(hi2, f2_mul(x2[j], x2[j]), s2, e2);
+        hi2 = s2;
+        lo2 = f2_add(lo2, e2);
+    }
+    float hi, lo;
+    {
+        float he, ho, le, lo_;
+        f2_unpack(hi2, he, ho);
+        f2_unpack(lo2, le, lo_);
+        float e;
+        two_sum(he, ho, hi, e);
+        lo = __fadd_rn(__fadd_rn(le, lo_), e);
+    }
+#pragma unroll
+    for (int m = 1; m < kLanes; m <<= 1) {  // both partners compute the same pair
+        const float ohi = __shfl_xor_sync(0xffffffffu, hi, m);
+        const float olo = __shfl_xor_sync(0xffffffffu, lo, m);
+        float s, e;
+        two_sum(hi, ohi, s, e);
+        lo = __fadd_rn(__fadd_rn(lo, olo), e);
+        hi = s;
+    }
+    const float ss = __fadd_rn(hi, lo);
+#else
+    uint64_t acc2 = 0;
+#pragma unroll
+    for (int j = 0; j < NP; ++j) acc2 = f2_add(acc2, f2_mul(x2[j], x2[j]));
+    float ae, ao;
+    f2_unpack(acc2, ae, ao);
+    float ss = __fadd_rn(ae, ao);
+#pragma unroll
+    for (int m = 1; m < kLanes; m <<= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, m));
+#endif
+    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(ss, kInvD), eps)));
+    const uint64_t inv2 = f2_pack(inv, inv);
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        float a, b;
+        f2_unpack(f2_mul(x2[j], inv2), a, b);
+        const uint32_t y = pack2<kF>(a, b);  // normalised value rounded before the weight scale
+        unpack2<kF>(mul2<kF>(y, wpk[j]), a, b);
+        const float4 c4 = cs[j / 2];
+        const float c = (j & 1) ? c4.z : c4.x;
+        const float s = (j & 1) ? c4.w : c4.y;
+        xw[j] = pack2<kF>(__fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s)), __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c)));
+    }
+}
+
+}  // namespace dev
+}  // namespace tfu

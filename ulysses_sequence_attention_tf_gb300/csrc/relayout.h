@@ -68,11 +68,25 @@ struct RelayoutParams {
     uint32_t n_chunks;   // ceil(nv / chunk_vecs(vec_bytes))
     uint32_t n_units;   // n_chunks * n_planes
     FastDiv div_vpr, div_hl, div_planes;
+    // shared-memory-staged kernel: units are row ranges of a plane
+    uint32_t row_bytes;   // D * esize
+    uint32_t rpu;         // rows per unit (tma_rows_per_unit)
+    uint32_t plane_rows;  // Sl * Hl
 };
 
 // Launch the relayout of every plane in `p` (vector width p.vec_bytes; for the
 // fused kernels the head row holds p.vpr vectors, D in {32, 64, 128, 256}).
 cudaError_t launch_relayout(const RelayoutParams& p, Dir dir, Fused fused, cudaStream_t stream);
+
+// Launch the shared-memory-staged (bulk-copy) relayout.  Requires rpu > 0 and,
+// with fused rows, row_bytes / 32 in {2, 4, 8, 16}; units are counted in rows
+// (n_chunks = ceil(plane_rows / rpu), n_units = n_chunks * n_planes).
+cudaError_t launch_relayout_staged(const RelayoutParams& p, Dir dir, Fused fused, cudaStream_t stream);
+
+// Device status word of the staged kernel: 0, or the bitwise OR of the reasons
+// a bounded wait gave up (1: a load never completed; 2: compute never signalled;
+// 4: a compute warp's load wait gave up).  read_staged_status optionally clears it.
+cudaError_t read_staged_status(unsigned* out, bool clear);
 
 // Fill table[S][D/2][2] with (cos, sin) of p * inv_freq[i] evaluated in double.
 cudaError_t launch_rope_table(float* table, const double* inv_freq_host, int S, int D, cudaStream_t stream);

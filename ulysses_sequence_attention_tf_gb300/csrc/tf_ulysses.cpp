@@ -24,6 +24,7 @@
 #include "noalloc.h"
 #include "relayout.h"
 #include "tf_ulysses.h"
+#include "tma_plan.h"
 
 namespace {
 
@@ -176,6 +177,55 @@ tf_status plan_units(RelayoutParams& p, const Shape& sh) {
     p.div_vpr = tfu::make_fastdiv(p.vpr);
     p.div_hl = tfu::make_fastdiv(p.Hl);
     p.div_planes = tfu::make_fastdiv(p.n_planes ? p.n_planes : 1);
+    return TF_OK;
+}
+
+#ifndef TFU_USE_STAGED
+#define TFU_USE_STAGED 1  // staged kernel for pure relayouts (copy scatters, gathers)
+#endif
+#ifndef TFU_STAGED_FUSED
+#define TFU_STAGED_FUSED 0  // staged kernel also for fused scatters (measured slower: off)
+#endif
+
+// Plan and launch one relayout: the shared-memory-staged (bulk-copy) kernel for
+// pure relayouts when a head row fits a stage, else -- and for the fused
+// scatter -- the register kernel with 32- or 16-byte vectors.
+tf_status launch_planned(RelayoutParams& p, const Shape& sh, tfu::Dir dir, tfu::Fused fused, int64_t src_tokens,
+                         int64_t dst_tokens, cudaStream_t stream) {
+    const uint32_t rb = uint32_t(int64_t(sh.D) * sh.esize);
+    // fused units also stage their tokens' cos/sin rows (D fp32 values per token)
+    const uint32_t table_row = fused == tfu::Fused::kNone ? 0u : uint32_t(sh.D) * 4u;
+    const uint32_t rpu = tfu::tma_rows_per_unit(uint32_t(sh.Hl), rb, table_row);
+    const bool lanes_ok = fused == tfu::Fused::kNone || (rb % 32 == 0 && rb / 32 >= 2 && rb / 32 <= 16);
+    cudaError_t e;
+    const bool staged = TFU_USE_STAGED && rpu > 0 && lanes_ok && (fused == tfu::Fused::kNone || TFU_STAGED_FUSED);
+    if (staged) {
+        p.P = uint32_t(sh.P);
+        p.B = uint32_t(sh.B);
+        p.Sl = uint32_t(sh.Sl);
+        p.Hl = uint32_t(sh.Hl);
+        p.row_bytes = rb;
+        p.rpu = rpu;
+        const uint64_t rows = uint64_t(sh.Sl) * uint64_t(sh.Hl);
+        if (rows >= (uint64_t(1) << 31)) return fail(TF_ERR_UNSUPPORTED, "one shard/head-group block exceeds 2^31 rows");
+        p.plane_rows = uint32_t(rows);
+        const uint64_t planes = uint64_t(sh.B) * sh.P * p.nx * sh.P;
+        const uint64_t chunks = (rows + rpu - 1) / rpu;
+        if (planes * chunks >= (uint64_t(1) << 31)) return fail(TF_ERR_UNSUPPORTED, "problem exceeds 2^31 work units");
+        p.n_planes = uint32_t(planes);
+        p.n_chunks = uint32_t(chunks);
+        p.n_units = uint32_t(planes * chunks);
+        p.div_hl = tfu::make_fastdiv(p.Hl);
+        p.div_planes = tfu::make_fastdiv(p.n_planes ? p.n_planes : 1);
+        e = tfu::launch_relayout_staged(p, dir, fused, stream);
+    } else {
+        p.vec_bytes = pick_vec_bytes(p, sh, src_tokens, dst_tokens);
+        tf_status s = plan_units(p, sh);
+        if (s != TF_OK) return s;
+        e = tfu::launch_relayout(p, dir, fused, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "launching the relayout kernel");
+    g_launches.fetch_add(1);
     return TF_OK;
 }
 
@@ -409,12 +459,9 @@ tf_status launch_scatter(ScatterPlan& pl, const tf_norm_rope* nr, int device, cu
         pl.p.table = t->ptr;
         *used = t;
     }
-    pl.p.vec_bytes = pick_vec_bytes(pl.p, pl.sh, pl.sh.Sl, int64_t(pl.sh.P) * pl.sh.Sl);
-    tf_status s = plan_units(pl.p, pl.sh);
+    tf_status s = launch_planned(pl.p, pl.sh, tfu::Dir::kScatter, pl.fused, pl.sh.Sl, int64_t(pl.sh.P) * pl.sh.Sl,
+                                 stream);
     if (s != TF_OK) return s;
-    cudaError_t e = tfu::launch_relayout(pl.p, tfu::Dir::kScatter, pl.fused, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "launching the scatter kernel");
-    g_launches.fetch_add(1);
     if (*used) cudaEventRecord((*used)->last_use, stream);
     return TF_OK;
 }
@@ -545,12 +592,7 @@ TF_API tf_status tf_ulysses_scatter_qkv_noalloc(const void* const* q, const void
         g_launches.fetch_add(1);
         pl.p.table = table;
     }
-    pl.p.vec_bytes = pick_vec_bytes(pl.p, pl.sh, pl.sh.Sl, int64_t(P) * S_local);
-    if ((s = plan_units(pl.p, pl.sh)) != TF_OK) return s;
-    cudaError_t e = tfu::launch_relayout(pl.p, tfu::Dir::kScatter, pl.fused, st);
-    if (e != cudaSuccess) return cuda_fail(e, "launching the scatter kernel");
-    g_launches.fetch_add(1);
-    return TF_OK;
+    return launch_planned(pl.p, pl.sh, tfu::Dir::kScatter, pl.fused, pl.sh.Sl, int64_t(P) * S_local, st);
 }
 
 TF_API tf_status tf_ulysses_gather_out(const char* tag, const void* const* attn, const tf_strides* attn_strides,
@@ -599,11 +641,7 @@ TF_API tf_status tf_ulysses_gather_out(const char* tag, const void* const* attn,
         return s;
     for (int r = 0; r < P; ++r) p.dst[0][r] = static_cast<uint8_t*>(dst ? dst[r] : e->buf[0][r]);
     if (!empty) {
-        p.vec_bytes = pick_vec_bytes(p, sh, S, S_local);
-        if ((s = plan_units(p, sh)) != TF_OK) return s;
-        cudaError_t err = tfu::launch_relayout(p, tfu::Dir::kGather, tfu::Fused::kNone, st);
-        if (err != cudaSuccess) return cuda_fail(err, "launching the gather kernel");
-        g_launches.fetch_add(1);
+        if ((s = launch_planned(p, sh, tfu::Dir::kGather, tfu::Fused::kNone, S, S_local, st)) != TF_OK) return s;
     }
     cudaError_t err = cudaEventRecord(e->done, st);
     if (err != cudaSuccess) return cuda_fail(err, "cudaEventRecord");
@@ -661,6 +699,13 @@ TF_API void tf_ulysses_set_allocator(tf_alloc_fn alloc, tf_free_fn release, void
     } else {
         g_alloc = Allocator{};
     }
+}
+
+TF_API tf_status tf_ulysses_device_status(int clear, unsigned* status) {
+    if (!status) return fail(TF_ERR_INVALID, "status is NULL");
+    cudaError_t e = tfu::read_staged_status(status, clear != 0);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+    return TF_OK;
 }
 
 TF_API const char* tf_ulysses_last_error(void) { return g_last_error.c_str(); }

@@ -1,0 +1,76 @@
+// tma_plan.h -- the work decomposition of the shared-memory-staged relayout
+// kernel, as plain host+device code so it can be checked on the host.
+//
+// A plane (batch b, shard r, slot x, head group g) holds Sl*Hl head rows of
+// row_bytes = D*esize bytes; plane row R = t*Hl + h.  A unit is the row range
+// [c*rpu, min((c+1)*rpu, Sl*Hl)) of one plane, staged whole in one shared-memory
+// stage (rpu*row_bytes <= kStageBytes).  Each unit is loaded with one bulk copy
+// per maximal run of rows that is contiguous in the source and stored with one
+// bulk copy per maximal run contiguous in the destination.
+#pragma once
+
+#include <cstdint>
+
+#ifndef __CUDACC__
+#ifndef __host__
+#define __host__
+#endif
+#ifndef __device__
+#define __device__
+#endif
+#endif
+
+namespace tfu {
+
+constexpr uint32_t kStageBytes = 32768;       // payload bytes of one shared-memory stage
+constexpr uint32_t kStageTableBytes = 16384;  // cos/sin rows staged beside a fused unit's payload
+
+// Rows per unit: whole tokens (all Hl heads) when a token's head band fits a
+// stage, else as many rows as fit.  table_row_bytes > 0 (fused units) also caps
+// the unit's tokens so their cos/sin rows fit kStageTableBytes.  0 if a single
+// row does not fit.
+__host__ __device__ inline uint32_t tma_rows_per_unit(uint32_t Hl, uint32_t row_bytes, uint32_t table_row_bytes = 0) {
+    if (row_bytes == 0 || row_bytes > kStageBytes || Hl == 0) return 0;
+    if (table_row_bytes > kStageTableBytes / 2) return 0;
+    const uint64_t token_bytes = uint64_t(Hl) * row_bytes;
+    if (token_bytes <= kStageBytes) {
+        uint32_t tokens = uint32_t(kStageBytes / token_bytes);
+        if (table_row_bytes && tokens > kStageTableBytes / table_row_bytes) tokens = kStageTableBytes / table_row_bytes;
+        return Hl * tokens;  // units start at token boundaries: a unit spans exactly `tokens` tokens
+    }
+    return uint32_t(kStageBytes / row_bytes);  // fewer rows than a token: a unit spans at most 2 tokens
+}
+
+// Tokens [first, last] touched by the plane rows [R0, R1).
+__host__ __device__ inline void unit_tokens(uint32_t R0, uint32_t R1, uint32_t Hl, uint32_t& first, uint32_t& last) {
+    first = R0 / Hl;
+    last = (R1 - 1) / Hl;
+}
+
+// Calls f(first_row_in_unit, n_rows, byte_offset_in_plane) for each maximal run
+// of rows [R0, R1) that is contiguous under the strides (st per token, sh per
+// head row) of one side of the copy.
+template <class F>
+__host__ __device__ inline void for_each_run(uint32_t R0, uint32_t R1, uint32_t Hl, int64_t st, int64_t sh,
+                                             uint32_t row_bytes, F&& f) {
+    if (R1 <= R0) return;
+    const bool heads_packed = sh == int64_t(row_bytes);
+    if (heads_packed && st == int64_t(Hl) * row_bytes) {  // the whole plane is contiguous
+        f(0u, R1 - R0, int64_t(R0) * row_bytes);
+        return;
+    }
+    uint32_t R = R0;
+    while (R < R1) {
+        const uint32_t t = R / Hl;
+        const uint32_t h = R - t * Hl;
+        uint32_t n = 1;
+        if (heads_packed) {
+            n = Hl - h;
+            if (n > R1 - R) n = R1 - R;
+        }
+        f(R - R0, n, int64_t(t) * st + int64_t(h) * sh);
+        R += n;
+    }
+}
+
+}  // namespace tfu
