@@ -251,12 +251,11 @@ typedef void (*tf_free_fn)(void *ptr, size_t bytes, void *stream, void *ctx);
 TF_API void tf_ulysses_set_allocator(tf_alloc_fn alloc, tf_free_fn release, void *ctx);
 
 /*
- * Device status word of the current device's staged kernels: 0 when every wait
- * completed; otherwise the OR of reasons a bounded in-kernel wait gave up (1: a
- * bulk load never completed, 2: the compute warps never finished a stage, 4: a
- * compute warp gave up waiting for a load) -- the kernel then stopped early and
- * its outputs are incomplete.  Synchronises with the device.  clear != 0 resets
- * the word after reading it.
+ * Device status word of the current device's staged (bulk-copy) kernel: 0 when
+ * every in-kernel wait completed; otherwise bit 0 is set when a bounded wait for
+ * a bulk load gave up -- the kernel then stopped early and its outputs are
+ * incomplete.  Synchronises with the device.  clear != 0 resets the word after
+ * reading it.
  */
 TF_API tf_status tf_ulysses_device_status(int clear, unsigned *status);
 

@@ -27,11 +27,8 @@ int main() {
     const int64_t sh = packed ? rb : int64_t(rb) + 16 * (1 + rnd(8));
     const int64_t band = int64_t(Hl - 1) * sh + rb;
     const int64_t st = rnd(3) == 0 && packed ? int64_t(Hl) * rb : band + 16 * rnd(64);
-    // fused units (16-bit payload) also stage D fp32 cos/sin values per token
-    const uint32_t table_row = (it & 1) ? rb * 2 : 0;
-    const uint32_t rpu = tma_rows_per_unit(Hl, rb, table_row);
+    const uint32_t rpu = tma_rows_per_unit(Hl, rb);
     const uint32_t rows = Sl * Hl;
-    if (table_row > kStageTableBytes / 2) { if (rpu != 0) ++bad; continue; }
     if (rpu == 0 || uint64_t(rpu) * rb > kStageBytes) { ++bad; continue; }
     if (uint64_t(Hl) * rb <= kStageBytes && rpu % Hl != 0) { ++bad; continue; }  // whole tokens
     const int64_t extent = int64_t(Sl - 1) * st + band;
@@ -50,10 +47,6 @@ int main() {
         next = i + n;
       });
       if (next != R1 - R0) ++bad;
-      uint32_t t0, t1;
-      unit_tokens(R0, R1, Hl, t0, t1);
-      if (t0 != R0 / Hl || t1 != (R1 - 1) / Hl || t1 >= Sl) ++bad;
-      if (table_row && uint64_t(t1 - t0 + 1) * table_row > kStageTableBytes) ++bad;  // table rows fit
     }
   }
   // a row larger than a stage is refused

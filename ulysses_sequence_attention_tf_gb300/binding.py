@@ -17,7 +17,8 @@ import threading
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libtf_ulysses.so")
+# the in-tree build, or another build of the same library named by TF_ULYSSES_LIBRARY
+LIB_PATH = os.environ.get("TF_ULYSSES_LIBRARY") or os.path.join(_PKG, "libtf_ulysses.so")
 
 TF_OK, TF_ERR_INVALID, TF_ERR_DIVISIBILITY, TF_ERR_ALIGNMENT = 0, 1, 2, 3
 TF_ERR_UNSUPPORTED, TF_ERR_OOM, TF_ERR_CUDA, TF_ERR_BUSY = 4, 5, 6, 7

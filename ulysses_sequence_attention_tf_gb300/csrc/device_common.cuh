@@ -182,26 +182,14 @@ __device__ __forceinline__ void f2_two_sum(uint64_t a, uint64_t b, uint64_t& s, 
 }
 
 // One lane's NP element pairs of a head row spread over kLanes lanes: RMSNorm,
-// weight scale (wpk: the lane's weights as packed pairs) and interleaved RoPE
-// with the lane's NP (cos, sin) pairs at tab[0 .. 2*NP) -- in shared memory when
-// kSmemTable, else read through the read-only global path.
-template <Fused kF, int kLanes, int NP, bool kSmemTable = false>
-__device__ __forceinline__ void norm_rope_lane(uint32_t (&xw)[NP], const uint32_t (&wpk)[NP], const float* tab,
-                                               bool valid, float eps) {
+// weight scale (wpk: the lane's weights as packed pairs) and interleaved RoPE.
+// The arithmetic of one lane: xw holds NP element pairs of one head row (the
+// row spread over kLanes lanes), wpk the matching weight pairs, cs the matching
+// (cos, sin) pairs, two per float4.  The pairs need not be contiguous in the row.
+template <Fused kF, int kLanes, int NP>
+__device__ __forceinline__ void norm_rope_core(uint32_t (&xw)[NP], const uint32_t (&wpk)[NP],
+                                               const float4 (&cs)[NP / 2], float eps) {
     constexpr float kInvD = 1.0f / float(kLanes * NP * 2);  // D is a power of two: exact scaling
-    float4 cs[NP / 2];
-#pragma unroll
-    for (int k = 0; k < NP / 2; ++k) cs[k] = make_float4(1.f, 0.f, 1.f, 0.f);
-    if (valid) {  // issued first: the reduction below hides its latency
-#pragma unroll
-        for (int k = 0; k < NP / 2; ++k) {
-            if constexpr (kSmemTable) {
-                cs[k] = reinterpret_cast<const float4*>(tab)[k];
-            } else {
-                cs[k] = ld_table(tab + 4 * k);
-            }
-        }
-    }
     uint64_t x2[NP];  // the lane's values as fp32 pairs
 #pragma unroll
     for (int j = 0; j < NP; ++j) {
@@ -262,6 +250,28 @@ __device__ __forceinline__ void norm_rope_lane(uint32_t (&xw)[NP], const uint32_
         const float s = (j & 1) ? c4.w : c4.y;
         xw[j] = pack2<kF>(__fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s)), __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c)));
     }
+}
+
+// norm_rope_core with the lane's NP contiguous (cos, sin) pairs at tab[0 .. 2*NP),
+// in shared memory when kSmemTable, else read through the read-only global path
+// (issued first, so the reduction hides their latency).
+template <Fused kF, int kLanes, int NP, bool kSmemTable = false>
+__device__ __forceinline__ void norm_rope_lane(uint32_t (&xw)[NP], const uint32_t (&wpk)[NP], const float* tab,
+                                               bool valid, float eps) {
+    float4 cs[NP / 2];
+#pragma unroll
+    for (int k = 0; k < NP / 2; ++k) cs[k] = make_float4(1.f, 0.f, 1.f, 0.f);
+    if (valid) {
+#pragma unroll
+        for (int k = 0; k < NP / 2; ++k) {
+            if constexpr (kSmemTable) {
+                cs[k] = reinterpret_cast<const float4*>(tab)[k];
+            } else {
+                cs[k] = ld_table(tab + 4 * k);
+            }
+        }
+    }
+    norm_rope_core<kF, kLanes, NP>(xw, wpk, cs, eps);
 }
 
 }  // namespace dev

@@ -11,7 +11,10 @@ namespace tfu {
 constexpr int kMaxShards = 8;
 constexpr int kMaxSlots = 3;      // Q, K, V
 constexpr int kThreads = 256;          // threads per CTA
-constexpr int kChunkBytes = 32768;     // payload bytes per work unit
+#ifndef TFU_CHUNK_BYTES
+#define TFU_CHUNK_BYTES 32768
+#endif
+constexpr int kChunkBytes = TFU_CHUNK_BYTES;  // payload bytes per work unit of the register kernel
 __host__ __device__ constexpr int chunk_vecs(int vec_bytes) { return kChunkBytes / vec_bytes; }
 
 // Unsigned 32-bit division by an invariant divisor as multiply-high, add and
@@ -78,14 +81,13 @@ struct RelayoutParams {
 // fused kernels the head row holds p.vpr vectors, D in {32, 64, 128, 256}).
 cudaError_t launch_relayout(const RelayoutParams& p, Dir dir, Fused fused, cudaStream_t stream);
 
-// Launch the shared-memory-staged (bulk-copy) relayout.  Requires rpu > 0 and,
-// with fused rows, row_bytes / 32 in {2, 4, 8, 16}; units are counted in rows
+// Launch the shared-memory-staged (bulk-copy) relayout of a pure relayout
+// (no fused rows).  Requires rpu > 0; units are counted in rows
 // (n_chunks = ceil(plane_rows / rpu), n_units = n_chunks * n_planes).
 cudaError_t launch_relayout_staged(const RelayoutParams& p, Dir dir, Fused fused, cudaStream_t stream);
 
-// Device status word of the staged kernel: 0, or the bitwise OR of the reasons
-// a bounded wait gave up (1: a load never completed; 2: compute never signalled;
-// 4: a compute warp's load wait gave up).  read_staged_status optionally clears it.
+// Device status word of the staged kernel: 0, or 1 when a bounded wait for a
+// bulk load gave up.  read_staged_status optionally clears it.
 cudaError_t read_staged_status(unsigned* out, bool clear);
 
 // Fill table[S][D/2][2] with (cos, sin) of p * inv_freq[i] evaluated in double.

@@ -74,10 +74,20 @@ __device__ __forceinline__ void copy_range(const RelayoutParams& p, const Plane&
     }
 }
 
+#ifndef TFU_FUSED_PIPELINE
+#define TFU_FUSED_PIPELINE 1  // 1: software-pipelined half batches, 0: load-all-then-compute batches
+#endif
+
+// Fused Q/K rows of one unit.  VB slots per thread; pipelined as two half
+// batches of VB/2 slots: the loads of one half are in flight while the other
+// half is normalised, rotated and stored, so a warp never computes with no
+// loads outstanding.
 template <Fused kF, int VW, int kLanes, int VB>
 __device__ __forceinline__ void norm_rope_range(const RelayoutParams& p, const Plane& pl, uint32_t v0, uint32_t v1) {
     constexpr int NP = VW / 4;                    // element pairs per lane
     constexpr int kRowFloats = kLanes * NP * 2;  // D floats per table row: D/2 (cos, sin) pairs
+    constexpr int H = TFU_FUSED_PIPELINE ? VB / 2 : VB;
+    constexpr uint32_t kStep = uint32_t(kThreads) * H;  // vectors per half batch
     const uint32_t dv = threadIdx.x % kLanes;    // v0 and kThreads are multiples of kLanes
     uint32_t wpk[NP];
     {
@@ -86,11 +96,9 @@ __device__ __forceinline__ void norm_rope_range(const RelayoutParams& p, const P
         for (int j = 0; j < NP; ++j) wpk[j] = wv.w[j];
     }
     const float* tab_lane = p.table + size_t(pl.pos0) * kRowFloats + dv * (2 * NP);
-#pragma unroll 1
-    for (uint32_t base = v0; base < v1; base += kThreads * VB) {
-        Vec<VW> buf[VB];
+    auto load = [&](Vec<VW>(&buf)[H], uint32_t base) {
 #pragma unroll
-        for (int i = 0; i < VB; ++i) {
+        for (int i = 0; i < H; ++i) {
             const uint32_t v = base + i * kThreads + threadIdx.x;
 #pragma unroll
             for (int j = 0; j < NP; ++j) buf[i].w[j] = 0u;
@@ -101,14 +109,107 @@ __device__ __forceinline__ void norm_rope_range(const RelayoutParams& p, const P
                 buf[i] = ld_stream<VW>(pl.src + int64_t(t) * pl.st + int64_t(h) * pl.sh + int64_t(dv) * VW);
             }
         }
+    };
+    auto compute_store = [&](Vec<VW>(&buf)[H], uint32_t base) {
 #pragma unroll
-        for (int i = 0; i < VB; ++i) {
+        for (int i = 0; i < H; ++i) {
             const uint32_t v = base + i * kThreads + threadIdx.x;
             const uint32_t t = fastdiv(v / kLanes, p.div_hl);
             // every lane runs the row reduction (it shuffles); only valid lanes load and store
             norm_rope_lane<kF, kLanes, NP>(buf[i].w, wpk, tab_lane + size_t(t) * kRowFloats, v < v1, p.eps);
             if (v < v1) st_stream<VW>(pl.dst + int64_t(v) * VW, buf[i]);
         }
+    };
+    Vec<VW> a[H];
+    if constexpr (TFU_FUSED_PIPELINE) {
+        Vec<VW> b[H];
+        load(a, v0);
+#pragma unroll 1
+        for (uint32_t base = v0; base < v1; base += 2 * kStep) {
+            load(b, base + kStep);  // fully masked past the end of the range
+            compute_store(a, base);
+            load(a, base + 2 * kStep);
+            compute_store(b, base + kStep);
+        }
+    } else {
+#pragma unroll 1
+        for (uint32_t base = v0; base < v1; base += kStep) {
+            load(a, base);
+            compute_store(a, base);
+        }
+    }
+}
+
+#ifndef TFU_FUSED_ROWMAJOR
+#define TFU_FUSED_ROWMAJOR 1  // 1: row runs per lane group (norm_rope_rows), 0: norm_rope_range
+#endif
+
+// Fused Q/K rows of one unit, row-major: the CTA's kThreads / kLanes row groups
+// each take a contiguous run of the unit's rows and walk it with four rows' loads
+// in flight (software pipeline).  Consecutive rows of a run mostly belong to the
+// same token (Hl heads per token), so a lane reloads its (cos, sin) pairs only
+// when the token changes.
+template <Fused kF, int VW, int kLanes>
+__device__ __forceinline__ void norm_rope_rows(const RelayoutParams& p, const Plane& pl, uint32_t v0, uint32_t v1) {
+    constexpr int NP = VW / 4;                    // element pairs per lane
+    constexpr int kRowFloats = kLanes * NP * 2;  // D floats per table row: D/2 (cos, sin) pairs
+    constexpr uint32_t kGroups = kThreads / kLanes;
+    const uint32_t g = threadIdx.x / kLanes, dv = threadIdx.x % kLanes;
+    const uint32_t row0 = v0 / kLanes;  // first plane row of the unit (v0 is a multiple of kLanes)
+    const uint32_t n_rows = (v1 - v0) / kLanes;
+    const uint32_t per = (n_rows + kGroups - 1) / kGroups;  // rows per group, the same for every lane
+    const uint32_t r_beg = g * per;
+    uint32_t wpk[NP];
+    {
+        const Vec<VW> wv = *reinterpret_cast<const Vec<VW>*>(static_cast<const uint8_t*>(p.weight[pl.x]) + dv * VW);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) wpk[j] = wv.w[j];
+    }
+    const float* tab_lane = p.table + size_t(pl.pos0) * kRowFloats + dv * (2 * NP);
+    float4 cs[NP / 2];
+#pragma unroll
+    for (int k = 0; k < NP / 2; ++k) cs[k] = make_float4(1.f, 0.f, 1.f, 0.f);
+    uint32_t t_cached = 0xffffffffu;
+    auto load = [&](Vec<VW>& buf, uint32_t j) {
+        const uint32_t i = r_beg + j;
+#pragma unroll
+        for (int w = 0; w < NP; ++w) buf.w[w] = 0u;
+        if (j < per && i < n_rows) {
+            const uint32_t R = row0 + i;
+            const uint32_t t = fastdiv(R, p.div_hl);
+            const uint32_t h = R - t * p.Hl;
+            buf = ld_stream<VW>(pl.src + int64_t(t) * pl.st + int64_t(h) * pl.sh + int64_t(dv) * VW);
+        }
+    };
+    auto compute_store = [&](Vec<VW>& buf, uint32_t j) {
+        const uint32_t i = r_beg + j;
+        const bool valid = j < per && i < n_rows;
+        const uint32_t t = fastdiv(row0 + i, p.div_hl);
+        if (valid && t != t_cached) {
+            const float* tab = tab_lane + size_t(t) * kRowFloats;
+#pragma unroll
+            for (int k = 0; k < NP / 2; ++k) cs[k] = ld_table(tab + 4 * k);
+            t_cached = t;
+        }
+        // every lane runs the row reduction (it shuffles); only valid rows are written
+        norm_rope_core<kF, kLanes, NP>(buf.w, wpk, cs, p.eps);
+        if (valid) st_stream<VW>(pl.dst + int64_t(row0 + i) * (kLanes * VW) + int64_t(dv) * VW, buf);
+    };
+    Vec<VW> b0, b1, b2, b3;
+    load(b0, 0);
+    load(b1, 1);
+    load(b2, 2);
+    load(b3, 3);
+#pragma unroll 1
+    for (uint32_t j = 0; j < per; j += 4) {
+        compute_store(b0, j);
+        load(b0, j + 4);
+        compute_store(b1, j + 1);
+        load(b1, j + 5);
+        compute_store(b2, j + 2);
+        load(b2, j + 6);
+        compute_store(b3, j + 3);
+        load(b3, j + 7);
     }
 }
 
@@ -154,7 +255,11 @@ __global__ void __launch_bounds__(kThreads, min_blocks<kF>()) relayout_kernel(co
         const uint32_t v1 = min(v0 + kChunk, p.nv);
         if constexpr (kF != Fused::kNone) {
             if ((p.fused_mask >> pl.x) & 1u) {
-                norm_rope_range<kF, VW, kLanes, fused_batch<VW>()>(p, pl, v0, v1);
+                if constexpr (TFU_FUSED_ROWMAJOR) {
+                    norm_rope_rows<kF, VW, kLanes>(p, pl, v0, v1);
+                } else {
+                    norm_rope_range<kF, VW, kLanes, fused_batch<VW>()>(p, pl, v0, v1);
+                }
                 continue;
             }
         }

@@ -183,22 +183,15 @@ tf_status plan_units(RelayoutParams& p, const Shape& sh) {
 #ifndef TFU_USE_STAGED
 #define TFU_USE_STAGED 1  // staged kernel for pure relayouts (copy scatters, gathers)
 #endif
-#ifndef TFU_STAGED_FUSED
-#define TFU_STAGED_FUSED 0  // staged kernel also for fused scatters (measured slower: off)
-#endif
-
 // Plan and launch one relayout: the shared-memory-staged (bulk-copy) kernel for
 // pure relayouts when a head row fits a stage, else -- and for the fused
 // scatter -- the register kernel with 32- or 16-byte vectors.
 tf_status launch_planned(RelayoutParams& p, const Shape& sh, tfu::Dir dir, tfu::Fused fused, int64_t src_tokens,
                          int64_t dst_tokens, cudaStream_t stream) {
     const uint32_t rb = uint32_t(int64_t(sh.D) * sh.esize);
-    // fused units also stage their tokens' cos/sin rows (D fp32 values per token)
-    const uint32_t table_row = fused == tfu::Fused::kNone ? 0u : uint32_t(sh.D) * 4u;
-    const uint32_t rpu = tfu::tma_rows_per_unit(uint32_t(sh.Hl), rb, table_row);
-    const bool lanes_ok = fused == tfu::Fused::kNone || (rb % 32 == 0 && rb / 32 >= 2 && rb / 32 <= 16);
+    const uint32_t rpu = tfu::tma_rows_per_unit(uint32_t(sh.Hl), rb);
     cudaError_t e;
-    const bool staged = TFU_USE_STAGED && rpu > 0 && lanes_ok && (fused == tfu::Fused::kNone || TFU_STAGED_FUSED);
+    const bool staged = TFU_USE_STAGED && rpu > 0 && fused == tfu::Fused::kNone;
     if (staged) {
         p.P = uint32_t(sh.P);
         p.B = uint32_t(sh.B);

@@ -22,29 +22,15 @@
 
 namespace tfu {
 
-constexpr uint32_t kStageBytes = 32768;       // payload bytes of one shared-memory stage
-constexpr uint32_t kStageTableBytes = 16384;  // cos/sin rows staged beside a fused unit's payload
+constexpr uint32_t kStageBytes = 32768;  // bytes of one shared-memory stage
 
 // Rows per unit: whole tokens (all Hl heads) when a token's head band fits a
-// stage, else as many rows as fit.  table_row_bytes > 0 (fused units) also caps
-// the unit's tokens so their cos/sin rows fit kStageTableBytes.  0 if a single
-// row does not fit.
-__host__ __device__ inline uint32_t tma_rows_per_unit(uint32_t Hl, uint32_t row_bytes, uint32_t table_row_bytes = 0) {
+// stage, else as many rows as fit.  0 if a single row does not fit.
+__host__ __device__ inline uint32_t tma_rows_per_unit(uint32_t Hl, uint32_t row_bytes) {
     if (row_bytes == 0 || row_bytes > kStageBytes || Hl == 0) return 0;
-    if (table_row_bytes > kStageTableBytes / 2) return 0;
     const uint64_t token_bytes = uint64_t(Hl) * row_bytes;
-    if (token_bytes <= kStageBytes) {
-        uint32_t tokens = uint32_t(kStageBytes / token_bytes);
-        if (table_row_bytes && tokens > kStageTableBytes / table_row_bytes) tokens = kStageTableBytes / table_row_bytes;
-        return Hl * tokens;  // units start at token boundaries: a unit spans exactly `tokens` tokens
-    }
-    return uint32_t(kStageBytes / row_bytes);  // fewer rows than a token: a unit spans at most 2 tokens
-}
-
-// Tokens [first, last] touched by the plane rows [R0, R1).
-__host__ __device__ inline void unit_tokens(uint32_t R0, uint32_t R1, uint32_t Hl, uint32_t& first, uint32_t& last) {
-    first = R0 / Hl;
-    last = (R1 - 1) / Hl;
+    if (token_bytes <= kStageBytes) return Hl * uint32_t(kStageBytes / token_bytes);
+    return uint32_t(kStageBytes / row_bytes);
 }
 
 // Calls f(first_row_in_unit, n_rows, byte_offset_in_plane) for each maximal run
