@@ -387,6 +387,61 @@ def test_padding_rows_normalise_to_zero(tf):
     assert int(ulp_diff(tq[0].cpu(), want[0]).max()) <= 1
 
 
+# ------------------------------------------------------------------ fused: slot patterns, head dims, unit tails
+@pytest.mark.parametrize("with_k,with_v", [(True, True), (True, False), (False, True), (False, False)])
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+def test_fused_slot_patterns_and_head_dims(tf, with_k, with_v, D):
+    """Q alone, Q+K, Q+V, Q+K+V, for every supported D; 3 * 37 * Hl rows per block
+    do not fill whole units of token blocks, and B=2 covers the batch stride."""
+    P, B, Sl, H = 3, 2, 37, 6
+    dtype = torch.bfloat16 if D != 64 else torch.float16
+    d = synth.qkv_shards(P, B, Sl, H, D, dtype, seed=40 + D, layout="fused", with_k=with_k, with_v=with_v)
+    wq, wk = synth.norm_weights(D, dtype, seed=D)
+    g = to_device_like(d)
+    tq, tk, tv, _ = tf.scatter_qkv(f"slots{D}{with_k}{with_v}", g["q"], g["k"], g["v"], norm_rope=True,
+                                   q_weight=wq.cuda(), k_weight=wk.cuda(), eps=EPS, theta=THETA)
+    assert (tk is None) == (not with_k) and (tv is None) == (not with_v)
+    table = oracle.rope_table(THETA, P * Sl, D)
+    fused = [("q", tq, wq)] + ([("k", tk, wk)] if with_k else [])
+    for key, tg, w in fused:
+        want = oracle.scatter_norm_rope(d[key], P, w, EPS, table)
+        for i in range(P):
+            assert_fused_ok(tg[i], want[i])
+    if with_v:
+        want_v = oracle.scatter(d["v"], P)
+        for i in range(P):
+            assert bits_equal(tv[i].cpu(), want_v[i])
+
+
+def test_fused_16_byte_aligned_sources(tf):
+    """Sources only 16-byte aligned (an 8-element offset into the projection):
+    the fused scatter falls back to 16-byte vectors with the same results."""
+    P, B, Sl, H, D = 2, 1, 300, 4, 128
+    dtype = torch.bfloat16
+    gen = torch.Generator().manual_seed(77)
+    HD = H * D
+    bufs = [torch.randn(B, Sl, 3 * HD + 8, generator=gen).to(dtype) for _ in range(P)]
+    q = [b[..., 8:8 + HD].unflatten(-1, (H, D)) for b in bufs]
+    k = [b[..., 8 + HD:8 + 2 * HD].unflatten(-1, (H, D)) for b in bufs]
+    v = [b[..., 8 + 2 * HD:8 + 3 * HD].unflatten(-1, (H, D)) for b in bufs]
+    wq, wk = synth.norm_weights(D, dtype, seed=77)
+    gb = [b.cuda() for b in bufs]
+    gq = [b[..., 8:8 + HD].unflatten(-1, (H, D)) for b in gb]
+    gk = [b[..., 8 + HD:8 + 2 * HD].unflatten(-1, (H, D)) for b in gb]
+    gv = [b[..., 8 + 2 * HD:8 + 3 * HD].unflatten(-1, (H, D)) for b in gb]
+    assert gq[0].data_ptr() % 32 == 16
+    tq, tk, tv, _ = tf.scatter_qkv("align16", gq, gk, gv, norm_rope=True, q_weight=wq.cuda(), k_weight=wk.cuda(),
+                                   eps=EPS, theta=THETA)
+    table = oracle.rope_table(THETA, P * Sl, D)
+    for src, tg, w in ((q, tq, wq), (k, tk, wk)):
+        want = oracle.scatter_norm_rope(src, P, w, EPS, table)
+        for i in range(P):
+            assert_fused_ok(tg[i], want[i])
+    want_v = oracle.scatter(v, P)
+    for i in range(P):
+        assert bits_equal(tv[i].cpu(), want_v[i])
+
+
 def test_device_status_clean_after_all_launches(tf):
     """No bounded in-kernel wait gave up during any launch of this module."""
     torch.cuda.synchronize()

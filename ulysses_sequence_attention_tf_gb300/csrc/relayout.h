@@ -86,6 +86,13 @@ cudaError_t launch_relayout(const RelayoutParams& p, Dir dir, Fused fused, cudaS
 // (n_chunks = ceil(plane_rows / rpu), n_units = n_chunks * n_planes).
 cudaError_t launch_relayout_staged(const RelayoutParams& p, Dir dir, Fused fused, cudaStream_t stream);
 
+// Launch the scatter over token blocks of all slots together (copied slots
+// first, then the fused ones, normalised and rotated in the same pass).
+// Requires vec_bytes == 32, vpr in {2, 4, 8, 16}, and units counted in rows of
+// one (b, r, g) block: n_planes = B * P * P, rpu = rows per unit,
+// n_chunks = ceil(plane_rows / rpu).  Destination rows are d_h bytes apart.
+cudaError_t launch_blocks(const RelayoutParams& p, Fused fused, cudaStream_t stream);
+
 // Device status word of the staged kernel: 0, or 1 when a bounded wait for a
 // bulk load gave up.  read_staged_status optionally clears it.
 cudaError_t read_staged_status(unsigned* out, bool clear);

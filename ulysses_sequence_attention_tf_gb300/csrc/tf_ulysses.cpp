@@ -183,38 +183,63 @@ tf_status plan_units(RelayoutParams& p, const Shape& sh) {
 #ifndef TFU_USE_STAGED
 #define TFU_USE_STAGED 1  // staged kernel for pure relayouts (copy scatters, gathers)
 #endif
-// Plan and launch one relayout: the shared-memory-staged (bulk-copy) kernel for
-// pure relayouts when a head row fits a stage, else -- and for the fused
-// scatter -- the register kernel with 32- or 16-byte vectors.
+#ifndef TFU_FUSED_BLOCKS
+#define TFU_FUSED_BLOCKS 1  // fused scatter with 32-byte vectors: one pass over token blocks of all slots
+#endif
+#ifndef TFU_COPY_BLOCKS
+#define TFU_COPY_BLOCKS 0  // the same single pass for copy scatters (else the staged kernel)
+#endif
+#ifndef TFU_BLOCK_ROWS
+#define TFU_BLOCK_ROWS 128  // rows of one (b, r, g) block per unit of the block kernel
+#endif
+
+// Plan and launch one relayout:
+//  * scatters with 32-byte vectors and D * esize in {64, 128, 256, 512} bytes
+//    (fused always, copies when TFU_COPY_BLOCKS): the block kernel, all slots
+//    of a token block in one pass;
+//  * other pure relayouts whose head row fits a stage: the shared-memory-staged
+//    (bulk-copy) kernel;
+//  * the rest: the register kernel with 32- or 16-byte vectors.
 tf_status launch_planned(RelayoutParams& p, const Shape& sh, tfu::Dir dir, tfu::Fused fused, int64_t src_tokens,
                          int64_t dst_tokens, cudaStream_t stream) {
     const uint32_t rb = uint32_t(int64_t(sh.D) * sh.esize);
-    const uint32_t rpu = tfu::tma_rows_per_unit(uint32_t(sh.Hl), rb);
-    cudaError_t e;
-    const bool staged = TFU_USE_STAGED && rpu > 0 && fused == tfu::Fused::kNone;
-    if (staged) {
-        p.P = uint32_t(sh.P);
-        p.B = uint32_t(sh.B);
-        p.Sl = uint32_t(sh.Sl);
-        p.Hl = uint32_t(sh.Hl);
-        p.row_bytes = rb;
-        p.rpu = rpu;
-        const uint64_t rows = uint64_t(sh.Sl) * uint64_t(sh.Hl);
-        if (rows >= (uint64_t(1) << 31)) return fail(TF_ERR_UNSUPPORTED, "one shard/head-group block exceeds 2^31 rows");
-        p.plane_rows = uint32_t(rows);
-        const uint64_t planes = uint64_t(sh.B) * sh.P * p.nx * sh.P;
+    const uint64_t rows = uint64_t(sh.Sl) * uint64_t(sh.Hl);
+    if (rows >= (uint64_t(1) << 31)) return fail(TF_ERR_UNSUPPORTED, "one shard/head-group block exceeds 2^31 rows");
+    p.P = uint32_t(sh.P);
+    p.B = uint32_t(sh.B);
+    p.Sl = uint32_t(sh.Sl);
+    p.Hl = uint32_t(sh.Hl);
+    p.row_bytes = rb;
+    p.plane_rows = uint32_t(rows);
+    p.div_hl = tfu::make_fastdiv(p.Hl);
+    // row-unit grids (block and staged kernels): `blocks` row ranges of rpu rows
+    auto plan_rows = [&](uint64_t blocks, uint32_t rpu) -> tf_status {
         const uint64_t chunks = (rows + rpu - 1) / rpu;
-        if (planes * chunks >= (uint64_t(1) << 31)) return fail(TF_ERR_UNSUPPORTED, "problem exceeds 2^31 work units");
-        p.n_planes = uint32_t(planes);
+        if (blocks * chunks >= (uint64_t(1) << 31)) return fail(TF_ERR_UNSUPPORTED, "problem exceeds 2^31 work units");
+        p.rpu = rpu;
+        p.n_planes = uint32_t(blocks);
         p.n_chunks = uint32_t(chunks);
-        p.n_units = uint32_t(planes * chunks);
-        p.div_hl = tfu::make_fastdiv(p.Hl);
+        p.n_units = uint32_t(blocks * chunks);
         p.div_planes = tfu::make_fastdiv(p.n_planes ? p.n_planes : 1);
+        return TF_OK;
+    };
+    tf_status s;
+    cudaError_t e;
+    const bool block_ok = dir == tfu::Dir::kScatter && (rb == 64 || rb == 128 || rb == 256 || rb == 512) &&
+                          (fused != tfu::Fused::kNone ? TFU_FUSED_BLOCKS : TFU_COPY_BLOCKS);
+    const uint32_t vec = pick_vec_bytes(p, sh, src_tokens, dst_tokens);
+    const uint32_t rpu = tfu::tma_rows_per_unit(uint32_t(sh.Hl), rb);
+    if (block_ok && vec == 32) {
+        p.vec_bytes = 32;
+        p.vpr = rb / 32;
+        if ((s = plan_rows(uint64_t(sh.B) * sh.P * sh.P, TFU_BLOCK_ROWS)) != TF_OK) return s;
+        e = tfu::launch_blocks(p, fused, stream);
+    } else if (TFU_USE_STAGED && rpu > 0 && fused == tfu::Fused::kNone) {
+        if ((s = plan_rows(uint64_t(sh.B) * sh.P * p.nx * sh.P, rpu)) != TF_OK) return s;
         e = tfu::launch_relayout_staged(p, dir, fused, stream);
     } else {
-        p.vec_bytes = pick_vec_bytes(p, sh, src_tokens, dst_tokens);
-        tf_status s = plan_units(p, sh);
-        if (s != TF_OK) return s;
+        p.vec_bytes = vec;
+        if ((s = plan_units(p, sh)) != TF_OK) return s;
         e = tfu::launch_relayout(p, dir, fused, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "launching the relayout kernel");
