@@ -10,7 +10,9 @@ Definitions and their sources are documented in ``tf_oracle.c``:
   * scatter  T_g[b, r*Sl + t, h, d] = S_r[b, t, g*Hl + h, d]
     (TeleFuser docs "Communication Architecture", Ulysses section)
   * gather   O_r[b, t, g*Hl + h, d] = A_g[b, r*Sl + t, h, d]   (same section)
-  * RMSNorm + interleaved RoPE on Q/K rows (flashinfer PR #6332, "Assumptions")
+  * RMSNorm + interleaved RoPE on Q/K rows (flashinfer PR #6332, "Assumptions"),
+    and the half-split pairing (i, i + D/2) as a variant
+  * the fused receive layout (flashinfer PR #6332, "Description", "Layouts")
 """
 from __future__ import annotations
 
@@ -62,7 +64,9 @@ def load(path: str | None = None):
         lib.tfo_rope_table.restype = None
         lib.tfo_rmsnorm_rope_row.argtypes = [i32, i32, vp, vp, ctypes.c_float, vp, vp]
         lib.tfo_rmsnorm_rope_row.restype = None
-        lib.tfo_scatter_norm_rope.argtypes = [i32] * 6 + [vp, i64, i64, i64, vp, ctypes.c_float, vp, vp]
+        lib.tfo_rmsnorm_rope_neox_row.argtypes = [i32, i32, vp, vp, ctypes.c_float, vp, vp]
+        lib.tfo_rmsnorm_rope_neox_row.restype = None
+        lib.tfo_scatter_norm_rope.argtypes = [i32] * 6 + [vp, i64, i64, i64, vp, ctypes.c_float, vp, vp, i32]
         lib.tfo_scatter_norm_rope.restype = None
         if path is None:
             _lib = lib
@@ -117,19 +121,30 @@ def rope_table(theta: float, S: int, D: int, lib=None) -> torch.Tensor:
     return out
 
 
-def rmsnorm_rope_row(x: torch.Tensor, w: torch.Tensor, eps: float, cs_row: torch.Tensor, lib=None):
-    """RMSNorm + weight + interleaved RoPE of one head row ``x[D]`` with table row ``cs_row[D/2, 2]``."""
+ROPE_STYLES = ("interleaved", "neox")
+
+
+def rmsnorm_rope_row(x: torch.Tensor, w: torch.Tensor, eps: float, cs_row: torch.Tensor, lib=None,
+                     style: str = "interleaved"):
+    """RMSNorm + weight + RoPE of one head row ``x[D]`` with table row ``cs_row[D/2, 2]``:
+    pairs (2i, 2i+1) for ``style="interleaved"``, (i, i + D/2) for ``style="neox"``."""
+    if style not in ROPE_STYLES:
+        raise ValueError(f"unknown RoPE style {style!r}")
     lib = lib or load()
     x, w, cs_row = x.contiguous(), w.contiguous(), cs_row.contiguous()
     _check_cpu([x, w, cs_row])
     out = torch.empty_like(x)
-    lib.tfo_rmsnorm_rope_row(FMT[x.dtype], x.numel(), x.data_ptr(), w.data_ptr(), eps,
-                             cs_row.data_ptr(), out.data_ptr())
+    fn = lib.tfo_rmsnorm_rope_neox_row if style == "neox" else lib.tfo_rmsnorm_rope_row
+    fn(FMT[x.dtype], x.numel(), x.data_ptr(), w.data_ptr(), eps, cs_row.data_ptr(), out.data_ptr())
     return out
 
 
-def scatter_norm_rope(srcs, P: int, w: torch.Tensor, eps: float, table: torch.Tensor, lib=None):
-    """Scatter of one Q or K tensor with RMSNorm + RoPE at global positions p = r*Sl + t."""
+def scatter_norm_rope(srcs, P: int, w: torch.Tensor, eps: float, table: torch.Tensor, lib=None,
+                      style: str = "interleaved"):
+    """Scatter of one Q or K tensor with RMSNorm + RoPE (``style`` as in
+    ``rmsnorm_rope_row``) at global positions p = r*Sl + t."""
+    if style not in ROPE_STYLES:
+        raise ValueError(f"unknown RoPE style {style!r}")
     lib = lib or load()
     w, table = w.contiguous(), table.contiguous()
     _check_cpu(list(srcs) + [w, table])
@@ -140,8 +155,16 @@ def scatter_norm_rope(srcs, P: int, w: torch.Tensor, eps: float, table: torch.Te
     Hl = H // P
     dsts = [torch.empty((B, P * Sl, Hl, D), dtype=srcs[0].dtype) for _ in range(P)]
     lib.tfo_scatter_norm_rope(FMT[srcs[0].dtype], P, B, Sl, H, D, _ptrs(srcs), sb, st, sh,
-                              w.data_ptr(), eps, table.data_ptr(), _ptrs(dsts))
+                              w.data_ptr(), eps, table.data_ptr(), _ptrs(dsts), int(style == "neox"))
     return dsts
+
+
+def fused_payload(tq, tk, tv):
+    """The fused receive layout of one scatter: per head group g the payload
+    ``[B, S, Hl, 3*D]`` whose head row is the Q row, then the K row, then the V
+    row of the separate targets (flashinfer PR #6332, "Description", layout
+    "fused"; its 2-D form ``[B*S, 3*Hl*D]`` is the same memory)."""
+    return [torch.cat([q, k, v], dim=-1) for q, k, v in zip(tq, tk, tv)]
 
 
 def decode16(dtype, bits: int) -> float:

@@ -1,6 +1,6 @@
 /*
  * tf_oracle.c -- plain, slow CPU oracle for the Ulysses sequence<->head relayout
- * and the fused per-head RMSNorm + interleaved RoPE applied to Q/K.
+ * and the fused per-head RMSNorm + RoPE (interleaved, or half-split) applied to Q/K.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product library calls, links or
  * includes this file; only the test suite, the package's smoke check and the
@@ -27,7 +27,9 @@
  *  - rounding to the 16-bit type happens after normalising, after the weight
  *    scale and after the rotation, each time round-to-nearest-even from fp32;
  *  - RoPE pair i of a head uses frequency theta^(-2i/D) at the global token
- *    index p = r*S_local + t; cos and sin are evaluated in double and stored as fp32.
+ *    index p = r*S_local + t; cos and sin are evaluated in double and stored as fp32;
+ *  - the half-split variant (not on the pages, which name only the interleaved
+ *    form) pairs element i with i + D/2 and uses the same table entry i.
  *
  * Build: gcc -std=c11 -O2 -ffp-contract=off -fPIC -shared (no FMA contraction, so
  * every float expression below is rounded to fp32 after each operation).
@@ -187,18 +189,15 @@ static float round16(int fmt, float v)
 }
 
 /*
- * One head row x[0..D) (16-bit, format fmt) at a token whose table row is cs:
+ * RMSNorm and weight scale of one head row x[0..D) (16-bit, format fmt):
  *   ms  = mean(x^2)                     (sum in double, mean rounded to fp32)
  *   inv = 1 / sqrt(ms + eps)            (fp32)
  *   y   = round16(x * inv)              (normalised value cast before the scale)
  *   z   = round16(y * w)                (16-bit weight scale, product in fp32)
- *   o[2i]   = round16(z[2i]*cos - z[2i+1]*sin)
- *   o[2i+1] = round16(z[2i]*sin + z[2i+1]*cos)
  */
-void tfo_rmsnorm_rope_row(int fmt, int D, const uint16_t *x, const uint16_t *w,
-                          float eps, const float *cs, uint16_t *out)
+static void rmsnorm_scale(int fmt, int D, const uint16_t *x, const uint16_t *w, float eps, float *z)
 {
-    float xf[1024], y[1024], z[1024];
+    float xf[1024], y[1024];
     double ss = 0.0;
     for (int d = 0; d < D; ++d) {
         xf[d] = (float)tfo_decode16(fmt, x[d]);
@@ -214,6 +213,19 @@ void tfo_rmsnorm_rope_row(int fmt, int D, const uint16_t *x, const uint16_t *w,
         float prod = y[d] * (float)tfo_decode16(fmt, w[d]);
         z[d] = round16(fmt, prod);
     }
+}
+
+/*
+ * One head row at a token whose table row is cs, interleaved (pairwise) RoPE:
+ * z = rmsnorm_scale(x), then for i < D/2
+ *   o[2i]   = round16(z[2i]*cos - z[2i+1]*sin)
+ *   o[2i+1] = round16(z[2i]*sin + z[2i+1]*cos)
+ */
+void tfo_rmsnorm_rope_row(int fmt, int D, const uint16_t *x, const uint16_t *w,
+                          float eps, const float *cs, uint16_t *out)
+{
+    float z[1024];
+    rmsnorm_scale(fmt, D, x, w, eps, z);
     for (int i = 0; i < D / 2; ++i) {
         float a = z[2 * i], b = z[2 * i + 1];
         float c = cs[2 * i], s = cs[2 * i + 1];
@@ -224,14 +236,37 @@ void tfo_rmsnorm_rope_row(int fmt, int D, const uint16_t *x, const uint16_t *w,
 }
 
 /*
+ * The same row with half-split RoPE (the GPT-NeoX pairing; RoFormer's rotation
+ * of each coordinate pair by p * theta_i): element i pairs with element i + D/2
+ * and both use table entry i, for i < D/2:
+ *   o[i]       = round16(z[i]*cos_i - z[i + D/2]*sin_i)
+ *   o[i + D/2] = round16(z[i]*sin_i + z[i + D/2]*cos_i)
+ */
+void tfo_rmsnorm_rope_neox_row(int fmt, int D, const uint16_t *x, const uint16_t *w,
+                               float eps, const float *cs, uint16_t *out)
+{
+    float z[1024];
+    int half = D / 2;
+    rmsnorm_scale(fmt, D, x, w, eps, z);
+    for (int i = 0; i < half; ++i) {
+        float first = z[i], second = z[i + half];
+        float cos_i = cs[2 * i], sin_i = cs[2 * i + 1];
+        float fc = first * cos_i, ss_ = second * sin_i, fs = first * sin_i, sc = second * cos_i;
+        out[i] = tfo_encode16(fmt, (double)(fc - ss_));
+        out[i + half] = tfo_encode16(fmt, (double)(fs + sc));
+    }
+}
+
+/*
  * Scatter of one tensor (Q or K) with the fused RMSNorm + RoPE: each target row
- * T_g[b][r*Sl + t][h][:] is tfo_rmsnorm_rope_row of source row S_r[b][t][g*Hl + h][:]
- * at global position p = r*Sl + t.  table: [>= P*Sl][D/2][2] fp32.
+ * T_g[b][r*Sl + t][h][:] is tfo_rmsnorm_rope_row (neox == 0) or
+ * tfo_rmsnorm_rope_neox_row (neox != 0) of source row S_r[b][t][g*Hl + h][:] at
+ * global position p = r*Sl + t.  table: [>= P*Sl][D/2][2] fp32.
  */
 void tfo_scatter_norm_rope(int fmt, int P, int B, int Sl, int H, int D,
                            const void *const *src, int64_t sb, int64_t st, int64_t sh,
                            const uint16_t *w, float eps, const float *table,
-                           void *const *dst)
+                           void *const *dst, int neox)
 {
     int Hl = H / P;
     int64_t S = (int64_t)P * Sl;
@@ -244,6 +279,9 @@ void tfo_scatter_norm_rope(int fmt, int P, int B, int Sl, int H, int D,
                         const uint16_t *row = (const uint16_t *)src[r] +
                                               (int64_t)b * sb + (int64_t)t * st + (int64_t)(g * Hl + h) * sh;
                         uint16_t *trow = (uint16_t *)dst[g] + (((int64_t)b * S + p) * Hl + h) * D;
-                        tfo_rmsnorm_rope_row(fmt, D, row, w, eps, table + p * D, trow);
+                        if (neox)
+                            tfo_rmsnorm_rope_neox_row(fmt, D, row, w, eps, table + p * D, trow);
+                        else
+                            tfo_rmsnorm_rope_row(fmt, D, row, w, eps, table + p * D, trow);
                     }
 }

@@ -298,6 +298,108 @@ def check_fused_scatter_composition(lib):
                     assert torch.equal(row.view(torch.int16), fused[g][b, p, h].view(torch.int16)), (g, b, p, h)
 
 
+# ----------------------------------------------------------------------------
+# Half-split (NeoX) RoPE and the fused receive layout
+# ----------------------------------------------------------------------------
+
+def _neox_to_interleaved(v: torch.Tensor) -> torch.Tensor:
+    """Reorder a head row so that half-split pair (i, i + D/2) sits at (2i, 2i+1)."""
+    h = v.shape[-1] // 2
+    return torch.stack([v[..., :h], v[..., h:]], dim=-1).reshape(v.shape).contiguous()
+
+
+def _interleaved_to_neox(v: torch.Tensor) -> torch.Tensor:
+    h = v.shape[-1] // 2
+    pairs = v.reshape(*v.shape[:-1], h, 2)
+    return torch.cat([pairs[..., 0], pairs[..., 1]], dim=-1).contiguous()
+
+
+def check_neox_vs_interleaved_reordering(lib):
+    """The half-split rotation of a row equals the interleaved rotation of the row
+    reordered so pair (i, i + D/2) sits at (2i, 2i+1), reordered back: RMSNorm does
+    not depend on the order (the double sum of squares of 16-bit values is exact
+    here) and both forms rotate pair i by table entry i."""
+    eps = 1e-6
+    for dtype in (torch.bfloat16, torch.float16):
+        for D in (32, 64, 128, 256):
+            tab = oracle.rope_table(10000.0, 64, D, lib=lib)
+            w, _ = synth.norm_weights(D, dtype, seed=D + 1)
+            gen = synth.make_generator(D + 2, "cpu")
+            for p in (0, 1, 5, 63):
+                x = torch.randn((D,), generator=gen).to(dtype)
+                got = oracle.rmsnorm_rope_row(x, w, eps, tab[p], lib=lib, style="neox")
+                inter = oracle.rmsnorm_rope_row(_neox_to_interleaved(x), _neox_to_interleaved(w), eps, tab[p],
+                                                lib=lib)
+                want = _interleaved_to_neox(inter)
+                assert torch.equal(got.view(torch.int16), want.view(torch.int16)), (dtype, D, p)
+
+
+def check_neox_rotate_half_textbook(lib):
+    """Half-split RoPE in its textbook form, z * [cos, cos] + rotate_half(z) * [sin, sin]
+    with rotate_half(z) = [-z2, z1], evaluated in numpy float32 (one rounding per
+    product and per sum, as the step-by-step fp32 definition) and cast to 16 bits
+    by torch, from the oracle's own unrotated row (table row p = 0)."""
+    eps = 1e-6
+    for dtype in (torch.bfloat16, torch.float16):
+        for D in (64, 128):
+            tab = oracle.rope_table(10000.0, 40, D, lib=lib)
+            _, w = synth.norm_weights(D, dtype, seed=3 * D)
+            gen = synth.make_generator(3 * D + 1, "cpu")
+            for p in (1, 7, 39):
+                x = torch.randn((D,), generator=gen).to(dtype)
+                z = oracle.rmsnorm_rope_row(x, w, eps, tab[0], lib=lib, style="neox").float().numpy()
+                c = tab[p][:, 0].numpy().astype(np.float32)
+                s_ = tab[p][:, 1].numpy().astype(np.float32)
+                cos2 = np.concatenate([c, c])
+                sin2 = np.concatenate([s_, s_])
+                h = D // 2
+                rot = np.concatenate([-z[h:], z[:h]]).astype(np.float32)
+                want32 = (z * cos2).astype(np.float32) + (rot * sin2).astype(np.float32)
+                want = torch.from_numpy(want32.astype(np.float32)).to(dtype)
+                got = oracle.rmsnorm_rope_row(x, w, eps, tab[p], lib=lib, style="neox")
+                assert torch.equal(got.view(torch.int16), want.view(torch.int16)), (dtype, D, p)
+
+
+def check_fused_scatter_neox_composition(lib):
+    """The half-split fused scatter equals the plain scatter followed by the
+    half-split row operation at the global position."""
+    P, B, Sl, H, D = 2, 1, 4, 4, 32
+    dtype = torch.float16
+    d = synth.qkv_shards(P, B, Sl, H, D, dtype, seed=8)
+    _, wk = synth.norm_weights(D, dtype, seed=8)
+    tab = oracle.rope_table(500.0, P * Sl, D, lib=lib)
+    fused = oracle.scatter_norm_rope(d["k"], P, wk, 1e-6, tab, lib=lib, style="neox")
+    plain = oracle.scatter(d["k"], P, lib=lib)
+    for g in range(P):
+        for p in range(P * Sl):
+            for h in range(H // P):
+                row = oracle.rmsnorm_rope_row(plain[g][0, p, h], wk, 1e-6, tab[p], lib=lib, style="neox")
+                assert torch.equal(row.view(torch.int16), fused[g][0, p, h].view(torch.int16)), (g, p, h)
+
+
+def check_fused_payload_brute_force(lib):
+    """Fused receive layout by index enumeration on distinct ids:
+    payload_g[b, r*Sl + t, h, x*D + d] = S^x_r[b, t, g*Hl + h, d] for x = Q, K, V."""
+    P, B, Sl, H, D = 2, 2, 3, 4, 8
+    srcs = synth.unique_id_shards(3 * P, B, Sl, H, D)
+    q, k, v = srcs[0:P], srcs[P:2 * P], srcs[2 * P:3 * P]
+    pay = oracle.fused_payload(oracle.scatter(q, P, lib=lib), oracle.scatter(k, P, lib=lib),
+                               oracle.scatter(v, P, lib=lib))
+    Hl = H // P
+    seen = 0
+    for g in range(P):
+        assert tuple(pay[g].shape) == (B, P * Sl, Hl, 3 * D)
+        for b in range(B):
+            for r in range(P):
+                for t in range(Sl):
+                    for h in range(Hl):
+                        for x, src in enumerate((q, k, v)):
+                            for dd in range(D):
+                                assert int(pay[g][b, r * Sl + t, h, x * D + dd]) == int(src[r][b, t, g * Hl + h, dd])
+                                seen += 1
+    assert seen == 3 * P * B * Sl * H * D
+
+
 ALL_CHECKS = [
     check_codec_decode,
     check_codec_encode,
@@ -309,4 +411,8 @@ ALL_CHECKS = [
     check_rmsnorm_closed_forms,
     check_rope_vs_complex,
     check_fused_scatter_composition,
+    check_neox_vs_interleaved_reordering,
+    check_neox_rotate_half_textbook,
+    check_fused_scatter_neox_composition,
+    check_fused_payload_brute_force,
 ]

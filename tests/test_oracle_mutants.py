@@ -25,6 +25,11 @@ MUTANTS = {
     "rope_wrong_frequency": ("pow(theta, -2.0 * i / D)", "pow(theta, -1.0 * i / D)"),
     "rope_local_position": ("int64_t p = (int64_t)r * Sl + t;", "int64_t p = t;"),
     "codec_truncates": ("nearbyint(", "floor("),
+    "neox_partner_adjacent": ("float first = z[i], second = z[i + half];", "float first = z[i], second = z[i + 1];"),
+    "neox_wrong_sign": ("(double)(fc - ss_)", "(double)(fc + ss_)"),
+    "neox_table_entry_of_element": ("float cos_i = cs[2 * i], sin_i = cs[2 * i + 1];",
+                                    "float cos_i = cs[i], sin_i = cs[i + 1];"),
+    "neox_style_ignored_in_scatter": ("        if (neox)\n", "        if (0)\n"),
 }
 
 
