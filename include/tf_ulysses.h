@@ -78,10 +78,33 @@ typedef enum tf_dtype {
     TF_BYTE = 3  /* any 1-byte element, e.g. fp8 or int8 (pure relayout only) */
 } tf_dtype;
 
+/*
+ * The mode of a call: one base mode, plus for the scatter entry points any of
+ * the flags below OR-ed in (cast the result to tf_mode).  The whole value is
+ * part of the cache key.
+ *
+ * TF_MODE_FLAG_FUSED_LAYOUT -- the fused receive layout (flashinfer PR #6332
+ *   commit message, "Description", "Layouts": one [B, S_global, H_local, 3*D]
+ *   payload, in 2-D form [B*S_global, 3*H_local*D]): head group g's targets are
+ *   ONE contiguous payload [B, S, Hl, 3*D] whose head row holds the Q row, then
+ *   the K row, then the V row.  q, k and v must all be present.  Cached calls
+ *   return out->q[g] = the payload, out->k[g] = payload + D elements,
+ *   out->v[g] = payload + 2*D elements (each a [B, S, Hl, D] view with element
+ *   strides (S*Hl*3*D, Hl*3*D, 3*D, 1)); the _into/_noalloc entry points take
+ *   the P payloads in q_out and require k_out == v_out == NULL.
+ * TF_MODE_FLAG_ROPE_NEOX -- with TF_MODE_SCATTER_NORM_ROPE only: half-split RoPE
+ *   (the GPT-NeoX pairing, not on the pages, which name the interleaved form):
+ *   element i pairs with element i + D/2, both rotated by table entry i:
+ *     o[i]       = round16(z[i] * cos(p, i) - z[i + D/2] * sin(p, i))
+ *     o[i + D/2] = round16(z[i] * sin(p, i) + z[i + D/2] * cos(p, i))
+ *   The table and every other step are those of tf_norm_rope.
+ */
 typedef enum tf_mode {
-    TF_MODE_SCATTER = 0,           /* bit-exact relayout of Q, K and V */
-    TF_MODE_SCATTER_NORM_ROPE = 1, /* V relayout; Q and K RMSNorm + RoPE, then relayout */
-    TF_MODE_GATHER = 2             /* head->sequence relayout (tf_ulysses_gather_out) */
+    TF_MODE_SCATTER = 0,                 /* bit-exact relayout of Q, K and V */
+    TF_MODE_SCATTER_NORM_ROPE = 1,       /* V relayout; Q and K RMSNorm + RoPE, then relayout */
+    TF_MODE_GATHER = 2,                  /* head->sequence relayout (tf_ulysses_gather_out) */
+    TF_MODE_FLAG_FUSED_LAYOUT = 0x100,   /* scatter: one [B, S, Hl, 3*D] payload per head group */
+    TF_MODE_FLAG_ROPE_NEOX = 0x200       /* fused scatter: half-split RoPE pairs (i, i + D/2) */
 } tf_mode;
 
 /* Element strides of a [B, tokens, heads, D] view (D stride is 1). */
@@ -144,7 +167,9 @@ typedef struct tf_targets {
  *             V may be a view into a fused projection (row stride 3*H*D).
  *  P, B, S_local, H, D, dtype   as in the notation above.  H % P == 0 is required.
  *  mode       TF_MODE_SCATTER or TF_MODE_SCATTER_NORM_ROPE (then nr is required,
- *             dtype is FP16 or BF16 and D is one of 32, 64, 128, 256).
+ *             dtype is FP16 or BF16 and D is one of 32, 64, 128, 256), optionally
+ *             with TF_MODE_FLAG_FUSED_LAYOUT and (fused mode only)
+ *             TF_MODE_FLAG_ROPE_NEOX; other bits give TF_ERR_INVALID.
  *  nr         fused parameters, or NULL for TF_MODE_SCATTER.
  *  stream     cudaStream_t the launch (and any first-use allocation) is ordered on.
  *  out        receives the target pointers and the completion event.
@@ -165,7 +190,9 @@ TF_API tf_status tf_ulysses_scatter_qkv(const char *tag,
  * (flashinfer PR #6332, "Description": `out=` copies into caller-owned tensors).
  *  q_out, k_out, v_out  host arrays of P device pointers to contiguous [B, S, Hl, D]
  *             targets, one array per present source tensor (NULL where the source
- *             is NULL).  Targets must not overlap the sources.
+ *             is NULL); with TF_MODE_FLAG_FUSED_LAYOUT, q_out holds the P
+ *             contiguous [B, S, Hl, 3*D] payloads and k_out, v_out are NULL.
+ *             Targets must not overlap the sources.
  * No cache entry and no event are involved.  The library allocates nothing when
  * mode is TF_MODE_SCATTER or nr->cos_sin is non-NULL; otherwise the first call for
  * a (theta, S, D) builds the resident RoPE table.

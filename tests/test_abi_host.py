@@ -70,6 +70,12 @@ def _scatter(tf, P=2, B=1, Sl=4, H=4, D=64, dtype=1, mode=0, q=True, k=True, v=T
     (dict(mode=1, dtype=2), 4),                           # fused fp32
     (dict(mode=1, D=96), 4),                              # fused D outside {32,64,128,256}
     (dict(tag=b"x" * 64), 1),                             # tag too long
+    (dict(mode=3), 1),                                    # unknown base mode
+    (dict(mode=0x400), 1),                                # unknown flag
+    (dict(mode=0x200), 1),                                # half-split RoPE without the fused mode
+    (dict(mode=0x100, v=False), 1),                       # fused layout without v
+    (dict(mode=0x100, k=False), 1),                       # fused layout without k
+    (dict(mode=0x102), 1),                                # fused layout on the gather mode
 ])
 def test_scatter_rejects_before_any_cuda_call(tf, kw, status):
     assert _scatter(tf, **kw) == status
@@ -92,6 +98,21 @@ def test_fused_parameter_checks(tf):
     assert _scatter(tf, mode=1, nr=nr) == 1
     nr = tf.NormRope(FAKE, FAKE, 1e-6, 10000.0, FAKE + 4)  # misaligned table
     assert _scatter(tf, mode=1, nr=nr) == 3
+
+
+def test_fused_layout_targets_checked_before_any_cuda_call(tf):
+    lib = tf.lib()
+    P, B, Sl, H, D = 2, 1, 4, 4, 64
+    arr = (ctypes.c_void_p * P)(*([FAKE] * P))
+    st = (tf.Strides * 3)(*([tf.Strides(Sl * H * D, H * D, D)] * 3))
+    into = lib.tf_ulysses_scatter_qkv_into
+    # the payloads go in q_out; k_out / v_out must be NULL
+    assert into(arr, arr, arr, st, P, B, Sl, H, D, 1, 0x100, None, None, None, None, None) == 1
+    assert into(arr, arr, arr, st, P, B, Sl, H, D, 1, 0x100, None, arr, arr, None, None) == 1
+    bad = (ctypes.c_void_p * P)(FAKE, FAKE + 8)
+    assert into(arr, arr, arr, st, P, B, Sl, H, D, 1, 0x100, None, bad, None, None, None) == 3
+    assert lib.tf_ulysses_scatter_qkv_noalloc(arr, arr, arr, st, P, B, Sl, H, D, 1, 0x100, None, arr, None, arr,
+                                              None) == 1
 
 
 def test_gather_rejects_before_any_cuda_call(tf):

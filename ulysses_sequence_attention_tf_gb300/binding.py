@@ -25,6 +25,7 @@ TF_ERR_UNSUPPORTED, TF_ERR_OOM, TF_ERR_CUDA, TF_ERR_BUSY = 4, 5, 6, 7
 STATUS_NAMES = {0: "TF_OK", 1: "TF_ERR_INVALID", 2: "TF_ERR_DIVISIBILITY", 3: "TF_ERR_ALIGNMENT",
                 4: "TF_ERR_UNSUPPORTED", 5: "TF_ERR_OOM", 6: "TF_ERR_CUDA", 7: "TF_ERR_BUSY"}
 TF_MODE_SCATTER, TF_MODE_SCATTER_NORM_ROPE, TF_MODE_GATHER = 0, 1, 2
+TF_MODE_FLAG_FUSED_LAYOUT, TF_MODE_FLAG_ROPE_NEOX = 0x100, 0x200
 MAX_SHARDS = 8
 CACHE_CAPACITY = 12
 
@@ -186,9 +187,29 @@ def _scatter_args(q, k, v):
     return P, B, Sl, H, D, strides
 
 
+def _mode(norm_rope, rope, layout):
+    if rope not in ("interleaved", "neox"):
+        raise ValueError(f"rope must be 'interleaved' or 'neox', not {rope!r}")
+    if layout not in ("bshd", "fused"):
+        raise ValueError(f"layout must be 'bshd' or 'fused', not {layout!r}")
+    mode = TF_MODE_SCATTER_NORM_ROPE if norm_rope else TF_MODE_SCATTER
+    if rope == "neox":
+        mode |= TF_MODE_FLAG_ROPE_NEOX  # the library rejects it without norm_rope
+    if layout == "fused":
+        mode |= TF_MODE_FLAG_FUSED_LAYOUT
+    return mode
+
+
+def _check_targets(outs, layout):
+    for o in outs:
+        if o is not None and any(not t.is_contiguous() for t in o):
+            raise ValueError("targets must be contiguous " +
+                             ("[B, S, H/P, 3*D] payloads" if layout == "fused" else "[B, S, H/P, D]"))
+
+
 # ---------------------------------------------------------------- public API
 def scatter_qkv(tag, q, k=None, v=None, *, norm_rope=False, q_weight=None, k_weight=None, eps=1e-6,
-                theta=10000.0, cos_sin=None, stream=None):
+                theta=10000.0, cos_sin=None, rope="interleaved", layout="bshd", stream=None):
     """Sequence->head scatter of P shards ``[B, S_local, H, D]`` of Q (and K, V)
     into cached final-layout targets, in one launch.
 
@@ -196,33 +217,52 @@ def scatter_qkv(tag, q, k=None, v=None, *, norm_rope=False, q_weight=None, k_wei
     ``[B, P*S_local, H/P, D]`` tensors viewing library-owned memory (valid until the
     next call with the same key, eviction or ``cache_clear``), ``None`` for absent
     tensors.  With ``norm_rope=True``, Q and K get RMSNorm (eps, q_weight/k_weight)
-    and interleaved RoPE at global positions (theta, or an fp32 ``cos_sin`` table
-    ``[>= S, D/2, 2]``); V is copied bit for bit.
+    and RoPE at global positions (theta, or an fp32 ``cos_sin`` table
+    ``[>= S, D/2, 2]``), pairs (2i, 2i+1) for ``rope="interleaved"`` or (i, i + D/2)
+    for ``rope="neox"``; V is copied bit for bit.  ``layout="fused"`` (q, k, v
+    all required) writes one ``[B, S, H/P, 3*D]`` payload per head group and returns
+    Q, K and V as views into it (``fused_payloads`` recovers the payloads).
     """
     P, B, Sl, H, D, strides = _scatter_args(q, k, v)
-    mode = TF_MODE_SCATTER_NORM_ROPE if norm_rope else TF_MODE_SCATTER
+    mode = _mode(norm_rope, rope, layout)
     nr = _norm_rope(q_weight, k_weight, eps, theta, cos_sin) if norm_rope else None
     out = Targets()
     _check(lib().tf_ulysses_scatter_qkv(
         tag.encode() if isinstance(tag, str) else tag, _ptr_array(q), _ptr_array(k), _ptr_array(v), strides,
         P, B, Sl, H, D, _dtype_code(q[0].dtype), mode, ctypes.byref(nr) if nr is not None else None,
         _stream_handle(stream), ctypes.byref(out)))
-    shape = (B, P * Sl, H // P, D)
+    S, Hl = P * Sl, H // P
     dev = q[0].device
+    if layout == "fused":
+        pay = [_wrap(out.q[g], (B, S, Hl, 3 * D), q[0].dtype, dev) for g in range(P)]
+        return ([t[..., :D] for t in pay], [t[..., D:2 * D] for t in pay], [t[..., 2 * D:] for t in pay],
+                out.done)
     res = []
     for arr, ts in ((out.q, q), (out.k, k), (out.v, v)):
-        res.append(None if ts is None else [_wrap(arr[g], shape, q[0].dtype, dev) for g in range(P)])
+        res.append(None if ts is None else [_wrap(arr[g], (B, S, Hl, D), q[0].dtype, dev) for g in range(P)])
     return res[0], res[1], res[2], out.done
 
 
+def fused_payloads(q_targets):
+    """The ``[B, S, H/P, 3*D]`` payloads behind the Q views returned by
+    ``scatter_qkv(..., layout="fused")``."""
+    res = []
+    for t in q_targets:
+        B, S, Hl, D = t.shape
+        if t.stride() != (S * Hl * 3 * D, Hl * 3 * D, 3 * D, 1):
+            raise ValueError("not a Q view of a fused-layout payload")
+        res.append(t.as_strided((B, S, Hl, 3 * D), (S * Hl * 3 * D, Hl * 3 * D, 3 * D, 1)))
+    return res
+
+
 def scatter_qkv_into(q, k, v, q_out, k_out=None, v_out=None, *, norm_rope=False, q_weight=None, k_weight=None,
-                     eps=1e-6, theta=10000.0, cos_sin=None, stream=None):
-    """Same scatter into caller-owned contiguous targets ``[B, P*S_local, H/P, D]``."""
+                     eps=1e-6, theta=10000.0, cos_sin=None, rope="interleaved", layout="bshd", stream=None):
+    """Same scatter into caller-owned contiguous targets ``[B, P*S_local, H/P, D]``;
+    with ``layout="fused"``, ``q_out`` holds the P payloads ``[B, P*S_local, H/P, 3*D]``
+    and ``k_out``, ``v_out`` stay None."""
     P, B, Sl, H, D, strides = _scatter_args(q, k, v)
-    for outs in (q_out, k_out, v_out):
-        if outs is not None and any(not o.is_contiguous() for o in outs):
-            raise ValueError("targets must be contiguous [B, S, H/P, D]")
-    mode = TF_MODE_SCATTER_NORM_ROPE if norm_rope else TF_MODE_SCATTER
+    _check_targets((q_out, k_out, v_out), layout)
+    mode = _mode(norm_rope, rope, layout)
     nr = _norm_rope(q_weight, k_weight, eps, theta, cos_sin) if norm_rope else None
     _check(lib().tf_ulysses_scatter_qkv_into(
         _ptr_array(q), _ptr_array(k), _ptr_array(v), strides, P, B, Sl, H, D, _dtype_code(q[0].dtype), mode,
@@ -232,16 +272,14 @@ def scatter_qkv_into(q, k, v, q_out, k_out=None, v_out=None, *, norm_rope=False,
 
 
 def scatter_qkv_noalloc(q, k, v, q_out, k_out=None, v_out=None, *, norm_rope=False, q_weight=None, k_weight=None,
-                        eps=1e-6, theta=10000.0, cos_sin=None, stream=None):
+                        eps=1e-6, theta=10000.0, cos_sin=None, rope="interleaved", layout="bshd", stream=None):
     """``scatter_qkv_into`` for callers that cannot allocate device memory: the
     library allocates nothing; a needed cos/sin table is rebuilt on every call
     in the library's fixed 16 MiB device scratch (P*S_local*D <= 4 Mi floats).
     Calls that overlap on the GPU race on that scratch."""
     P, B, Sl, H, D, strides = _scatter_args(q, k, v)
-    for outs in (q_out, k_out, v_out):
-        if outs is not None and any(not o.is_contiguous() for o in outs):
-            raise ValueError("targets must be contiguous [B, S, H/P, D]")
-    mode = TF_MODE_SCATTER_NORM_ROPE if norm_rope else TF_MODE_SCATTER
+    _check_targets((q_out, k_out, v_out), layout)
+    mode = _mode(norm_rope, rope, layout)
     nr = _norm_rope(q_weight, k_weight, eps, theta, cos_sin) if norm_rope else None
     _check(lib().tf_ulysses_scatter_qkv_noalloc(
         _ptr_array(q), _ptr_array(k), _ptr_array(v), strides, P, B, Sl, H, D, _dtype_code(q[0].dtype), mode,

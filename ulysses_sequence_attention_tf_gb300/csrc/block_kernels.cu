@@ -1,0 +1,204 @@
+// block_kernels.cu -- the scatter over token blocks of all tensors together
+// (sm_103a), used for every fused scatter with 32-byte vectors.
+//
+// What is computed (TeleFuser docs, "Communication Architecture", section
+// "Sequence Parallel Communication / Ulysses"; head bands and rank order as in
+// flashinfer PR #6332 commit message, "Assumptions / Exchange algorithm"):
+//   T^x_g[b, r*Sl + t, h, :] = f_x(S^x_r[b, t, g*Hl + h, :], p = r*Sl + t)
+// with f_x the bit copy for V (and every tensor of a plain scatter) and, for Q/K
+// of a fused scatter, RMSNorm + weight + RoPE (flashinfer PR #6332,
+// "Assumptions / Operator math"; interleaved pairs, or half-split pairs).
+// TeleFuser PR #27 overlaps V's transfer with the Q/K norm/RoPE ("Changes
+// Made"); on one GPU both are SM work, so here they share every warp: a unit
+// carries V's rows and Q/K's rows of the same token block.
+//
+// Design:
+//  * A unit is the row range [c*rpu, (c+1)*rpu) of one (batch b, shard r, head
+//    group g) block, for every slot: kCopy copied slots (V first) and kNF fused
+//    ones (Q, then K).  A persistent grid walks the units, chunk-major with g
+//    innermost, so CTAs running together read whole source token rows and
+//    write all P head groups of a token block.
+//  * Each lane group of kLanes = D*2/32 lanes takes a contiguous run of the
+//    unit's rows and keeps kDepth rows (of every slot) loaded ahead of the one it
+//    computes.  One 32-byte vector per lane per row and slot; loads bypass L1,
+//    stores are evict-first.
+//  * The (cos, sin) entries are loaded once per token and reused across its
+//    heads and by Q and K.  Destination rows are d_h bytes apart, so the same
+//    code writes the separate [B, S, Hl, D] targets (d_h = D*esize) and the
+//    fused receive layout [B, S, Hl, 3*D] (d_h = 3*D*esize, slot offsets 0, D, 2D).
+#include "device_common.cuh"
+#include "relayout.h"
+
+#ifndef TFU_FUSED_MIN_BLOCKS
+#define TFU_FUSED_MIN_BLOCKS 2  // resident 256-thread CTAs per SM the fused register budget is sized for
+#endif
+#ifndef TFU_COPY_BLOCK_MIN_BLOCKS
+#define TFU_COPY_BLOCK_MIN_BLOCKS 2  // resident CTAs per SM the copy block kernel's registers allow
+#endif
+
+namespace tfu {
+namespace {
+
+using namespace dev;
+
+int block_device_sms() {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms > 0 ? sms : 1;
+}
+
+template <Fused kF, int kLanes, int kCopy, int kNF, bool kNeox>
+__global__ void __launch_bounds__(kThreads, kNF > 0 ? TFU_FUSED_MIN_BLOCKS : TFU_COPY_BLOCK_MIN_BLOCKS)
+    block_kernel(const __grid_constant__ RelayoutParams p) {
+    constexpr int VW = 32, NP = 8;                // 32 bytes = 8 element pairs per lane
+    constexpr int kSlots = kCopy + kNF;
+    constexpr int kDepth = kNF > 0 ? kBlockDepth : kCopyBlockDepth;
+    constexpr int kRowFloats = kLanes * NP * 2;  // D floats per table row
+    constexpr int kCs = cs_vecs<kNeox, NP>();
+    constexpr uint32_t kGroups = kThreads / kLanes;
+    static_assert(kSlots >= 1 && kSlots <= kMaxSlots && (kNF == 0) == (kF == Fused::kNone), "slot pattern");
+    const uint32_t g_row = threadIdx.x / kLanes, dv = threadIdx.x % kLanes;
+    uint32_t w[kNF > 0 ? kNF : 1][NP];  // this lane's weight pairs of each fused slot
+#pragma unroll
+    for (int f = 0; f < kNF; ++f) {
+        const Vec<VW> wv =
+            *reinterpret_cast<const Vec<VW>*>(static_cast<const uint8_t*>(p.weight[kCopy + f]) + dv * VW);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) w[f][j] = wv.w[j];
+    }
+#pragma unroll 1
+    for (uint32_t u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+        const uint32_t c = fastdiv(u, p.div_planes);
+        const uint32_t q = u - c * p.n_planes;  // q = (b * P + r) * P + g
+        const uint32_t g = q % p.P;
+        const uint32_t r = (q / p.P) % p.P;
+        const uint32_t b = q / (p.P * p.P);
+        const uint8_t* src[kSlots];
+        uint8_t* dst[kSlots];
+#pragma unroll
+        for (int x = 0; x < kSlots; ++x) {
+            src[x] = p.src[x][r] + int64_t(b) * p.s_b[x] + int64_t(g) * p.Hl * p.s_h[x] + int64_t(dv) * VW;
+            dst[x] = p.dst[x][g] + int64_t(b) * p.d_b[x] + int64_t(r) * p.Sl * p.d_t[x] + int64_t(dv) * VW;
+        }
+        const uint32_t R0 = c * p.rpu;
+        const uint32_t n_rows = min(R0 + p.rpu, p.plane_rows) - R0;
+        const uint32_t per = (n_rows + kGroups - 1) / kGroups;  // rows per group, the same for every lane
+        const uint32_t r_beg = R0 + g_row * per;                 // first plane row of this group
+        const uint32_t r_end = min(r_beg + per, R0 + n_rows);    // may be <= r_beg for trailing groups
+        const float* tab_lane =
+            kNF > 0 ? p.table + size_t(r) * p.Sl * kRowFloats + cs_lane_offset<kNeox, kLanes, NP>(dv) : nullptr;
+        float4 cs[kCs];
+#pragma unroll
+        for (int k = 0; k < kCs; ++k) cs[k] = make_float4(1.f, 0.f, 1.f, 0.f);
+        uint32_t t_cached = 0xffffffffu;
+        auto load = [&](Vec<VW>(&buf)[kSlots], uint32_t R) {
+            const uint32_t t = fastdiv(R, p.div_hl);
+            const uint32_t h = R - t * p.Hl;
+#pragma unroll
+            for (int x = 0; x < kSlots; ++x) {
+                if constexpr (kNF > 0) {  // masked rows still go through the row reduction
+#pragma unroll
+                    for (int k = 0; k < NP; ++k) buf[x].w[k] = 0u;
+                }
+                if (R < r_end) buf[x] = ld_stream<VW>(src[x] + int64_t(t) * p.s_t[x] + int64_t(h) * p.s_h[x]);
+            }
+        };
+        auto compute_store = [&](Vec<VW>(&buf)[kSlots], uint32_t R) {
+            const bool valid = R < r_end;
+            if constexpr (kNF > 0) {
+                const uint32_t t = fastdiv(R, p.div_hl);
+                if (valid && t != t_cached) {
+                    const float* tab = tab_lane + size_t(t) * kRowFloats;
+#pragma unroll
+                    for (int k = 0; k < kCs; ++k) cs[k] = ld_table(tab + 4 * k);
+                    t_cached = t;
+                }
+                // every lane runs the row reductions (they shuffle); only valid rows are written
+#pragma unroll
+                for (int f = 0; f < kNF; ++f)
+                    norm_rope_core<kF, kLanes, NP, kNeox>(buf[kCopy + f].w, w[f], cs, p.eps);
+            }
+            if (valid) {
+#pragma unroll
+                for (int x = 0; x < kSlots; ++x) st_stream<VW>(dst[x] + int64_t(R) * p.d_h[x], buf[x]);
+            }
+        };
+        Vec<VW> bufs[kDepth][kSlots];
+#pragma unroll
+        for (int d = 0; d < kDepth; ++d) load(bufs[d], r_beg + d);
+#pragma unroll 1
+        for (uint32_t R = r_beg; R < r_beg + per; R += kDepth) {
+#pragma unroll
+            for (int d = 0; d < kDepth; ++d) {
+                compute_store(bufs[d], R + d);
+                load(bufs[d], R + d + kDepth);
+            }
+        }
+    }
+}
+
+template <Fused kF, int kLanes, int kCopy, int kNF, bool kNeox>
+cudaError_t launch_block(const RelayoutParams& p, cudaStream_t stream) {
+    static int blocks_per_sm = 0;  // same for every device of one architecture
+    if (blocks_per_sm == 0) {
+        int bps = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &bps, block_kernel<kF, kLanes, kCopy, kNF, kNeox>, kThreads, 0);
+        if (e != cudaSuccess) return e;
+        blocks_per_sm = bps > 0 ? bps : 1;
+    }
+    const int64_t want = int64_t(block_device_sms()) * blocks_per_sm;
+    const unsigned grid = unsigned(want < int64_t(p.n_units) ? want : int64_t(p.n_units));
+    block_kernel<kF, kLanes, kCopy, kNF, kNeox><<<grid, kThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <Fused kF, int kCopy, int kNF, bool kNeox>
+cudaError_t launch_block_lanes(const RelayoutParams& p, cudaStream_t stream) {
+    switch (p.vpr) {  // lanes per head row = D * esize / 32
+        case 2: return launch_block<kF, 2, kCopy, kNF, kNeox>(p, stream);
+        case 4: return launch_block<kF, 4, kCopy, kNF, kNeox>(p, stream);
+        case 8: return launch_block<kF, 8, kCopy, kNF, kNeox>(p, stream);
+        case 16: return launch_block<kF, 16, kCopy, kNF, kNeox>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <Fused kF, bool kNeox>
+cudaError_t launch_block_fused(const RelayoutParams& p, cudaStream_t stream) {
+    const uint32_t n_copy = (p.fused_mask & 1u) ? 0u : 1u;  // V (unfused) can only be slot 0
+    const uint32_t nf = p.nx - n_copy;
+    if (nf < 1 || nf > 2 || p.fused_mask != ((1u << nf) - 1u) << n_copy) return cudaErrorInvalidValue;
+    if (n_copy)
+        return nf == 2 ? launch_block_lanes<kF, 1, 2, kNeox>(p, stream) : launch_block_lanes<kF, 1, 1, kNeox>(p, stream);
+    return nf == 2 ? launch_block_lanes<kF, 0, 2, kNeox>(p, stream) : launch_block_lanes<kF, 0, 1, kNeox>(p, stream);
+}
+
+template <Fused kF>
+cudaError_t launch_block_style(const RelayoutParams& p, cudaStream_t stream) {
+    if (!p.table) return cudaErrorInvalidValue;
+    return p.rope_neox ? launch_block_fused<kF, true>(p, stream) : launch_block_fused<kF, false>(p, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_blocks(const RelayoutParams& p, Fused fused, cudaStream_t stream) {
+    if (p.n_units == 0) return cudaSuccess;
+    if (p.vec_bytes != 32 || p.rpu == 0) return cudaErrorInvalidValue;
+    switch (fused) {
+        case Fused::kNone:
+            if (p.fused_mask != 0) return cudaErrorInvalidValue;
+            switch (p.nx) {
+                case 1: return launch_block_lanes<Fused::kNone, 1, 0, false>(p, stream);
+                case 2: return launch_block_lanes<Fused::kNone, 2, 0, false>(p, stream);
+                case 3: return launch_block_lanes<Fused::kNone, 3, 0, false>(p, stream);
+                default: return cudaErrorInvalidValue;
+            }
+        case Fused::kBF16: return launch_block_style<Fused::kBF16>(p, stream);
+        case Fused::kFP16: return launch_block_style<Fused::kFP16>(p, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace tfu

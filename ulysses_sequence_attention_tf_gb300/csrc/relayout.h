@@ -2,6 +2,7 @@
 // Not part of the public ABI (that is include/tf_ulysses.h).
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -16,6 +17,17 @@ constexpr int kThreads = 256;          // threads per CTA
 #endif
 constexpr int kChunkBytes = TFU_CHUNK_BYTES;  // payload bytes per work unit of the register kernel
 __host__ __device__ constexpr int chunk_vecs(int vec_bytes) { return kChunkBytes / vec_bytes; }
+
+// Block kernel pipeline: rows (of every slot) each lane keeps loaded ahead of the
+// one it computes, with and without fused slots.
+#ifndef TFU_BLOCK_DEPTH
+#define TFU_BLOCK_DEPTH 2
+#endif
+#ifndef TFU_COPY_BLOCK_DEPTH
+#define TFU_COPY_BLOCK_DEPTH 4
+#endif
+constexpr int kBlockDepth = TFU_BLOCK_DEPTH;
+constexpr int kCopyBlockDepth = TFU_COPY_BLOCK_DEPTH;
 
 // Unsigned 32-bit division by an invariant divisor as multiply-high, add and
 // shift (Granlund & Montgomery, "Division by invariant integers using
@@ -75,10 +87,16 @@ struct RelayoutParams {
     uint32_t row_bytes;   // D * esize
     uint32_t rpu;         // rows per unit (tma_rows_per_unit)
     uint32_t plane_rows;  // Sl * Hl
+    uint32_t rope_neox;   // fused slots: 0 interleaved pairs (2i, 2i+1), 1 half-split pairs (i, i + D/2)
 };
+// Field order is part of the staged kernel's speed: inserting one 4-byte field
+// before `nx` (shifting every later field by 4 bytes) measured ~1.3 % slower
+// bulk copies on the video-DiT shape.  New fields go at the end.
 
-// Launch the relayout of every plane in `p` (vector width p.vec_bytes; for the
-// fused kernels the head row holds p.vpr vectors, D in {32, 64, 128, 256}).
+// Launch the relayout of every plane in `p` with the register kernel (vector
+// width p.vec_bytes).  Fused scatters need vec_bytes == 16 (p.vpr = D / 8 lanes
+// per head row, D in {32, 64, 128, 256}).  Scatter destination rows of a plane
+// are d_h bytes apart.
 cudaError_t launch_relayout(const RelayoutParams& p, Dir dir, Fused fused, cudaStream_t stream);
 
 // Launch the shared-memory-staged (bulk-copy) relayout of a pure relayout

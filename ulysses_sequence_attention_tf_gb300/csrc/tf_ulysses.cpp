@@ -189,14 +189,14 @@ tf_status plan_units(RelayoutParams& p, const Shape& sh) {
 #ifndef TFU_COPY_BLOCKS
 #define TFU_COPY_BLOCKS 0  // the same single pass for copy scatters (else the staged kernel)
 #endif
-#ifndef TFU_BLOCK_ROWS
-#define TFU_BLOCK_ROWS 128  // rows of one (b, r, g) block per unit of the block kernel
+#ifndef TFU_BLOCK_PASSES
+#define TFU_BLOCK_PASSES 0  // pipeline passes per row group and unit of the block kernel; 0: by slot count
 #endif
 
 // Plan and launch one relayout:
 //  * scatters with 32-byte vectors and D * esize in {64, 128, 256, 512} bytes
-//    (fused always, copies when TFU_COPY_BLOCKS): the block kernel, all slots
-//    of a token block in one pass;
+//    (fused always; copies into the fused receive layout, or all copies when
+//    TFU_COPY_BLOCKS): the block kernel, all slots of a token block in one pass;
 //  * other pure relayouts whose head row fits a stage: the shared-memory-staged
 //    (bulk-copy) kernel;
 //  * the rest: the register kernel with 32- or 16-byte vectors.
@@ -225,20 +225,27 @@ tf_status launch_planned(RelayoutParams& p, const Shape& sh, tfu::Dir dir, tfu::
     };
     tf_status s;
     cudaError_t e;
+    bool dst_rows_packed = true;  // scatter target rows adjacent (else the fused receive layout)
+    for (uint32_t x = 0; x < p.nx; ++x) dst_rows_packed = dst_rows_packed && p.d_h[x] == int64_t(rb);
     const bool block_ok = dir == tfu::Dir::kScatter && (rb == 64 || rb == 128 || rb == 256 || rb == 512) &&
-                          (fused != tfu::Fused::kNone ? TFU_FUSED_BLOCKS : TFU_COPY_BLOCKS);
+                          (fused != tfu::Fused::kNone ? TFU_FUSED_BLOCKS : (TFU_COPY_BLOCKS || !dst_rows_packed));
     const uint32_t vec = pick_vec_bytes(p, sh, src_tokens, dst_tokens);
     const uint32_t rpu = tfu::tma_rows_per_unit(uint32_t(sh.Hl), rb);
     if (block_ok && vec == 32) {
         p.vec_bytes = 32;
         p.vpr = rb / 32;
-        if ((s = plan_rows(uint64_t(sh.B) * sh.P * sh.P, TFU_BLOCK_ROWS)) != TF_OK) return s;
+        // a unit gives every row group of the CTA whole pipeline passes (kThreads / vpr
+        // groups, depth rows each): one pass when three slots share the rows, else two
+        const uint32_t depth = fused != tfu::Fused::kNone ? tfu::kBlockDepth : tfu::kCopyBlockDepth;
+        const uint32_t passes = TFU_BLOCK_PASSES > 0 ? TFU_BLOCK_PASSES : (p.nx >= 3 ? 1u : 2u);
+        const uint32_t unit_rows = uint32_t(tfu::kThreads) / p.vpr * depth * passes;
+        if ((s = plan_rows(uint64_t(sh.B) * sh.P * sh.P, unit_rows)) != TF_OK) return s;
         e = tfu::launch_blocks(p, fused, stream);
     } else if (TFU_USE_STAGED && rpu > 0 && fused == tfu::Fused::kNone) {
         if ((s = plan_rows(uint64_t(sh.B) * sh.P * p.nx * sh.P, rpu)) != TF_OK) return s;
         e = tfu::launch_relayout_staged(p, dir, fused, stream);
     } else {
-        p.vec_bytes = vec;
+        p.vec_bytes = fused != tfu::Fused::kNone ? 16 : vec;  // the register kernel's fused rows use 16 bytes
         if ((s = plan_units(p, sh)) != TF_OK) return s;
         e = tfu::launch_relayout(p, dir, fused, stream);
     }
@@ -398,7 +405,12 @@ struct ScatterPlan {
     int slot_of[3] = {-1, -1, -1};  // tensor (q=0, k=1, v=2) -> slot
     int present = 0;                // bit per tensor
     bool empty = false;
+    bool fused_layout = false;       // one [B, S, Hl, 3*D] payload per head group
+    int64_t row_off[3] = {0, 0, 0};  // byte offset of tensor x's row inside a payload row
 };
+
+constexpr int kModeBase = 0xff;
+constexpr int kModeFlags = TF_MODE_FLAG_FUSED_LAYOUT | TF_MODE_FLAG_ROPE_NEOX;
 
 tf_status plan_scatter(const void* const* q, const void* const* k, const void* const* v, const tf_strides* strides,
                        int P, int B, int Sl, int H, int D, tf_dtype dtype, tf_mode mode, const tf_norm_rope* nr,
@@ -406,8 +418,15 @@ tf_status plan_scatter(const void* const* q, const void* const* k, const void* c
     ScatterPlan& pl = *plan;
     tf_status s = check_shape(P, B, Sl, H, D, dtype, &pl.sh);
     if (s != TF_OK) return s;
-    if (mode != TF_MODE_SCATTER && mode != TF_MODE_SCATTER_NORM_ROPE)
+    const int base = int(mode) & kModeBase, flags = int(mode) & ~kModeBase;
+    if (base != TF_MODE_SCATTER && base != TF_MODE_SCATTER_NORM_ROPE)
         return fail(TF_ERR_INVALID, "mode %d is not a scatter mode", int(mode));
+    if (flags & ~kModeFlags) return fail(TF_ERR_INVALID, "unknown mode flags 0x%x", unsigned(flags & ~kModeFlags));
+    const bool neox = (flags & TF_MODE_FLAG_ROPE_NEOX) != 0;
+    if (neox && base != TF_MODE_SCATTER_NORM_ROPE)
+        return fail(TF_ERR_INVALID, "TF_MODE_FLAG_ROPE_NEOX needs TF_MODE_SCATTER_NORM_ROPE");
+    pl.fused_layout = (flags & TF_MODE_FLAG_FUSED_LAYOUT) != 0;
+    if (pl.fused_layout && (!k || !v)) return fail(TF_ERR_INVALID, "the fused layout needs q, k and v");
     if (!q) return fail(TF_ERR_INVALID, "q is NULL");
     if (!strides) return fail(TF_ERR_INVALID, "strides is NULL");
     const void* const* src[3] = {q, k, v};
@@ -418,7 +437,7 @@ tf_status plan_scatter(const void* const* q, const void* const* k, const void* c
         if (B > 0 && Sl > 0 && (s = check_ptrs(names[x], src[x], P)) != TF_OK) return s;
         if ((s = check_strides(names[x], strides[x], pl.sh.esize, B, Sl, H)) != TF_OK) return s;
     }
-    if (mode == TF_MODE_SCATTER_NORM_ROPE) {
+    if (base == TF_MODE_SCATTER_NORM_ROPE) {
         if (dtype != TF_FP16 && dtype != TF_BF16)
             return fail(TF_ERR_UNSUPPORTED, "the fused mode needs fp16 or bf16 (dtype %d)", int(dtype));
         if (D != 32 && D != 64 && D != 128 && D != 256)
@@ -448,21 +467,50 @@ tf_status plan_scatter(const void* const* q, const void* const* k, const void* c
         p.s_b[slot] = strides[x].b * pl.sh.esize;
         p.s_t[slot] = strides[x].t * pl.sh.esize;
         p.s_h[slot] = strides[x].h * pl.sh.esize;
-        const int64_t rowb = int64_t(D) * pl.sh.esize;  // targets: contiguous [B, S, Hl, D]
-        p.d_h[slot] = rowb;
-        p.d_t[slot] = rowb * pl.sh.Hl;
-        p.d_b[slot] = rowb * pl.sh.Hl * int64_t(P) * Sl;
-        if (mode == TF_MODE_SCATTER_NORM_ROPE && x != 2) {
+        // targets: contiguous [B, S, Hl, D], or [B, S, Hl, 3*D] payloads holding Q, K, V rows
+        const int64_t rowb = int64_t(D) * pl.sh.esize;
+        const int64_t pitch = pl.fused_layout ? 3 * rowb : rowb;
+        pl.row_off[x] = pl.fused_layout ? int64_t(x) * rowb : 0;
+        p.d_h[slot] = pitch;
+        p.d_t[slot] = pitch * pl.sh.Hl;
+        p.d_b[slot] = pitch * pl.sh.Hl * int64_t(P) * Sl;
+        if (base == TF_MODE_SCATTER_NORM_ROPE && x != 2) {
             p.fused_mask |= 1u << slot;
             p.weight[slot] = x == 0 ? nr->q_weight : nr->k_weight;
         }
     }
     p.nx = nx;
+    p.rope_neox = neox ? 1u : 0u;
     p.eps = nr ? nr->eps : 0.f;
     p.table = nr ? nr->cos_sin : nullptr;
     p.vec_bytes = 16;  // size limits checked for the larger vector count; re-planned at launch
     if ((s = plan_units(p, pl.sh)) != TF_OK) return s;
     pl.empty = B == 0 || Sl == 0;
+    return TF_OK;
+}
+
+// Destinations of the _into / _noalloc entry points: one array per present
+// tensor, or with the fused layout the P payloads in q_out (k_out, v_out NULL).
+tf_status set_caller_targets(ScatterPlan& pl, void* const* q_out, void* const* k_out, void* const* v_out) {
+    const int P = pl.sh.P;
+    tf_status s;
+    if (pl.fused_layout) {
+        if (!q_out) return fail(TF_ERR_INVALID, "q_out (the payloads) is NULL");
+        if (k_out || v_out) return fail(TF_ERR_INVALID, "the fused layout takes its payloads in q_out only");
+        if (!pl.empty && (s = check_ptrs("q_out", q_out, P)) != TF_OK) return s;
+        for (int x = 0; x < 3; ++x)
+            for (int g = 0; g < P; ++g)
+                pl.p.dst[pl.slot_of[x]][g] = static_cast<uint8_t*>(q_out[g]) + (q_out[g] ? pl.row_off[x] : 0);
+        return TF_OK;
+    }
+    void* const* dsts[3] = {q_out, k_out, v_out};
+    const char* names[3] = {"q_out", "k_out", "v_out"};
+    for (int x = 0; x < 3; ++x) {
+        if (!(pl.present & (1 << x))) continue;
+        if (!dsts[x]) return fail(TF_ERR_INVALID, "%s is NULL for a present source", names[x]);
+        if (!pl.empty && (s = check_ptrs(names[x], dsts[x], P)) != TF_OK) return s;
+        for (int g = 0; g < P; ++g) pl.p.dst[pl.slot_of[x]][g] = static_cast<uint8_t*>(dsts[x][g]);
+    }
     return TF_OK;
 }
 
@@ -517,16 +565,26 @@ TF_API tf_status tf_ulysses_scatter_qkv(const char* tag, const void* const* q, c
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     std::lock_guard<std::mutex> lock(g_mu);
-    const size_t target_bytes = size_t(B) * size_t(P) * size_t(S_local) * size_t(pl.sh.Hl) * size_t(D) * pl.sh.esize;
+    size_t target_bytes = size_t(B) * size_t(P) * size_t(S_local) * size_t(pl.sh.Hl) * size_t(D) * pl.sh.esize;
     int counts[3] = {0, 0, 0};
     for (int x = 0; x < 3; ++x)
         if (pl.present & (1 << x)) counts[x] = P;
+    if (pl.fused_layout) {  // P payloads holding all three tensors
+        target_bytes *= 3;
+        counts[1] = counts[2] = 0;
+    }
     Entry* e = nullptr;
     if ((s = get_entry(key, int(mode), pl.present, pl.sh, device, target_bytes, counts, st, &e)) != TF_OK) return s;
+    void* bufs[3][TF_ULYSSES_MAX_SHARDS] = {};
+    for (int x = 0; x < 3; ++x)
+        for (int g = 0; g < P; ++g) {
+            uint8_t* base = static_cast<uint8_t*>(e->buf[pl.fused_layout ? 0 : x][g]);
+            bufs[x][g] = base ? base + pl.row_off[x] : nullptr;
+        }
     for (int x = 0; x < 3; ++x) {
         const int slot = pl.slot_of[x];
         if (slot < 0) continue;
-        for (int g = 0; g < P; ++g) pl.p.dst[slot][g] = static_cast<uint8_t*>(e->buf[x][g]);
+        for (int g = 0; g < P; ++g) pl.p.dst[slot][g] = static_cast<uint8_t*>(bufs[x][g]);
     }
     Table* used = nullptr;
     if ((s = launch_scatter(pl, nr, device, st, &used)) != TF_OK) return s;
@@ -535,9 +593,9 @@ TF_API tf_status tf_ulysses_scatter_qkv(const char* tag, const void* const* q, c
     e->last_stream = st;
     std::memset(out, 0, sizeof *out);
     for (int g = 0; g < P; ++g) {
-        out->q[g] = e->buf[0][g];
-        out->k[g] = e->buf[1][g];
-        out->v[g] = e->buf[2][g];
+        out->q[g] = bufs[0][g];
+        out->k[g] = bufs[1][g];
+        out->v[g] = bufs[2][g];
     }
     out->done = e->done;
     return TF_OK;
@@ -551,14 +609,7 @@ TF_API tf_status tf_ulysses_scatter_qkv_into(const void* const* q, const void* c
     ScatterPlan pl;
     tf_status s = plan_scatter(q, k, v, strides, P, B, S_local, H, D, dtype, mode, nr, &pl);
     if (s != TF_OK) return s;
-    void* const* dsts[3] = {q_out, k_out, v_out};
-    const char* names[3] = {"q_out", "k_out", "v_out"};
-    for (int x = 0; x < 3; ++x) {
-        if (!(pl.present & (1 << x))) continue;
-        if (!dsts[x]) return fail(TF_ERR_INVALID, "%s is NULL for a present source", names[x]);
-        if (!pl.empty && (s = check_ptrs(names[x], dsts[x], P)) != TF_OK) return s;
-        for (int g = 0; g < P; ++g) pl.p.dst[pl.slot_of[x]][g] = static_cast<uint8_t*>(dsts[x][g]);
-    }
+    if ((s = set_caller_targets(pl, q_out, k_out, v_out)) != TF_OK) return s;
     int device = 0;
     if ((s = current_device(&device)) != TF_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -580,14 +631,7 @@ TF_API tf_status tf_ulysses_scatter_qkv_noalloc(const void* const* q, const void
     ScatterPlan pl;
     tf_status s = plan_scatter(q, k, v, strides, P, B, S_local, H, D, dtype, mode, nr, &pl);
     if (s != TF_OK) return s;
-    void* const* dsts[3] = {q_out, k_out, v_out};
-    const char* names[3] = {"q_out", "k_out", "v_out"};
-    for (int x = 0; x < 3; ++x) {
-        if (!(pl.present & (1 << x))) continue;
-        if (!dsts[x]) return fail(TF_ERR_INVALID, "%s is NULL for a present source", names[x]);
-        if (!pl.empty && (s = check_ptrs(names[x], dsts[x], P)) != TF_OK) return s;
-        for (int g = 0; g < P; ++g) pl.p.dst[pl.slot_of[x]][g] = static_cast<uint8_t*>(dsts[x][g]);
-    }
+    if ((s = set_caller_targets(pl, q_out, k_out, v_out)) != TF_OK) return s;
     const bool own_table = pl.fused != tfu::Fused::kNone && !nr->cos_sin;
     const uint64_t table_floats = uint64_t(P) * uint64_t(S_local) * uint64_t(D);
     if (own_table && table_floats > tfu::kNoAllocTableFloats)
