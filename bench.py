@@ -56,7 +56,7 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=12)
     ap.add_argument("--sets", type=int, default=2, help="rotating input sets (each ~2 GB)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-tokens", type=int, default=1024, help="tokens per shard in the CPU-baseline sample")
+    ap.add_argument("--cpu-tokens", type=int, default=4096, help="tokens per shard in the CPU-baseline sample")
     return ap.parse_args()
 
 
@@ -97,9 +97,9 @@ def profiled_traffic():
                 if ":" in line:
                     k, v = line.split(":", 1)
                     fields[k.strip()] = v.strip()
-        if fields.get("kernel_source_sha256_16") != kernel_source_hash():
+        if fields.get("kernel_source_sha256_16", "").split()[:1] != [kernel_source_hash()]:
             return None
-        return int(float(fields["dram_bytes_per_full_launch"]))
+        return int(float(fields["dram_bytes_per_full_launch"].split()[0]))
     except (OSError, KeyError, ValueError):
         return None
 
