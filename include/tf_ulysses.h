@@ -234,6 +234,42 @@ TF_API tf_status tf_ulysses_scatter_qkv_noalloc(const void *const *q, const void
                                                 void *stream);
 
 /*
+ * tf_ulysses_scatter_qkv_heads_into -- the scatter of tf_ulysses_scatter_qkv_into
+ * restricted to a head chunk: heads [h0, h1) of every head band, written to the
+ * same heads of the caller's final-layout targets; every other target element
+ * is left as it was.  Chunks of a partition of [0, Hl), issued one after
+ * another (or on several streams), produce the whole scatter, so attention on
+ * the first chunk can start while later chunks still move (flashinfer PR #6332
+ * commit message, "Speedup": baselines B2/B3 exchange Q/K/V per head chunk with
+ * `scatter_qkv_head_chunk`).
+ *  h0, h1     0 <= h0 < h1 <= Hl = H / P; otherwise TF_ERR_INVALID.
+ * Every other argument, layout flag and error is that of _into; targets keep
+ * their full shape ([B, S, Hl, D], or [B, S, Hl, 3*D] payloads).
+ */
+TF_API tf_status tf_ulysses_scatter_qkv_heads_into(const void *const *q, const void *const *k, const void *const *v,
+                                                   const tf_strides *strides,
+                                                   int P, int B, int S_local, int H, int D,
+                                                   tf_dtype dtype, tf_mode mode, const tf_norm_rope *nr,
+                                                   int h0, int h1,
+                                                   void *const *q_out, void *const *k_out, void *const *v_out,
+                                                   void *stream);
+
+/*
+ * tf_ulysses_exchange_chunks -- the all-to-all over destination-major payloads
+ * (flashinfer UlyssesCommunicator PCIe PR description, "Transforms":
+ * `exchange_chunks` takes [1, 1, world_size, chunk] to the same shape, over a
+ * payload a preceding pack already laid out destination-major, and interleaves
+ * nothing): for P logical ranks,
+ *     dst[g][r*chunk_bytes + i] = src[r][g*chunk_bytes + i]
+ *  src, dst      host arrays of P device pointers, each to P*chunk_bytes bytes,
+ *                16-byte aligned; dst must not overlap src.
+ *  chunk_bytes   a multiple of 16 (otherwise TF_ERR_ALIGNMENT); 0 = nothing to do.
+ * Bit copy of any element type, one launch on `stream`, no allocation.
+ */
+TF_API tf_status tf_ulysses_exchange_chunks(const void *const *src, void *const *dst, int P, size_t chunk_bytes,
+                                            void *stream);
+
+/*
  * tf_ulysses_gather_out -- head->sequence gather of the attention output (the
  * inverse all-to-all of the Ulysses section; TeleFuser PR #27 keeps it for the
  * output path).

@@ -167,6 +167,30 @@ def fused_payload(tq, tk, tv):
     return [torch.cat([q, k, v], dim=-1) for q, k, v in zip(tq, tk, tv)]
 
 
+def exchange_chunks(srcs, P: int):
+    """All-to-all over destination-major payloads (flashinfer UlyssesCommunicator
+    PCIe PR description, "Transforms", ``exchange_chunks``: each rank's payload
+    already holds one chunk per destination, in destination order, and the
+    exchange interleaves nothing): out_g = concat over r of chunk g of src_r.
+    srcs: P byte tensors [P, chunk]; returns P new [P, chunk] tensors."""
+    _check_cpu(srcs)
+    out = []
+    for g in range(P):
+        out.append(torch.stack([srcs[r][g].clone() for r in range(P)]))
+    return out
+
+
+def scatter_heads_chunk(srcs, P: int, h0: int, h1: int, full_targets):
+    """Head-chunk scatter: the targets ``full_targets`` (P tensors [B, P*Sl, Hl, D],
+    copied) with heads [h0, h1) of every head group replaced by the plain
+    scatter's values there; every other element keeps its previous value."""
+    full = scatter(srcs, P)
+    out = [t.clone() for t in full_targets]
+    for g in range(P):
+        out[g][:, :, h0:h1] = full[g][:, :, h0:h1]
+    return out
+
+
 def decode16(dtype, bits: int) -> float:
     return load().tfo_decode16(FMT[dtype], bits & 0xFFFF)
 

@@ -51,6 +51,13 @@ def run(rank, world, port, shapes, result_dir):
                 # oracle gather of the oracle targets agrees with the collective's inverse
                 tg = oracle.scatter(shards[key], world)
                 assert torch.equal(oracle.gather(tg, world)[rank].view(torch.uint8), back.view(torch.uint8))
+        # the chunk exchange: a destination-major payload through all_to_all_single
+        for chunk in (16, 48, 4096):
+            gen = torch.Generator().manual_seed(7 * chunk)
+            payloads = [torch.randint(0, 256, (world, chunk), generator=gen, dtype=torch.uint8) for _ in range(world)]
+            recv = torch.empty_like(payloads[rank])
+            dist.all_to_all_single(recv.view(-1), payloads[rank].view(-1))
+            assert torch.equal(recv, oracle.exchange_chunks(payloads, world)[rank]), (rank, chunk)
         with open(os.path.join(result_dir, f"ok{rank}"), "w") as f:
             f.write("ok")
     finally:

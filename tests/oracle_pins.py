@@ -400,6 +400,38 @@ def check_fused_payload_brute_force(lib):
     assert seen == 3 * P * B * Sl * H * D
 
 
+def check_head_chunks_compose_to_the_scatter(lib):
+    """Head-chunk scatters of a partition of [0, Hl) into one set of targets equal
+    the whole scatter, and a single chunk leaves the other heads untouched."""
+    P, B, Sl, H, D = 2, 2, 3, 8, 8
+    srcs = synth.unique_id_shards(P, B, Sl, H, D)
+    whole = oracle.scatter(srcs, P, lib=lib)
+    Hl = H // P
+    fill = [torch.full_like(t, -1) for t in whole]
+    acc = fill
+    for h0, h1 in ((0, 1), (1, 3), (3, Hl)):
+        acc = oracle.scatter_heads_chunk(srcs, P, h0, h1, acc)
+    for g in range(P):
+        assert torch.equal(acc[g], whole[g]), g
+    one = oracle.scatter_heads_chunk(srcs, P, 1, 3, fill)
+    for g in range(P):
+        assert torch.equal(one[g][:, :, 1:3], whole[g][:, :, 1:3])
+        assert bool((one[g][:, :, :1] == -1).all()) and bool((one[g][:, :, 3:] == -1).all())
+
+
+def check_exchange_chunks_is_the_scatter_of_single_head_bands(lib):
+    """The chunk exchange equals the Ulysses scatter with one head per band and the
+    chunk as the head row (sequence length 1): the same all-to-all."""
+    P = 3
+    gen = torch.Generator().manual_seed(5)
+    payloads = [torch.randint(0, 256, (P, 32), generator=gen, dtype=torch.uint8) for _ in range(P)]
+    ex = oracle.exchange_chunks(payloads, P)
+    as_shards = [x.view(1, 1, P, 32) for x in payloads]  # [B=1, Sl=1, H=P, D=32]
+    sc = oracle.scatter(as_shards, P, lib=lib)  # [1, P, 1, 32] per group
+    for g in range(P):
+        assert torch.equal(ex[g], sc[g].view(P, 32)), g
+
+
 ALL_CHECKS = [
     check_codec_decode,
     check_codec_encode,
@@ -415,4 +447,6 @@ ALL_CHECKS = [
     check_neox_rotate_half_textbook,
     check_fused_scatter_neox_composition,
     check_fused_payload_brute_force,
+    check_head_chunks_compose_to_the_scatter,
+    check_exchange_chunks_is_the_scatter_of_single_head_bands,
 ]

@@ -115,6 +115,23 @@ def test_fused_layout_targets_checked_before_any_cuda_call(tf):
                                               None) == 1
 
 
+def test_head_chunk_and_exchange_checked_before_any_cuda_call(tf):
+    lib = tf.lib()
+    P, B, Sl, H, D = 2, 1, 4, 8, 64
+    arr = (ctypes.c_void_p * P)(*([FAKE] * P))
+    st = (tf.Strides * 3)(*([tf.Strides(Sl * H * D, H * D, D)] * 3))
+    heads = lib.tf_ulysses_scatter_qkv_heads_into
+    for h0, h1 in ((-1, 2), (2, 2), (3, 1), (0, 5)):  # Hl = 4
+        assert heads(arr, arr, arr, st, P, B, Sl, H, D, 1, 0, None, h0, h1, arr, arr, arr, None) == 1, (h0, h1)
+    bad = (ctypes.c_void_p * P)(FAKE, FAKE + 8)
+    assert heads(arr, arr, arr, st, P, B, Sl, H, D, 1, 0, None, 0, 2, bad, arr, arr, None) == 3
+    ex = lib.tf_ulysses_exchange_chunks
+    assert ex(arr, arr, 0, 64, None) == 1
+    assert ex(None, arr, P, 64, None) == 1
+    assert ex(arr, arr, P, 40, None) == 3    # chunk not a multiple of 16 bytes
+    assert ex(bad, arr, P, 64, None) == 3    # misaligned payload
+
+
 def test_gather_rejects_before_any_cuda_call(tf):
     lib = tf.lib()
     arr = (ctypes.c_void_p * 2)(FAKE, FAKE)

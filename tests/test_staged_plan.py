@@ -20,7 +20,7 @@ static uint32_t rnd(uint32_t n) { x ^= x << 13; x ^= x >> 7; x ^= x << 17; retur
 int main() {
   long bad = 0, cases = 0;
   for (int it = 0; it < 4000; ++it) {
-    const uint32_t Sl = 1 + rnd(300), Hl = 1 + rnd(70);
+    const uint32_t Sl = 1 + rnd(300), Hl = rnd(4) == 0 ? 1 : 1 + rnd(70);
     const uint32_t rb = 16 * (1 + rnd(40));            // D * esize, a multiple of 16
     // source-like strides: packed heads or spread heads, token stride >= band
     const bool packed = rnd(3) != 0;

@@ -72,10 +72,14 @@ def _declare(lib):
     lib.tf_ulysses_scatter_qkv_into.argtypes = [PP, PP, PP, ctypes.POINTER(Strides), i32, i32, i32, i32, i32,
                                                 i32, i32, ctypes.POINTER(NormRope), PP, PP, PP, vp]
     lib.tf_ulysses_scatter_qkv_noalloc.argtypes = lib.tf_ulysses_scatter_qkv_into.argtypes
+    lib.tf_ulysses_scatter_qkv_heads_into.argtypes = [PP, PP, PP, ctypes.POINTER(Strides), i32, i32, i32, i32, i32,
+                                                      i32, i32, ctypes.POINTER(NormRope), i32, i32, PP, PP, PP, vp]
+    lib.tf_ulysses_exchange_chunks.argtypes = [PP, PP, i32, ctypes.c_size_t, vp]
     lib.tf_ulysses_gather_out.argtypes = [ctypes.c_char_p, PP, ctypes.POINTER(Strides), i32, i32, i32, i32, i32,
                                           i32, PP, ctypes.POINTER(Strides), vp, ctypes.POINTER(Targets)]
     lib.tf_ulysses_rope_table.argtypes = [ctypes.c_float, i32, i32, vp, ctypes.POINTER(ctypes.c_void_p)]
-    for name in ("tf_ulysses_scatter_qkv", "tf_ulysses_scatter_qkv_into", "tf_ulysses_scatter_qkv_noalloc",
+    for name in ("tf_ulysses_scatter_qkv_heads_into", "tf_ulysses_exchange_chunks",
+                 "tf_ulysses_scatter_qkv", "tf_ulysses_scatter_qkv_into", "tf_ulysses_scatter_qkv_noalloc",
                  "tf_ulysses_gather_out",
                  "tf_ulysses_rope_table", "tf_ulysses_cache_clear"):
         getattr(lib, name).restype = i32
@@ -286,6 +290,41 @@ def scatter_qkv_noalloc(q, k, v, q_out, k_out=None, v_out=None, *, norm_rope=Fal
         ctypes.byref(nr) if nr is not None else None, _ptr_array(q_out), _ptr_array(k_out), _ptr_array(v_out),
         _stream_handle(stream)))
     return q_out, k_out, v_out
+
+
+def scatter_qkv_heads_into(q, k, v, q_out, k_out=None, v_out=None, *, h0, h1, norm_rope=False, q_weight=None,
+                           k_weight=None, eps=1e-6, theta=10000.0, cos_sin=None, rope="interleaved", layout="bshd",
+                           stream=None):
+    """``scatter_qkv_into`` restricted to heads [h0, h1) of every head band: those
+    heads of the caller's targets are written, every other element is kept."""
+    P, B, Sl, H, D, strides = _scatter_args(q, k, v)
+    _check_targets((q_out, k_out, v_out), layout)
+    mode = _mode(norm_rope, rope, layout)
+    nr = _norm_rope(q_weight, k_weight, eps, theta, cos_sin) if norm_rope else None
+    _check(lib().tf_ulysses_scatter_qkv_heads_into(
+        _ptr_array(q), _ptr_array(k), _ptr_array(v), strides, P, B, Sl, H, D, _dtype_code(q[0].dtype), mode,
+        ctypes.byref(nr) if nr is not None else None, int(h0), int(h1), _ptr_array(q_out), _ptr_array(k_out),
+        _ptr_array(v_out), _stream_handle(stream)))
+    return q_out, k_out, v_out
+
+
+def exchange_chunks(src, dst=None, *, stream=None):
+    """All-to-all over destination-major payloads: P tensors ``src[r]`` of P equal
+    chunks (chunk g goes to rank g) -> ``dst[g]`` holding chunk g of every rank in
+    rank order.  Tensors must be contiguous with P*chunk bytes, chunk a multiple
+    of 16 bytes; ``dst`` defaults to new tensors shaped like ``src``."""
+    P = len(src)
+    if any(not t.is_contiguous() or t.shape != src[0].shape or t.dtype != src[0].dtype for t in src):
+        raise ValueError("src must be P contiguous tensors of one shape and dtype")
+    nbytes = src[0].numel() * src[0].element_size()
+    if nbytes % P:
+        raise ValueError("a payload must split into P equal chunks")
+    if dst is None:
+        dst = [torch.empty_like(t) for t in src]
+    if any(not t.is_contiguous() or t.numel() * t.element_size() != nbytes for t in dst):
+        raise ValueError("dst must be P contiguous tensors of the payload size")
+    _check(lib().tf_ulysses_exchange_chunks(_ptr_array(src), _ptr_array(dst), P, nbytes // P, _stream_handle(stream)))
+    return dst
 
 
 def gather_out(tag, attn, out=None, *, stream=None):

@@ -23,9 +23,10 @@
 //    computes.  One 32-byte vector per lane per row and slot; loads bypass L1,
 //    stores are evict-first.
 //  * The (cos, sin) entries are loaded once per token and reused across its
-//    heads and by Q and K.  Destination rows are d_h bytes apart, so the same
-//    code writes the separate [B, S, Hl, D] targets (d_h = D*esize) and the
-//    fused receive layout [B, S, Hl, 3*D] (d_h = 3*D*esize, slot offsets 0, D, 2D).
+//    heads and by Q and K.  Destination row (t, h) sits at t*d_t + h*d_h, so the
+//    same code writes the separate [B, S, Hl, D] targets, the fused receive
+//    layout [B, S, Hl, 3*D] (d_h = 3*D*esize, slot offsets 0, D, 2D) and a head
+//    chunk of wider targets (d_t > Hl*d_h; source bands Hg heads apart).
 #include "device_common.cuh"
 #include "relayout.h"
 
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(kThreads, kNF > 0 ? TFU_FUSED_MIN_BLOCKS : TFU
         uint8_t* dst[kSlots];
 #pragma unroll
         for (int x = 0; x < kSlots; ++x) {
-            src[x] = p.src[x][r] + int64_t(b) * p.s_b[x] + int64_t(g) * p.Hl * p.s_h[x] + int64_t(dv) * VW;
+            src[x] = p.src[x][r] + int64_t(b) * p.s_b[x] + int64_t(g) * p.Hg * p.s_h[x] + int64_t(dv) * VW;
             dst[x] = p.dst[x][g] + int64_t(b) * p.d_b[x] + int64_t(r) * p.Sl * p.d_t[x] + int64_t(dv) * VW;
         }
         const uint32_t R0 = c * p.rpu;
@@ -106,8 +107,9 @@ __global__ void __launch_bounds__(kThreads, kNF > 0 ? TFU_FUSED_MIN_BLOCKS : TFU
         };
         auto compute_store = [&](Vec<VW>(&buf)[kSlots], uint32_t R) {
             const bool valid = R < r_end;
+            const uint32_t t = fastdiv(R, p.div_hl);
+            const uint32_t h = R - t * p.Hl;
             if constexpr (kNF > 0) {
-                const uint32_t t = fastdiv(R, p.div_hl);
                 if (valid && t != t_cached) {
                     const float* tab = tab_lane + size_t(t) * kRowFloats;
 #pragma unroll
@@ -121,7 +123,8 @@ __global__ void __launch_bounds__(kThreads, kNF > 0 ? TFU_FUSED_MIN_BLOCKS : TFU
             }
             if (valid) {
 #pragma unroll
-                for (int x = 0; x < kSlots; ++x) st_stream<VW>(dst[x] + int64_t(R) * p.d_h[x], buf[x]);
+                for (int x = 0; x < kSlots; ++x)
+                    st_stream<VW>(dst[x] + int64_t(t) * p.d_t[x] + int64_t(h) * p.d_h[x], buf[x]);
             }
         };
         Vec<VW> bufs[kDepth][kSlots];

@@ -85,12 +85,12 @@ __device__ __forceinline__ Plane decode_plane(const RelayoutParams& p, uint32_t 
     pl.dt = p.d_t[x];
     pl.dh = p.d_h[x];
     if constexpr (kDir == Dir::kScatter) {
-        pl.src = p.src[x][r] + int64_t(b) * p.s_b[x] + int64_t(g) * p.Hl * pl.sh;
+        pl.src = p.src[x][r] + int64_t(b) * p.s_b[x] + int64_t(g) * p.Hg * pl.sh;
         pl.dst = p.dst[x][g] + int64_t(b) * p.d_b[x] + int64_t(r) * p.Sl * pl.dt;
         pl.pos0 = r * p.Sl;
     } else {
         pl.src = p.src[x][g] + int64_t(b) * p.s_b[x] + int64_t(r) * p.Sl * pl.st;
-        pl.dst = p.dst[x][r] + int64_t(b) * p.d_b[x] + int64_t(g) * p.Hl * pl.dh;
+        pl.dst = p.dst[x][r] + int64_t(b) * p.d_b[x] + int64_t(g) * p.Hg * pl.dh;
         pl.pos0 = 0;
     }
     return pl;

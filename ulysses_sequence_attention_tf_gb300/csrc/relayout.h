@@ -88,6 +88,9 @@ struct RelayoutParams {
     uint32_t rpu;         // rows per unit (tma_rows_per_unit)
     uint32_t plane_rows;  // Sl * Hl
     uint32_t rope_neox;   // fused slots: 0 interleaved pairs (2i, 2i+1), 1 half-split pairs (i, i + D/2)
+    uint32_t Hg;          // heads between consecutive head groups on the head-major side (scatter
+                          // source, gather destination): Hl, or the whole band when a launch moves
+                          // a head chunk of Hl heads out of every band
 };
 // Field order is part of the staged kernel's speed: inserting one 4-byte field
 // before `nx` (shifting every later field by 4 bytes) measured ~1.3 % slower

@@ -53,16 +53,12 @@ __device__ __forceinline__ int64_t vec_offset(const RelayoutParams& p, uint32_t 
     return int64_t(t) * st + int64_t(h) * sh + int64_t(dv) * VW;
 }
 
-// Scatter target rows of a plane are d_h bytes apart (row R = t*Hl + h; D*esize
-// for separate targets, 3*D*esize in the fused receive layout).
+// Destination offset of vector v of a plane: row (t, h) at t*dt + h*dh on
+// either side (scatter targets may be the fused receive layout or a head chunk
+// of wider targets).
 template <Dir kDir, int VW>
 __device__ __forceinline__ int64_t dst_offset(const RelayoutParams& p, const Plane& pl, uint32_t v) {
-    if constexpr (kDir == Dir::kScatter) {
-        const uint32_t row = fastdiv(v, p.div_vpr);
-        return int64_t(row) * pl.dh + int64_t(v - row * p.vpr) * VW;
-    } else {
-        return vec_offset<VW>(p, v, pl.dt, pl.dh);
-    }
+    return vec_offset<VW>(p, v, pl.dt, pl.dh);
 }
 
 template <Dir kDir, int VW, int VB>
@@ -125,6 +121,7 @@ __device__ __forceinline__ void norm_rope_rows(const RelayoutParams& p, const Pl
         const uint32_t i = r_beg + j;
         const bool valid = j < per && i < n_rows;
         const uint32_t t = fastdiv(row0 + i, p.div_hl);
+        const uint32_t h = row0 + i - t * p.Hl;
         if (valid && t != t_cached) {
             const float* tab = tab_lane + size_t(t) * kRowFloats;
 #pragma unroll
@@ -133,7 +130,7 @@ __device__ __forceinline__ void norm_rope_rows(const RelayoutParams& p, const Pl
         }
         // every lane runs the row reduction (it shuffles); only valid rows are written
         norm_rope_core<kF, kLanes, NP, kNeox>(buf.w, wpk, cs, p.eps);
-        if (valid) st_stream<VW>(pl.dst + int64_t(row0 + i) * pl.dh + int64_t(dv) * VW, buf);
+        if (valid) st_stream<VW>(pl.dst + int64_t(t) * pl.dt + int64_t(h) * pl.dh + int64_t(dv) * VW, buf);
     };
     Vec<VW> b0, b1, b2, b3;
     load(b0, 0);

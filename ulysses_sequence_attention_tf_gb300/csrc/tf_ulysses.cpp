@@ -95,6 +95,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct Shape {
     int P, B, Sl, H, D, Hl, esize;
     tf_dtype dtype;
+    int Hg;  // heads between consecutive head groups on the head-major side (Hl unless a head chunk)
 };
 
 tf_status check_shape(int P, int B, int Sl, int H, int D, tf_dtype dtype, Shape* sh) {
@@ -107,7 +108,7 @@ tf_status check_shape(int P, int B, int Sl, int H, int D, tf_dtype dtype, Shape*
     if ((int64_t(D) * e) % 16 != 0)
         return fail(TF_ERR_ALIGNMENT, "a head row (D=%d x %d B) must be a multiple of 16 bytes", D, e);
     if (int64_t(P) * Sl > INT32_MAX) return fail(TF_ERR_UNSUPPORTED, "P*S_local too large");
-    *sh = Shape{P, B, Sl, H, D, H / P, e, dtype};
+    *sh = Shape{P, B, Sl, H, D, H / P, e, dtype, H / P};
     return TF_OK;
 }
 
@@ -162,6 +163,7 @@ tf_status plan_units(RelayoutParams& p, const Shape& sh) {
     p.B = uint32_t(sh.B);
     p.Sl = uint32_t(sh.Sl);
     p.Hl = uint32_t(sh.Hl);
+    p.Hg = uint32_t(sh.Hg);
     if (p.vec_bytes != 16 && p.vec_bytes != 32) p.vec_bytes = 16;
     p.vpr = uint32_t(int64_t(sh.D) * sh.esize / p.vec_bytes);
     const uint64_t nv = uint64_t(sh.Sl) * uint64_t(sh.Hl) * p.vpr;
@@ -209,6 +211,7 @@ tf_status launch_planned(RelayoutParams& p, const Shape& sh, tfu::Dir dir, tfu::
     p.B = uint32_t(sh.B);
     p.Sl = uint32_t(sh.Sl);
     p.Hl = uint32_t(sh.Hl);
+    p.Hg = uint32_t(sh.Hg);
     p.row_bytes = rb;
     p.plane_rows = uint32_t(rows);
     p.div_hl = tfu::make_fastdiv(p.Hl);
@@ -655,6 +658,82 @@ TF_API tf_status tf_ulysses_scatter_qkv_noalloc(const void* const* q, const void
         pl.p.table = table;
     }
     return launch_planned(pl.p, pl.sh, tfu::Dir::kScatter, pl.fused, pl.sh.Sl, int64_t(P) * S_local, st);
+}
+
+// Head-chunk scatter into caller-owned targets: heads [h0, h1) of every band.
+TF_API tf_status tf_ulysses_scatter_qkv_heads_into(const void* const* q, const void* const* k, const void* const* v,
+                                                   const tf_strides* strides, int P, int B, int S_local, int H,
+                                                   int D, tf_dtype dtype, tf_mode mode, const tf_norm_rope* nr,
+                                                   int h0, int h1, void* const* q_out, void* const* k_out,
+                                                   void* const* v_out, void* stream) {
+    ScatterPlan pl;
+    tf_status s = plan_scatter(q, k, v, strides, P, B, S_local, H, D, dtype, mode, nr, &pl);
+    if (s != TF_OK) return s;
+    if (h0 < 0 || h1 <= h0 || h1 > pl.sh.Hl)
+        return fail(TF_ERR_INVALID, "head chunk [%d, %d) is not a non-empty range within [0, %d)", h0, h1, pl.sh.Hl);
+    if ((s = set_caller_targets(pl, q_out, k_out, v_out)) != TF_OK) return s;
+    // the chunk: sources start h0 heads into every band, targets h0 heads into every token;
+    // bands stay Hl heads apart (Hg), a plane has (h1 - h0) heads per token
+    RelayoutParams& p = pl.p;
+    for (uint32_t x = 0; x < p.nx; ++x)
+        for (int i = 0; i < P; ++i) {
+            if (p.src[x][i]) p.src[x][i] += int64_t(h0) * p.s_h[x];
+            if (p.dst[x][i]) p.dst[x][i] += int64_t(h0) * p.d_h[x];
+        }
+    pl.sh.Hg = pl.sh.Hl;
+    pl.sh.Hl = h1 - h0;
+    int device = 0;
+    if ((s = current_device(&device)) != TF_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Table* used = nullptr;
+    if (pl.fused != tfu::Fused::kNone && !nr->cos_sin) {
+        std::lock_guard<std::mutex> lock(g_mu);
+        return launch_scatter(pl, nr, device, st, &used);
+    }
+    return launch_scatter(pl, nr, device, st, &used);
+}
+
+// All-to-all over destination-major payloads: out_g[r] = in_r[g], chunks of
+// chunk_bytes.  As a scatter: B = 1, one head per band (H = P), a chunk is
+// S_local rows of `row` bytes, sources read with token stride `row` and head
+// stride chunk_bytes.
+TF_API tf_status tf_ulysses_exchange_chunks(const void* const* src, void* const* dst, int P, size_t chunk_bytes,
+                                            void* stream) {
+    if (P < 1 || P > TF_ULYSSES_MAX_SHARDS) return fail(TF_ERR_INVALID, "P=%d outside [1, %d]", P, TF_ULYSSES_MAX_SHARDS);
+    if (!src || !dst) return fail(TF_ERR_INVALID, "src or dst is NULL");
+    if (chunk_bytes % 16 != 0) return fail(TF_ERR_ALIGNMENT, "chunk_bytes=%zu is not a multiple of 16", chunk_bytes);
+    tf_status s;
+    if (chunk_bytes > 0) {
+        if ((s = check_ptrs("src", src, P)) != TF_OK) return s;
+        if ((s = check_ptrs("dst", dst, P)) != TF_OK) return s;
+    }
+    // row: the whole chunk when it fits a stage, else the largest power of two <= a
+    // stage that divides it (consecutive rows of a chunk are contiguous on both sides)
+    size_t row = chunk_bytes <= tfu::kStageBytes && chunk_bytes > 0 ? chunk_bytes : size_t(tfu::kStageBytes);
+    while (row > 16 && chunk_bytes % row != 0) row /= 2;
+    const uint64_t rows = chunk_bytes / row;
+    if (rows > uint64_t(INT32_MAX)) return fail(TF_ERR_UNSUPPORTED, "chunk_bytes too large");
+    Shape sh;
+    if ((s = check_shape(P, 1, int(rows), P, int(row), TF_BYTE, &sh)) != TF_OK) return s;
+    RelayoutParams p{};
+    p.nx = 1;
+    for (int i = 0; i < P; ++i) {
+        p.src[0][i] = static_cast<const uint8_t*>(src[i]);
+        p.dst[0][i] = static_cast<uint8_t*>(dst[i]);
+    }
+    p.s_b[0] = int64_t(P) * int64_t(chunk_bytes);
+    p.s_t[0] = int64_t(row);
+    p.s_h[0] = int64_t(chunk_bytes);
+    p.d_b[0] = int64_t(P) * int64_t(chunk_bytes);
+    p.d_t[0] = int64_t(row);
+    p.d_h[0] = int64_t(row);
+    p.vec_bytes = 16;
+    if ((s = plan_units(p, sh)) != TF_OK) return s;
+    int device = 0;
+    if ((s = current_device(&device)) != TF_OK) return s;
+    if (rows == 0) return TF_OK;
+    return launch_planned(p, sh, tfu::Dir::kScatter, tfu::Fused::kNone, int64_t(rows), int64_t(P) * int64_t(rows),
+                          static_cast<cudaStream_t>(stream));
 }
 
 TF_API tf_status tf_ulysses_gather_out(const char* tag, const void* const* attn, const tf_strides* attn_strides,

@@ -40,7 +40,7 @@ template <class F>
 __host__ __device__ inline void for_each_run(uint32_t R0, uint32_t R1, uint32_t Hl, int64_t st, int64_t sh,
                                              uint32_t row_bytes, F&& f) {
     if (R1 <= R0) return;
-    const bool heads_packed = sh == int64_t(row_bytes);
+    const bool heads_packed = Hl == 1 || sh == int64_t(row_bytes);  // one head per token is always packed
     if (heads_packed && st == int64_t(Hl) * row_bytes) {  // the whole plane is contiguous
         f(0u, R1 - R0, int64_t(R0) * row_bytes);
         return;
