@@ -39,6 +39,22 @@
  *    the launch was enqueued, not that it finished.
  *  - All entry points are thread-safe; the target cache is process-wide and
  *    guarded by a mutex.
+ *
+ * CUDA graphs (flashinfer PR #6332 commit message, "Description", "CUDA graphs":
+ * a prepared call allocates nothing; a size first seen inside a capture raises
+ * instead of allocating; replays interleave with eager calls).  Every entry
+ * point may be called while `stream` is being captured (cudaStreamBeginCapture,
+ * torch.cuda.graph).  Inside a capture the library allocates and frees nothing:
+ * a call whose cache entry or RoPE table does not exist yet returns
+ * TF_ERR_UNSUPPORTED before enqueuing anything -- make one eager call with the
+ * same key (or tf_ulysses_rope_table) first.  Events are recorded as external
+ * event nodes, so every replay records `done`; waits on events recorded outside
+ * the capture become external waits.  A captured call writes the targets (the
+ * rotating slot, see tf_ulysses_set_slots) current at capture time, and every
+ * replay rewrites those; ordering replays against eager calls that read or
+ * write the same targets is the caller's, as for two eager calls on different
+ * streams.  tf_ulysses_scatter_qkv_noalloc additionally needs one eager call on
+ * the device before capturing (it looks up its scratch address).
  */
 #ifndef TF_ULYSSES_H
 #define TF_ULYSSES_H
@@ -59,6 +75,7 @@ extern "C" {
 #define TF_ULYSSES_ABI_VERSION 1
 #define TF_ULYSSES_MAX_SHARDS 8      /* largest P */
 #define TF_ULYSSES_CACHE_CAPACITY 12 /* cached target sets (TeleFuser PR #27: "up to 12 cached targets") */
+#define TF_ULYSSES_MAX_SLOTS 8       /* rotating target sets per cache entry (tf_ulysses_set_slots) */
 
 typedef enum tf_status {
     TF_OK = 0,
@@ -321,6 +338,24 @@ TF_API void tf_ulysses_set_allocator(tf_alloc_fn alloc, tf_free_fn release, void
  * reading it.
  */
 TF_API tf_status tf_ulysses_device_status(int clear, unsigned *status);
+
+/*
+ * tf_ulysses_set_slots -- rotating target sets for a tag (flashinfer PR #6332
+ * commit message, "Description": outputs are views of the current receive slot
+ * and stay valid until the slot is reused num_slots calls later).  Cache entries
+ * created for `tag` after this call hold num_slots target sets (1..8, default 1)
+ * and successive calls with the same key write them in turn: the targets a call
+ * returns stay untouched for the next num_slots - 1 calls of that key.  Entries
+ * that already exist keep their slot count (tf_ulysses_cache_clear drops them).
+ * At most num_slots calls of one key may be captured into one graph without an
+ * eager call between (later captured calls would rewrite earlier ones' slots).
+ * Errors: TF_ERR_INVALID for a bad tag or num_slots.
+ */
+TF_API tf_status tf_ulysses_set_slots(const char *tag, int num_slots);
+
+/* Number of device allocations (cache entries and RoPE tables) this library has
+ * made in this process: unchanged across calls that hit the cache. */
+TF_API uint64_t tf_ulysses_alloc_count(void);
 
 /* One-line reason for the calling thread's last non-TF_OK status ("" if none). */
 TF_API const char *tf_ulysses_last_error(void);

@@ -132,6 +132,15 @@ def test_head_chunk_and_exchange_checked_before_any_cuda_call(tf):
     assert ex(bad, arr, P, 64, None) == 3    # misaligned payload
 
 
+def test_slot_configuration_checked(tf):
+    lib = tf.lib()
+    assert lib.tf_ulysses_set_slots(b"rot", 0) == 1
+    assert lib.tf_ulysses_set_slots(b"rot", 9) == 1
+    assert lib.tf_ulysses_set_slots(b"x" * 64, 2) == 1
+    assert lib.tf_ulysses_set_slots(b"rot", 2) == 0  # configuration only: no CUDA call
+    assert lib.tf_ulysses_alloc_count() == 0
+
+
 def test_gather_rejects_before_any_cuda_call(tf):
     lib = tf.lib()
     arr = (ctypes.c_void_p * 2)(FAKE, FAKE)

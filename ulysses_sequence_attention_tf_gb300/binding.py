@@ -94,6 +94,10 @@ def _declare(lib):
     lib.tf_ulysses_last_error.restype = ctypes.c_char_p
     lib.tf_ulysses_launch_count.argtypes = []
     lib.tf_ulysses_launch_count.restype = ctypes.c_uint64
+    lib.tf_ulysses_set_slots.argtypes = [ctypes.c_char_p, i32]
+    lib.tf_ulysses_set_slots.restype = i32
+    lib.tf_ulysses_alloc_count.argtypes = []
+    lib.tf_ulysses_alloc_count.restype = ctypes.c_uint64
     lib.tf_ulysses_abi_version.argtypes = []
     lib.tf_ulysses_abi_version.restype = i32
     del i64
@@ -365,6 +369,16 @@ def device_status(clear: bool = False) -> int:
     v = ctypes.c_uint()
     _check(lib().tf_ulysses_device_status(1 if clear else 0, ctypes.byref(v)))
     return int(v.value)
+
+
+def set_slots(tag, num_slots: int):
+    """Rotating target sets for cache entries of ``tag`` created from now on."""
+    _check(lib().tf_ulysses_set_slots(tag.encode() if isinstance(tag, str) else tag, int(num_slots)))
+
+
+def alloc_count() -> int:
+    """Device allocations the library has made in this process."""
+    return int(lib().tf_ulysses_alloc_count())
 
 
 def cache_entries() -> int:

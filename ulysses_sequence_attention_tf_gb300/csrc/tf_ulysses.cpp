@@ -32,6 +32,7 @@ using tfu::RelayoutParams;
 
 thread_local std::string g_last_error;
 std::atomic<uint64_t> g_launches{0};
+std::atomic<uint64_t> g_allocs{0};  // device allocations made (cache entries, tables)
 std::mutex g_mu;  // guards the cache, the tables and the allocator
 
 tf_status fail(tf_status s, const char* fmt, ...) {
@@ -48,6 +49,29 @@ tf_status cuda_fail(cudaError_t e, const char* what) {
     return fail(TF_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
+// ---------------------------------------------------------------- stream capture
+// CUDA-graph capture protocol (flashinfer PR #6332 commit message, "Description",
+// "CUDA graphs": a prepared call allocates nothing; a size first seen inside a
+// capture raises instead of allocating; captured calls interleave with eager
+// ones).  Inside a capture the library allocates and frees nothing, records its
+// events as external event nodes (so every replay records them) and waits on
+// events recorded outside the capture as external waits.
+tf_status capture_state(cudaStream_t s, bool* capturing) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    *capturing = st != cudaStreamCaptureStatusNone;
+    return TF_OK;
+}
+
+cudaError_t record_event(cudaEvent_t ev, cudaStream_t s, bool capturing) {
+    return capturing ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal) : cudaEventRecord(ev, s);
+}
+
+cudaError_t wait_event(cudaStream_t s, cudaEvent_t ev, bool capturing) {
+    return cudaStreamWaitEvent(s, ev, capturing ? cudaEventWaitExternal : 0);
+}
+
 // ---------------------------------------------------------------- allocator
 struct Allocator {
     tf_alloc_fn alloc = nullptr;
@@ -58,6 +82,7 @@ Allocator g_alloc;
 
 void* dev_alloc(const Allocator& a, size_t bytes, cudaStream_t s) {
     if (bytes == 0) return nullptr;
+    g_allocs.fetch_add(1);
     if (a.alloc) return a.alloc(bytes, s, a.ctx);
     void* p = nullptr;
     if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
@@ -273,16 +298,20 @@ uint64_t g_clock = 0;
 
 // Caller holds g_mu.  Returns a table with >= S rows for (theta, D) on `device`,
 // ordered on `stream` after its build.
-tf_status get_table(float theta, int S, int D, int device, cudaStream_t stream, Table** out) {
+tf_status get_table(float theta, int S, int D, int device, cudaStream_t stream, bool capturing, Table** out) {
     for (auto& t : g_tables) {
         if (t.device == device && t.D == D && t.S >= S && std::memcmp(&t.theta, &theta, sizeof theta) == 0) {
             t.stamp = ++g_clock;
-            cudaError_t e = cudaStreamWaitEvent(stream, t.last_use, 0);
+            cudaError_t e = wait_event(stream, t.last_use, capturing);
             if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(table)");
             *out = &t;
             return TF_OK;
         }
     }
+    if (capturing)
+        return fail(TF_ERR_UNSUPPORTED,
+                    "the RoPE table for (theta, S=%d, D=%d) is first needed inside a stream capture: make one eager "
+                    "call (or tf_ulysses_rope_table) before capturing; nothing is allocated during a capture", S, D);
     if (int(g_tables.size()) >= kMaxTables) {  // evict the least recently used table
         size_t lru = 0;
         for (size_t i = 1; i < g_tables.size(); ++i)
@@ -330,12 +359,29 @@ struct Entry {
     void* slab = nullptr;
     size_t bytes = 0;
     Allocator alloc;
-    void* buf[3][TF_ULYSSES_MAX_SHARDS] = {};
+    void* buf[3][TF_ULYSSES_MAX_SHARDS] = {};  // slot 0's buffers
+    size_t slot_bytes = 0;                     // slot s's buffers are slot 0's + s * slot_bytes
+    int slots = 1, next_slot = 0;              // rotating target sets; the next call writes next_slot
     cudaEvent_t done = nullptr;
-    cudaStream_t last_stream = nullptr;
+    cudaStream_t last_stream = nullptr;  // null: unknown (e.g. last written by a graph replay)
     uint64_t stamp = 0;
 };
 std::vector<Entry> g_entries;
+
+// Rotating target sets per tag (tf_ulysses_set_slots), read when an entry is created.
+std::vector<std::pair<std::string, int>> g_tag_slots;
+
+int slots_of(const std::string& tag) {
+    for (auto& ts : g_tag_slots)
+        if (ts.first == tag) return ts.second;
+    return 1;
+}
+
+// The buffer of tensor x, group/shard i, in the slot a call uses.
+void* slot_buffer(const Entry& e, int slot, int x, int i) {
+    uint8_t* base = static_cast<uint8_t*>(e.buf[x][i]);
+    return base ? base + size_t(slot) * e.slot_bytes : nullptr;
+}
 
 void reclaim_entry(Entry& e, cudaStream_t stream) {
     dev_release(e.alloc, e.slab, e.bytes, e.done, stream);
@@ -348,12 +394,12 @@ size_t round_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
 
 // Caller holds g_mu.  buffer_bytes: size of one target; counts[x]: buffers of tensor x.
 tf_status get_entry(const std::string& tag, int mode, int present, const Shape& sh, int device, size_t buffer_bytes,
-                    const int counts[3], cudaStream_t stream, Entry** out) {
+                    const int counts[3], cudaStream_t stream, bool capturing, Entry** out) {
     for (auto& e : g_entries) {
         if (e.tag == tag && e.mode == mode && e.present == present && e.P == sh.P && e.B == sh.B && e.Sl == sh.Sl &&
             e.H == sh.H && e.D == sh.D && e.dtype == int(sh.dtype) && e.device == device) {
             if (e.last_stream != stream) {  // order the rewrite after the previous one
-                cudaError_t err = cudaStreamWaitEvent(stream, e.done, 0);
+                cudaError_t err = wait_event(stream, e.done, capturing);
                 if (err != cudaSuccess) return cuda_fail(err, "cudaStreamWaitEvent(entry)");
             }
             e.stamp = ++g_clock;
@@ -361,6 +407,10 @@ tf_status get_entry(const std::string& tag, int mode, int present, const Shape& 
             return TF_OK;
         }
     }
+    if (capturing)
+        return fail(TF_ERR_UNSUPPORTED,
+                    "cache key (tag \"%s\", this shape, dtype and mode) first seen inside a stream capture: make one "
+                    "eager call with it before capturing; nothing is allocated during a capture", tag.c_str());
     if (int(g_entries.size()) >= TF_ULYSSES_CACHE_CAPACITY) {
         size_t lru = 0;
         for (size_t i = 1; i < g_entries.size(); ++i)
@@ -380,8 +430,10 @@ tf_status get_entry(const std::string& tag, int mode, int present, const Shape& 
     e.dtype = int(sh.dtype);
     e.device = device;
     e.alloc = g_alloc;
+    e.slots = slots_of(tag);
     const size_t stride = round_up(buffer_bytes, 256);
-    e.bytes = stride * size_t(counts[0] + counts[1] + counts[2]);
+    e.slot_bytes = stride * size_t(counts[0] + counts[1] + counts[2]);
+    e.bytes = e.slot_bytes * size_t(e.slots);
     e.slab = dev_alloc(e.alloc, e.bytes, stream);
     if (e.bytes && !e.slab) return fail(TF_ERR_OOM, "allocating %zu bytes of targets failed", e.bytes);
     size_t off = 0;
@@ -518,12 +570,13 @@ tf_status set_caller_targets(ScatterPlan& pl, void* const* q_out, void* const* k
 }
 
 // Caller holds g_mu when the plan needs a library table.
-tf_status launch_scatter(ScatterPlan& pl, const tf_norm_rope* nr, int device, cudaStream_t stream, Table** used) {
+tf_status launch_scatter(ScatterPlan& pl, const tf_norm_rope* nr, int device, cudaStream_t stream, bool capturing,
+                         Table** used) {
     *used = nullptr;
     if (pl.empty) return TF_OK;
     if (pl.fused != tfu::Fused::kNone && !nr->cos_sin) {
         Table* t = nullptr;
-        tf_status s = get_table(nr->theta, pl.sh.P * pl.sh.Sl, pl.sh.D, device, stream, &t);
+        tf_status s = get_table(nr->theta, pl.sh.P * pl.sh.Sl, pl.sh.D, device, stream, capturing, &t);
         if (s != TF_OK) return s;
         pl.p.table = t->ptr;
         *used = t;
@@ -531,7 +584,7 @@ tf_status launch_scatter(ScatterPlan& pl, const tf_norm_rope* nr, int device, cu
     tf_status s = launch_planned(pl.p, pl.sh, tfu::Dir::kScatter, pl.fused, pl.sh.Sl, int64_t(pl.sh.P) * pl.sh.Sl,
                                  stream);
     if (s != TF_OK) return s;
-    if (*used) cudaEventRecord((*used)->last_use, stream);
+    if (*used) record_event((*used)->last_use, stream, capturing);
     return TF_OK;
 }
 
@@ -566,6 +619,8 @@ TF_API tf_status tf_ulysses_scatter_qkv(const char* tag, const void* const* q, c
     int device = 0;
     if ((s = current_device(&device)) != TF_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    bool cap = false;
+    if ((s = capture_state(st, &cap)) != TF_OK) return s;
 
     std::lock_guard<std::mutex> lock(g_mu);
     size_t target_bytes = size_t(B) * size_t(P) * size_t(S_local) * size_t(pl.sh.Hl) * size_t(D) * pl.sh.esize;
@@ -577,11 +632,13 @@ TF_API tf_status tf_ulysses_scatter_qkv(const char* tag, const void* const* q, c
         counts[1] = counts[2] = 0;
     }
     Entry* e = nullptr;
-    if ((s = get_entry(key, int(mode), pl.present, pl.sh, device, target_bytes, counts, st, &e)) != TF_OK) return s;
+    if ((s = get_entry(key, int(mode), pl.present, pl.sh, device, target_bytes, counts, st, cap, &e)) != TF_OK)
+        return s;
+    const int slot_now = e->next_slot;
     void* bufs[3][TF_ULYSSES_MAX_SHARDS] = {};
     for (int x = 0; x < 3; ++x)
         for (int g = 0; g < P; ++g) {
-            uint8_t* base = static_cast<uint8_t*>(e->buf[pl.fused_layout ? 0 : x][g]);
+            uint8_t* base = static_cast<uint8_t*>(slot_buffer(*e, slot_now, pl.fused_layout ? 0 : x, g));
             bufs[x][g] = base ? base + pl.row_off[x] : nullptr;
         }
     for (int x = 0; x < 3; ++x) {
@@ -590,10 +647,11 @@ TF_API tf_status tf_ulysses_scatter_qkv(const char* tag, const void* const* q, c
         for (int g = 0; g < P; ++g) pl.p.dst[slot][g] = static_cast<uint8_t*>(bufs[x][g]);
     }
     Table* used = nullptr;
-    if ((s = launch_scatter(pl, nr, device, st, &used)) != TF_OK) return s;
-    cudaError_t err = cudaEventRecord(e->done, st);
+    if ((s = launch_scatter(pl, nr, device, st, cap, &used)) != TF_OK) return s;
+    cudaError_t err = record_event(e->done, st, cap);
     if (err != cudaSuccess) return cuda_fail(err, "cudaEventRecord");
-    e->last_stream = st;
+    e->last_stream = cap ? nullptr : st;  // a replay may run on any stream
+    e->next_slot = (slot_now + 1) % e->slots;
     std::memset(out, 0, sizeof *out);
     for (int g = 0; g < P; ++g) {
         out->q[g] = bufs[0][g];
@@ -616,12 +674,14 @@ TF_API tf_status tf_ulysses_scatter_qkv_into(const void* const* q, const void* c
     int device = 0;
     if ((s = current_device(&device)) != TF_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    bool cap = false;
+    if ((s = capture_state(st, &cap)) != TF_OK) return s;
     Table* used = nullptr;
     if (pl.fused != tfu::Fused::kNone && !nr->cos_sin) {  // the resident table lives under the lock
         std::lock_guard<std::mutex> lock(g_mu);
-        return launch_scatter(pl, nr, device, st, &used);
+        return launch_scatter(pl, nr, device, st, cap, &used);
     }
-    return launch_scatter(pl, nr, device, st, &used);
+    return launch_scatter(pl, nr, device, st, cap, &used);
 }
 
 // Allocation-free scatter: the library-built cos/sin table goes to the fixed
@@ -685,12 +745,14 @@ TF_API tf_status tf_ulysses_scatter_qkv_heads_into(const void* const* q, const v
     int device = 0;
     if ((s = current_device(&device)) != TF_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    bool cap = false;
+    if ((s = capture_state(st, &cap)) != TF_OK) return s;
     Table* used = nullptr;
     if (pl.fused != tfu::Fused::kNone && !nr->cos_sin) {
         std::lock_guard<std::mutex> lock(g_mu);
-        return launch_scatter(pl, nr, device, st, &used);
+        return launch_scatter(pl, nr, device, st, cap, &used);
     }
-    return launch_scatter(pl, nr, device, st, &used);
+    return launch_scatter(pl, nr, device, st, cap, &used);
 }
 
 // All-to-all over destination-major payloads: out_g[r] = in_r[g], chunks of
@@ -772,21 +834,26 @@ TF_API tf_status tf_ulysses_gather_out(const char* tag, const void* const* attn,
     int device = 0;
     if ((s = current_device(&device)) != TF_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    bool cap = false;
+    if ((s = capture_state(st, &cap)) != TF_OK) return s;
 
     std::lock_guard<std::mutex> lock(g_mu);
     const size_t out_bytes = size_t(B) * size_t(S_local) * size_t(H) * size_t(D) * sh.esize;
     int counts[3] = {dst ? 0 : P, 0, 0};
     Entry* e = nullptr;
     const int present = dst ? 0 : 1;  // caller-owned outputs and cached outputs are different keys
-    if ((s = get_entry(key, int(TF_MODE_GATHER), present, sh, device, dst ? 0 : out_bytes, counts, st, &e)) != TF_OK)
+    if ((s = get_entry(key, int(TF_MODE_GATHER), present, sh, device, dst ? 0 : out_bytes, counts, st, cap, &e)) !=
+        TF_OK)
         return s;
-    for (int r = 0; r < P; ++r) p.dst[0][r] = static_cast<uint8_t*>(dst ? dst[r] : e->buf[0][r]);
+    const int slot_now = e->next_slot;
+    for (int r = 0; r < P; ++r) p.dst[0][r] = static_cast<uint8_t*>(dst ? dst[r] : slot_buffer(*e, slot_now, 0, r));
     if (!empty) {
         if ((s = launch_planned(p, sh, tfu::Dir::kGather, tfu::Fused::kNone, S, S_local, st)) != TF_OK) return s;
     }
-    cudaError_t err = cudaEventRecord(e->done, st);
+    cudaError_t err = record_event(e->done, st, cap);
     if (err != cudaSuccess) return cuda_fail(err, "cudaEventRecord");
-    e->last_stream = st;
+    e->last_stream = cap ? nullptr : st;
+    e->next_slot = (slot_now + 1) % e->slots;
     std::memset(out, 0, sizeof *out);
     for (int r = 0; r < P; ++r) out->q[r] = p.dst[0][r];
     if (empty)
@@ -803,9 +870,11 @@ TF_API tf_status tf_ulysses_rope_table(float theta, int S, int D, void* stream, 
     int device = 0;
     tf_status s = current_device(&device);
     if (s != TF_OK) return s;
+    bool cap = false;
+    if ((s = capture_state(static_cast<cudaStream_t>(stream), &cap)) != TF_OK) return s;
     std::lock_guard<std::mutex> lock(g_mu);
     Table* t = nullptr;
-    if ((s = get_table(theta, S, D, device, static_cast<cudaStream_t>(stream), &t)) != TF_OK) return s;
+    if ((s = get_table(theta, S, D, device, static_cast<cudaStream_t>(stream), cap, &t)) != TF_OK) return s;
     *table = t->ptr;
     return TF_OK;
 }
@@ -827,6 +896,24 @@ TF_API tf_status tf_ulysses_cache_clear(void) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     return TF_OK;
 }
+
+TF_API tf_status tf_ulysses_set_slots(const char* tag, int num_slots) {
+    std::string key;
+    tf_status s = check_tag(tag, &key);
+    if (s != TF_OK) return s;
+    if (num_slots < 1 || num_slots > TF_ULYSSES_MAX_SLOTS)
+        return fail(TF_ERR_INVALID, "num_slots=%d outside [1, %d]", num_slots, TF_ULYSSES_MAX_SLOTS);
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (auto& ts : g_tag_slots)
+        if (ts.first == key) {
+            ts.second = num_slots;
+            return TF_OK;
+        }
+    g_tag_slots.emplace_back(key, num_slots);
+    return TF_OK;
+}
+
+TF_API uint64_t tf_ulysses_alloc_count(void) { return g_allocs.load(); }
 
 TF_API int tf_ulysses_cache_entries(void) {
     std::lock_guard<std::mutex> lock(g_mu);
