@@ -68,6 +68,10 @@ def load(path: str | None = None):
         lib.tfo_rmsnorm_rope_neox_row.restype = None
         lib.tfo_scatter_norm_rope.argtypes = [i32] * 6 + [vp, i64, i64, i64, vp, ctypes.c_float, vp, vp, i32]
         lib.tfo_scatter_norm_rope.restype = None
+        lib.tfo_project_row.argtypes = [i32, i32, vp, vp, i64, i32, i32, vp]
+        lib.tfo_project_row.restype = None
+        lib.tfo_project.argtypes = [i32, i32, i32, i32, vp, i64, vp, i64, vp]
+        lib.tfo_project.restype = None
         if path is None:
             _lib = lib
         return lib
@@ -188,6 +192,47 @@ def scatter_heads_chunk(srcs, P: int, h0: int, h1: int, full_targets):
     out = [t.clone() for t in full_targets]
     for g in range(P):
         out[g][:, :, h0:h1] = full[g][:, :, h0:h1]
+    return out
+
+
+def project(x: torch.Tensor, w: torch.Tensor, lib=None) -> torch.Tensor:
+    """QKV projection of the rows of ``x`` [M, K] by the nn.Linear weight ``w``
+    [N, K]: out[m, n] = round16(sum_k x[m, k] * w[n, k]) (exact sum, one rounding)."""
+    lib = lib or load()
+    w = w.contiguous()
+    if x.stride(-1) != 1:
+        x = x.contiguous()
+    _check_cpu([x, w])
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K or K > 8192:
+        raise ValueError("x [M, K] and w [N, K] with K <= 8192")
+    out = torch.empty((M, N), dtype=x.dtype)
+    lib.tfo_project(FMT[x.dtype], M, N, K, x.data_ptr(), x.stride(0), w.data_ptr(), w.stride(0), out.data_ptr())
+    return out
+
+
+def project_row_range(x_row: torch.Tensor, w: torch.Tensor, n0: int, n1: int, lib=None) -> torch.Tensor:
+    """Features [n0, n1) of the projection of one hidden vector ``x_row`` [K]."""
+    lib = lib or load()
+    x_row, w = x_row.contiguous(), w.contiguous()
+    _check_cpu([x_row, w])
+    out = torch.empty((n1 - n0,), dtype=x_row.dtype)
+    lib.tfo_project_row(FMT[x_row.dtype], x_row.numel(), x_row.data_ptr(), w.data_ptr(), w.stride(0), n0, n1,
+                        out.data_ptr())
+    return out
+
+
+def project_qkv(x_shards, w: torch.Tensor, H: int, D: int, lib=None):
+    """Q, K, V shards [B, Sl, H, D] of the projection of hidden-state shards
+    ``x_shards`` [B, Sl, hidden] by ``w`` [3*H*D, hidden] (Q, K, V feature blocks
+    in that order, head h at features [h*D, (h+1)*D) of each block)."""
+    out = {"q": [], "k": [], "v": []}
+    for x in x_shards:
+        B, Sl, K = x.shape
+        y = project(x.reshape(B * Sl, K), w, lib=lib).view(B, Sl, 3, H, D)
+        for i, key in enumerate("qkv"):
+            out[key].append(y[:, :, i].contiguous())
     return out
 
 

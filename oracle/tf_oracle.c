@@ -285,3 +285,41 @@ void tfo_scatter_norm_rope(int fmt, int P, int B, int Sl, int H, int D,
                             tfo_rmsnorm_rope_row(fmt, D, row, w, eps, table + p * D, trow);
                     }
 }
+
+/* ------------------------------------------------------------------------- */
+/* QKV projection (the GEMM in front of the exchange).                        */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * One row of the projection of flashinfer PR #6332 ("Description": a BF16 QKV
+ * projection feeds per-head RMSNorm, RoPE and the head exchange; "Assumptions /
+ * Operator math": order projection -> QK-norm -> RoPE, 16-bit operands and
+ * outputs).  x[0..K) is one token's hidden vector, w the [N][K] weight in the
+ * nn.Linear layout (row n holds output feature n, w_row elements apart); for
+ * n in [n0, n1):
+ *     out[n - n0] = round16( sum_k x[k] * w[n][k] )
+ * with the sum accumulated in double (products of 16-bit values are exact; the
+ * sum is exact up to double rounding) and rounded once to the 16-bit type.
+ */
+void tfo_project_row(int fmt, int K, const uint16_t *x, const uint16_t *w, int64_t w_row, int n0, int n1,
+                     uint16_t *out)
+{
+    double xd[8192];
+    for (int k = 0; k < K; ++k)
+        xd[k] = tfo_decode16(fmt, x[k]);
+    for (int n = n0; n < n1; ++n) {
+        const uint16_t *wn = w + (int64_t)n * w_row;
+        double acc = 0.0;
+        for (int k = 0; k < K; ++k)
+            acc += xd[k] * tfo_decode16(fmt, wn[k]);
+        out[n - n0] = tfo_encode16(fmt, acc);
+    }
+}
+
+/* All M rows of one shard: x [M][K] with row stride x_row, out [M][N] contiguous. */
+void tfo_project(int fmt, int M, int N, int K, const uint16_t *x, int64_t x_row, const uint16_t *w, int64_t w_row,
+                 uint16_t *out)
+{
+    for (int m = 0; m < M; ++m)
+        tfo_project_row(fmt, K, x + (int64_t)m * x_row, w, w_row, 0, N, out + (int64_t)m * N);
+}

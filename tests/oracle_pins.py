@@ -432,6 +432,56 @@ def check_exchange_chunks_is_the_scatter_of_single_head_bands(lib):
         assert torch.equal(ex[g], sc[g].view(P, 32)), g
 
 
+# ----------------------------------------------------------------------------
+# QKV projection
+# ----------------------------------------------------------------------------
+
+def check_projection_vs_fp64_matmul(lib):
+    """The projection equals a float64 library matmul of the same 16-bit values
+    rounded once to the 16-bit type (torch's round-to-nearest-even cast)."""
+    for dtype in (torch.bfloat16, torch.float16):
+        gen = synth.make_generator(31, "cpu")
+        for M, N, K in ((7, 40, 64), (33, 96, 320)):
+            x = torch.randn((M, K), generator=gen).to(dtype)
+            w = (torch.randn((N, K), generator=gen) / K ** 0.5).to(dtype)
+            got = oracle.project(x, w, lib=lib)
+            want = (x.double() @ w.double().T).to(dtype)
+            assert torch.equal(got.view(torch.int16), want.view(torch.int16)), (dtype, M, N, K)
+            # a column range of one row agrees with the whole projection
+            part = oracle.project_row_range(x[M // 2], w, 5, 29, lib=lib)
+            assert torch.equal(part.view(torch.int16), got[M // 2, 5:29].view(torch.int16))
+
+
+def check_projection_closed_forms(lib):
+    """Identity and permutation weights reproduce / permute the input exactly,
+    and a weight row of twos doubles the row sum (a power-of-two scale)."""
+    K = 48
+    x = (torch.arange(6 * K, dtype=torch.float32).view(6, K) / 7.0 - 17.0).to(torch.bfloat16)
+    eye = torch.eye(K).to(torch.bfloat16)
+    assert torch.equal(oracle.project(x, eye, lib=lib).view(torch.int16), x.view(torch.int16))
+    perm = torch.randperm(K, generator=torch.Generator().manual_seed(3))
+    got = oracle.project(x, eye[perm], lib=lib)
+    assert torch.equal(got.view(torch.int16), x[:, perm].view(torch.int16))
+    xs = torch.tensor([[1.0, 2.0, -0.5, 0.25]], dtype=torch.bfloat16)
+    twos = torch.full((1, 4), 2.0, dtype=torch.bfloat16)
+    assert float(oracle.project(xs, twos, lib=lib)[0, 0]) == 5.5
+
+
+def check_project_qkv_blocks(lib):
+    """Q, K, V come from feature blocks [0, HD), [HD, 2HD), [2HD, 3HD) of the
+    weight, head h from features [h*D, (h+1)*D) of its block."""
+    B, Sl, H, D, K = 2, 3, 2, 4, 8
+    gen = torch.Generator().manual_seed(4)
+    x = [torch.randn((B, Sl, K), generator=gen).to(torch.bfloat16)]
+    w = torch.randn((3 * H * D, K), generator=gen).to(torch.bfloat16)
+    out = oracle.project_qkv(x, w, H, D, lib=lib)
+    full = oracle.project(x[0].reshape(B * Sl, K), w, lib=lib)
+    for i, key in enumerate("qkv"):
+        for h in range(H):
+            want = full[:, i * H * D + h * D:i * H * D + (h + 1) * D].reshape(B, Sl, D)
+            assert torch.equal(out[key][0][:, :, h].view(torch.int16), want.view(torch.int16)), (key, h)
+
+
 ALL_CHECKS = [
     check_codec_decode,
     check_codec_encode,
@@ -449,4 +499,7 @@ ALL_CHECKS = [
     check_fused_payload_brute_force,
     check_head_chunks_compose_to_the_scatter,
     check_exchange_chunks_is_the_scatter_of_single_head_bands,
+    check_projection_vs_fp64_matmul,
+    check_projection_closed_forms,
+    check_project_qkv_blocks,
 ]

@@ -30,6 +30,9 @@ MUTANTS = {
     "neox_table_entry_of_element": ("float cos_i = cs[2 * i], sin_i = cs[2 * i + 1];",
                                     "float cos_i = cs[i], sin_i = cs[i + 1];"),
     "neox_style_ignored_in_scatter": ("        if (neox)\n", "        if (0)\n"),
+    "projection_transposed_weight": ("const uint16_t *wn = w + (int64_t)n * w_row;", "const uint16_t *wn = w + n;"),
+    "projection_drops_last_term": ("for (int k = 0; k < K; ++k)\n            acc +=", "for (int k = 0; k < K - 1; ++k)\n            acc +="),
+    "projection_truncates": ("out[n - n0] = tfo_encode16(fmt, acc);", "out[n - n0] = tfo_encode16(fmt, (float)(int)acc);"),
 }
 
 
