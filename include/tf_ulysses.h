@@ -287,6 +287,38 @@ TF_API tf_status tf_ulysses_exchange_chunks(const void *const *src, void *const 
                                             void *stream);
 
 /*
+ * tf_ulysses_project_qkv_into -- the QKV projection in front of the exchange,
+ * fused with it (flashinfer PR #6332 commit message, "Description": the BF16
+ * QKV projection, per-head RMSNorm of Q and K, interleaved RoPE and the head
+ * exchange in one call, every head band stored straight from the GEMM
+ * epilogue).  For shard r, token row m = b*S_local + t and feature n:
+ *     Y[m, n] = round_bf16( sum_k x_r[m, k] * w_qkv[n, k] )   (fp32 accumulation
+ *                                                             on the tensor cores)
+ * Features [0, HD), [HD, 2HD), [2HD, 3HD) (HD = H*D) are Q, K and V, head h at
+ * features [h*D, (h+1)*D) of its block; each head row is written to head group
+ * h / Hl of the targets exactly as tf_ulysses_scatter_qkv_into writes a shard's
+ * head row, after the RMSNorm + RoPE of tf_norm_rope for Q and K when mode is
+ * TF_MODE_SCATTER_NORM_ROPE.  The projection output is rounded to bf16 before
+ * the normalisation, as a separate bf16 projection would (the pages' order
+ * projection -> QK-norm -> RoPE, BF16 operands and outputs).
+ *  x            host array of P device pointers; shard r's hidden states, rows
+ *               m = b*S_local + t of `hidden` bf16 elements, x_row_stride elements
+ *               apart (>= hidden, a multiple of 8).
+ *  w_qkv        device [3*H*D][hidden] bf16 weight (the nn.Linear layout: row n
+ *               is output feature n), rows w_row_stride elements apart.
+ *  dtype        TF_BF16;  D = 128;  H even (two heads per output tile);
+ *               hidden a multiple of 64.  Otherwise TF_ERR_UNSUPPORTED.
+ *  mode, nr, q_out, k_out, v_out   as tf_ulysses_scatter_qkv_into (every target
+ *               array is required: the projection produces Q, K and V).
+ * One kernel launch on `stream` (plus the resident table's first build).
+ */
+TF_API tf_status tf_ulysses_project_qkv_into(const void *const *x, int64_t x_row_stride, const void *w_qkv,
+                                             int64_t w_row_stride, int P, int B, int S_local, int hidden, int H,
+                                             int D, tf_dtype dtype, tf_mode mode, const tf_norm_rope *nr,
+                                             void *const *q_out, void *const *k_out, void *const *v_out,
+                                             void *stream);
+
+/*
  * tf_ulysses_gather_out -- head->sequence gather of the attention output (the
  * inverse all-to-all of the Ulysses section; TeleFuser PR #27 keeps it for the
  * output path).
@@ -331,11 +363,11 @@ typedef void (*tf_free_fn)(void *ptr, size_t bytes, void *stream, void *ctx);
 TF_API void tf_ulysses_set_allocator(tf_alloc_fn alloc, tf_free_fn release, void *ctx);
 
 /*
- * Device status word of the current device's staged (bulk-copy) kernel: 0 when
- * every in-kernel wait completed; otherwise bit 0 is set when a bounded wait for
- * a bulk load gave up -- the kernel then stopped early and its outputs are
- * incomplete.  Synchronises with the device.  clear != 0 resets the word after
- * reading it.
+ * Device status of the current device's kernels that wait in-kernel: 0 when
+ * every wait completed; bit 0 is set when a bounded wait of the staged
+ * (bulk-copy) kernel gave up, bit 1 when one of the projection kernel did --
+ * that kernel then stopped early and its outputs are incomplete.  Synchronises
+ * with the device.  clear != 0 resets the words after reading them.
  */
 TF_API tf_status tf_ulysses_device_status(int clear, unsigned *status);
 

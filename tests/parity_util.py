@@ -45,6 +45,22 @@ def fused_compare(got: torch.Tensor, want: torch.Tensor) -> dict:
     )
 
 
+def assert_projected_ok(got, want, min_identical=0.9):
+    """Outputs of the projection path on N(0, 1) data (the tensor cores sum in fp32
+    in their own order; the oracle rounds the exact sum once): flashinfer PR #6332
+    ("Assumptions / Tolerance") checks against a step-by-step reference with
+    atol = rtol = 1e-2, single-ulp differences classified apart.  Every element
+    within atol + rtol*|want| or one ulp, and most elements bit-identical."""
+    got, want = got.cpu(), want.cpu()
+    diff = (got.float() - want.float()).abs()
+    ulp = ulp_diff(got, want)
+    ok = (diff <= 1e-2 + 1e-2 * want.float().abs()) | (ulp <= 1)
+    assert bool(ok.all()), (float(diff.max()), int((~ok).sum()))
+    same = float((ulp == 0).float().mean()) if got.numel() else 1.0
+    assert same >= min_identical, same
+    return same
+
+
 def assert_fused_ok(got, want, max_flip_fraction=1e-5):
     st = fused_compare(got, want)
     assert st["ok"], st

@@ -75,10 +75,12 @@ def _declare(lib):
     lib.tf_ulysses_scatter_qkv_heads_into.argtypes = [PP, PP, PP, ctypes.POINTER(Strides), i32, i32, i32, i32, i32,
                                                       i32, i32, ctypes.POINTER(NormRope), i32, i32, PP, PP, PP, vp]
     lib.tf_ulysses_exchange_chunks.argtypes = [PP, PP, i32, ctypes.c_size_t, vp]
+    lib.tf_ulysses_project_qkv_into.argtypes = [PP, i64, vp, i64, i32, i32, i32, i32, i32, i32, i32, i32,
+                                                ctypes.POINTER(NormRope), PP, PP, PP, vp]
     lib.tf_ulysses_gather_out.argtypes = [ctypes.c_char_p, PP, ctypes.POINTER(Strides), i32, i32, i32, i32, i32,
                                           i32, PP, ctypes.POINTER(Strides), vp, ctypes.POINTER(Targets)]
     lib.tf_ulysses_rope_table.argtypes = [ctypes.c_float, i32, i32, vp, ctypes.POINTER(ctypes.c_void_p)]
-    for name in ("tf_ulysses_scatter_qkv_heads_into", "tf_ulysses_exchange_chunks",
+    for name in ("tf_ulysses_scatter_qkv_heads_into", "tf_ulysses_exchange_chunks", "tf_ulysses_project_qkv_into",
                  "tf_ulysses_scatter_qkv", "tf_ulysses_scatter_qkv_into", "tf_ulysses_scatter_qkv_noalloc",
                  "tf_ulysses_gather_out",
                  "tf_ulysses_rope_table", "tf_ulysses_cache_clear"):
@@ -100,7 +102,6 @@ def _declare(lib):
     lib.tf_ulysses_alloc_count.restype = ctypes.c_uint64
     lib.tf_ulysses_abi_version.argtypes = []
     lib.tf_ulysses_abi_version.restype = i32
-    del i64
     return lib
 
 
@@ -309,6 +310,34 @@ def scatter_qkv_heads_into(q, k, v, q_out, k_out=None, v_out=None, *, h0, h1, no
         _ptr_array(q), _ptr_array(k), _ptr_array(v), strides, P, B, Sl, H, D, _dtype_code(q[0].dtype), mode,
         ctypes.byref(nr) if nr is not None else None, int(h0), int(h1), _ptr_array(q_out), _ptr_array(k_out),
         _ptr_array(v_out), _stream_handle(stream)))
+    return q_out, k_out, v_out
+
+
+def project_qkv_into(x, w_qkv, H, q_out, k_out=None, v_out=None, *, norm_rope=False, q_weight=None, k_weight=None,
+                     eps=1e-6, theta=10000.0, cos_sin=None, rope="interleaved", layout="bshd", stream=None):
+    """QKV projection fused with the scatter: ``x`` is P shards ``[B, S_local,
+    hidden]`` (bf16, unit stride along hidden, rows of one shard equally spaced),
+    ``w_qkv`` the ``[3*H*D, hidden]`` weight (nn.Linear layout, D = 128).  Q, K, V
+    head rows land in the targets as ``scatter_qkv_into`` writes them, after the
+    RMSNorm + RoPE on Q/K when ``norm_rope``."""
+    P = len(x)
+    B, Sl, hidden = x[0].shape
+    for t in x:
+        if t.shape != x[0].shape or t.stride() != x[0].stride() or t.dtype != x[0].dtype:
+            raise ValueError("all x shards must share shape, strides and dtype")
+    if x[0].stride(2) != 1 or (B > 1 and x[0].stride(0) != Sl * x[0].stride(1)):
+        raise ValueError("x rows must be equally spaced with unit stride along hidden")
+    if w_qkv.stride(1) != 1:
+        raise ValueError("w_qkv needs unit stride along hidden")
+    D = w_qkv.shape[0] // (3 * H)
+    _check_targets((q_out, k_out, v_out), layout)
+    mode = _mode(norm_rope, rope, layout)
+    nr = _norm_rope(q_weight, k_weight, eps, theta, cos_sin) if norm_rope else None
+    _check(lib().tf_ulysses_project_qkv_into(
+        _ptr_array(x), x[0].stride(1) if Sl > 1 or B > 1 else hidden, ctypes.c_void_p(w_qkv.data_ptr()),
+        w_qkv.stride(0), P, B, Sl, hidden, H, D, _dtype_code(x[0].dtype), mode,
+        ctypes.byref(nr) if nr is not None else None, _ptr_array(q_out), _ptr_array(k_out), _ptr_array(v_out),
+        _stream_handle(stream)))
     return q_out, k_out, v_out
 
 

@@ -21,8 +21,9 @@ LIB = os.path.join(PKG, "libtf_ulysses.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               f"-I{INCLUDE}", f"-I{CSRC}"]
-SOURCES = ["block_kernels.cu", "relayout_kernels.cu", "staged_kernels.cu", "tf_ulysses.cpp", "noalloc.cu"]
-DEPS = SOURCES + ["relayout.h", "noalloc.h", "device_common.cuh", "tma_plan.h"]
+SOURCES = ["gemm_kernels.cu", "block_kernels.cu", "relayout_kernels.cu", "staged_kernels.cu", "tf_ulysses.cpp",
+           "noalloc.cu"]
+DEPS = SOURCES + ["relayout.h", "noalloc.h", "device_common.cuh", "tma_plan.h", "gemm.h"]
 
 
 def nvcc() -> str:

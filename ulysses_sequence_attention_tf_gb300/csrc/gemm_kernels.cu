@@ -1,0 +1,474 @@
+// gemm_kernels.cu -- the QKV projection in front of the Ulysses exchange on the
+// 5th-generation tensor cores (sm_103a), with the Q/K RMSNorm + RoPE and the
+// scatter into the final-layout targets in the epilogue.
+//
+// What is computed (flashinfer PR #6332 commit message, "Description": the BF16
+// QKV projection, per-head RMSNorm of Q and K, interleaved RoPE from a per-token
+// cos/sin table and the head exchange in one call, the exchange stored straight
+// from the GEMM epilogue; "Assumptions / Operator math": projection -> QK-norm ->
+// RoPE, BF16 operands and outputs).  For shard r, token row m = b*Sl + t,
+// feature n:
+//     Y[m, n] = round_bf16( sum_k X_r[m, k] * W[n, k] )     (fp32 accumulation)
+// Y's feature blocks [0, HD), [HD, 2HD), [2HD, 3HD) are Q, K, V; head h of a block
+// lands in head group g = h / Hl at target row r*Sl + t, head h % Hl; Q and K rows
+// then get the RMSNorm + RoPE of tf_ulysses.h at global position p = r*Sl + t.
+//
+// Design (one CTA per 128 x 256 output tile, 192 threads):
+//  * warp 0, one lane: TMA producer.  Each stage holds a 128 x 64 tile of X and a
+//    256 x 64 tile of W (bf16, 128-byte swizzle), loaded with
+//    cp.async.bulk.tensor onto the stage's mbarrier (transaction bytes).
+//  * warp 1: allocates 256 TMEM columns (the 128 x 256 fp32 accumulator), and one
+//    lane issues tcgen05.mma (kind::f16, M = 128, N = 256, K = 16, four per
+//    stage) from shared-memory descriptors, committing each stage back to the
+//    producer and the finished accumulator to the epilogue.
+//  * warps 2-5: the epilogue.  Warp w reads TMEM lanes 32*(w%4).. with
+//    tcgen05.ld, so each thread holds one token row: per head, 128 fp32
+//    accumulators are rounded to bf16 (the projection's output), and for Q/K
+//    normalised (exact sum of squares, in-thread), scaled and rotated, then
+//    stored as one 256-byte row of the head-group target.
+//  * Tiles are rasterised in passes over n_group column tiles, so the weight
+//    columns of a pass stay in L2 while every row tile streams past.
+//  * Every mbarrier wait is bounded; a wait that gives up records a status bit,
+//    raises a shared abort flag, and the CTA drains its copies and MMAs (bounded)
+//    and frees its TMEM before returning.
+#include <cudaTypedefs.h>
+
+#include "device_common.cuh"
+#include "gemm.h"
+
+namespace tfu {
+
+__device__ unsigned g_gemm_status;
+
+namespace {
+
+using namespace dev;
+
+constexpr int kStagesG = 4;
+constexpr uint32_t kABytes = kGemmBM * kGemmBK * 2;  // 16 KiB
+constexpr uint32_t kBBytes = kGemmBN * kGemmBK * 2;  // 32 KiB
+constexpr uint32_t kStageBytesG = kABytes + kBBytes;
+constexpr int kThreadsG = 192;
+constexpr uint32_t kTmemCols = 256;
+constexpr size_t kSmemG = size_t(kStagesG) * kStageBytesG + 256 + 1024;  // stages, barriers, alignment slack
+constexpr long long kWaitCyclesG = 4000000000LL;                           // ~2 s at 2 GHz
+constexpr unsigned kStatusWait = 1u;
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A and
+// B bf16 (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits
+// 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kGemmBN >> 3) << 17) |
+                            (uint32_t(kGemmBM >> 4) << 24);
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarriers
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Wait for the phase of `bar` with parity `parity`; false if the abort flag is
+// raised or the budget runs out (then records the status and raises the flag).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > kWaitCyclesG) {
+                atomicOr(&g_gemm_status, kStatusWait);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// The same without the abort flag (draining after an abort): bounded only.
+__device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kWaitCyclesG) return;
+    }
+}
+
+// ---------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t smem_result, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_result), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one M=128 x N=256 x K=16 step.
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile whose rows are 128
+// bytes (64 bf16) with the 128-byte swizzle, 8-row groups 1024 bytes apart:
+// start address >> 4 (bits 0-13), leading byte offset (unused by this layout, 1)
+// at bits 16-29, stride byte offset 1024 >> 4 at bits 32-45, descriptor version
+// 1 at bits 46-47, base offset 0 (tiles are 1024-byte aligned), swizzle mode
+// 2 = 128-byte at bits 61-63.  A K step of 16 elements advances the start by 32 bytes.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
+    return uint64_t((smem_addr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
+           (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// 32 consecutive fp32 accumulator columns of this thread's TMEM lane (warp-collective:
+// the warp is reconverged first).
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    __syncwarp();
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------- epilogue
+// 16 packed bf16 pairs of 32 accumulator columns: the projection's output rounding.
+__device__ __forceinline__ void round_chunk(const uint32_t (&r)[32], uint32_t (&z)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) z[i] = pack2<Fused::kBF16>(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+}
+
+// y = round(x * inv), z = round(y * w) for 16 pairs; wp: the chunk's weight pairs.
+__device__ __forceinline__ void scale_chunk(uint32_t (&z)[16], float inv, const uint32_t* wp) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float a, b;
+        unpack2<Fused::kBF16>(z[i], a, b);
+        z[i] = mul2<Fused::kBF16>(pack2<Fused::kBF16>(__fmul_rn(a, inv), __fmul_rn(b, inv)), __ldg(wp + i));
+    }
+}
+
+__device__ __forceinline__ void store_chunk(uint8_t* dst, const uint32_t (&z)[16]) {
+    Vec<32> v0, v1;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        v0.w[k] = z[k];
+        v1.w[k] = z[8 + k];
+    }
+    st_stream<32>(dst, v0);
+    st_stream<32>(dst + 32, v1);
+}
+
+// One head of this thread's token row, TMEM columns [taddr, taddr + 128): the
+// projection rounded to bf16, then for a Q/K head the RMSNorm (exact in-thread
+// sum of squares, first pass over TMEM), the bf16 weight scale and RoPE
+// (interleaved pairs (2i, 2i+1), or half-split pairs (i, i + 64)) in a second
+// pass, 32 columns (64 output bytes) at a time.  tcgen05.ld is warp-collective:
+// every lane loads, only valid rows store.
+template <bool kFusedT, bool kNeox>
+__device__ __forceinline__ void epilogue_head(uint32_t taddr, bool valid, bool norm, const uint32_t* wpairs,
+                                              const float* tab, float eps, uint8_t* dst_row) {
+    if (!(kFusedT && norm)) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            uint32_t r[32], z[16];
+            tc_ld32(taddr + uint32_t(c * 32), r);
+            tc_wait_ld();
+            round_chunk(r, z);
+            if (valid) store_chunk(dst_row + c * 64, z);
+        }
+        return;
+    }
+    float hi = 0.f, lo = 0.f;  // sum of squares of the rounded row: hi + lo exact
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+        uint32_t r[32], z[16];
+        tc_ld32(taddr + uint32_t(c * 32), r);
+        tc_wait_ld();
+        round_chunk(r, z);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float a, b, s, e;
+            unpack2<Fused::kBF16>(z[i], a, b);
+            two_sum(hi, __fmul_rn(a, a), s, e);  // squares of bf16 values are exact in fp32
+            lo = __fadd_rn(lo, e);
+            hi = s;
+            two_sum(hi, __fmul_rn(b, b), s, e);
+            lo = __fadd_rn(lo, e);
+            hi = s;
+        }
+    }
+    const float ss = __fadd_rn(hi, lo);
+    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(ss, 1.0f / kGemmHeadDim), eps)));
+    if constexpr (!kNeox) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {  // pairs 16c .. 16c + 15, table entries likewise
+            uint32_t r[32], z[16];
+            tc_ld32(taddr + uint32_t(c * 32), r);
+            tc_wait_ld();
+            round_chunk(r, z);  // rows past the end compute on zeros and store nothing
+            scale_chunk(z, inv, wpairs + c * 16);
+            const float4* t4 = reinterpret_cast<const float4*>(tab) + c * 8;  // two pairs per float4
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+                const float4 cs = __ldg(t4 + i / 2);
+                float a, b;
+                unpack2<Fused::kBF16>(z[i], a, b);
+                z[i] = pack2<Fused::kBF16>(__fsub_rn(__fmul_rn(a, cs.x), __fmul_rn(b, cs.y)),
+                                           __fadd_rn(__fmul_rn(a, cs.y), __fmul_rn(b, cs.x)));
+                unpack2<Fused::kBF16>(z[i + 1], a, b);
+                z[i + 1] = pack2<Fused::kBF16>(__fsub_rn(__fmul_rn(a, cs.z), __fmul_rn(b, cs.w)),
+                                               __fadd_rn(__fmul_rn(a, cs.w), __fmul_rn(b, cs.z)));
+            }
+            if (valid) store_chunk(dst_row + c * 64, z);
+        }
+    } else {
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {  // columns 32c.. pair with 32c + 64..; entries 32c .. 32c + 31
+            uint32_t r[32], zl[16], zh[16];
+            tc_ld32(taddr + uint32_t(c * 32), r);
+            tc_wait_ld();
+            round_chunk(r, zl);
+            tc_ld32(taddr + uint32_t(c * 32 + 64), r);
+            tc_wait_ld();
+            round_chunk(r, zh);
+            scale_chunk(zl, inv, wpairs + c * 16);
+            scale_chunk(zh, inv, wpairs + c * 16 + 32);
+            const float4* t4 = reinterpret_cast<const float4*>(tab) + c * 16;  // entries 2i, 2i+1 per float4
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float4 cs = __ldg(t4 + i);
+                float a0, a1, b0, b1;
+                unpack2<Fused::kBF16>(zl[i], a0, a1);
+                unpack2<Fused::kBF16>(zh[i], b0, b1);
+                zl[i] = pack2<Fused::kBF16>(__fsub_rn(__fmul_rn(a0, cs.x), __fmul_rn(b0, cs.y)),
+                                            __fsub_rn(__fmul_rn(a1, cs.z), __fmul_rn(b1, cs.w)));
+                zh[i] = pack2<Fused::kBF16>(__fadd_rn(__fmul_rn(a0, cs.y), __fmul_rn(b0, cs.x)),
+                                            __fadd_rn(__fmul_rn(a1, cs.w), __fmul_rn(b1, cs.z)));
+            }
+            if (valid) {
+                store_chunk(dst_row + c * 64, zl);
+                store_chunk(dst_row + c * 64 + 128, zh);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- the kernel
+template <bool kFusedT, bool kNeox>
+__global__ void __launch_bounds__(kThreadsG, 1) qkv_gemm_kernel(const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kStagesG) * kStageBytesG);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStagesG), acc_full = smem_u32(bars + 2 * kStagesG);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStagesG + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    // tile: passes of n_group column tiles; inside a pass, row tiles (over all
+    // shards) outer, column tiles inner
+    const uint32_t MT = p.P * p.m_tiles;
+    const uint32_t G = p.n_group;
+    const uint32_t pass = blockIdx.x / (G * MT);
+    const uint32_t within = blockIdx.x - pass * G * MT;
+    const uint32_t gw = min(G, p.n_tiles - pass * G);
+    const uint32_t mt = within / gw;
+    const uint32_t n_tile = pass * G + (within - mt * gw);
+    const uint32_t r = mt / p.m_tiles;
+    const uint32_t m_tile = mt - r * p.m_tiles;
+    const uint32_t KB = p.K / kGemmBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStagesG; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        mbar_init(acc_full, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer
+        const CUtensorMap* mx = &p.tmap_x[r];
+        const CUtensorMap* mw = &p.tmap_w;
+        uint32_t issued = 0;
+        for (uint32_t kb = 0; kb < KB; ++kb) {
+            const uint32_t s = kb % kStagesG, use = kb / kStagesG;
+            if (use > 0 && !wait_phase(empty0 + 8 * s, (use - 1) & 1u, abort_flag)) break;
+            const uint32_t a = smem_u32(smem + size_t(s) * kStageBytesG);
+            mbar_expect_tx(full0 + 8 * s, kStageBytesG);
+            tma_load_2d(a, mx, int(kb * kGemmBK), int(m_tile * kGemmBM), full0 + 8 * s);
+            tma_load_2d(a + kABytes, mw, int(kb * kGemmBK), int(n_tile * kGemmBN), full0 + 8 * s);
+            issued = kb + 1;
+        }
+        // drain: the last load issued into each stage has landed before the CTA exits
+        for (uint32_t kb = issued > uint32_t(kStagesG) ? issued - kStagesG : 0; kb < issued; ++kb)
+            drain_phase(full0 + 8 * (kb % kStagesG), (kb / kStagesG) & 1u);
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer
+        for (uint32_t kb = 0; kb < KB; ++kb) {
+            const uint32_t s = kb % kStagesG, use = kb / kStagesG;
+            if (!wait_phase(full0 + 8 * s, use & 1u, abort_flag)) break;
+            tc_fence_after();
+            const uint32_t a = smem_u32(smem + size_t(s) * kStageBytesG);
+#pragma unroll
+            for (uint32_t kk = 0; kk < kGemmBK / 16; ++kk)
+                tc_mma(tmem, sw128_desc(a + kk * 32), sw128_desc(a + kABytes + kk * 32), (kb | kk) != 0);
+            tc_commit(empty0 + 8 * s);  // the stage is free once these MMAs have read it
+        }
+        tc_commit(acc_full);  // every MMA issued above has completed (also after an abort)
+    } else if (warp >= 2) {
+        // ---------------- epilogue
+        const bool ok = wait_phase(acc_full, 0, abort_flag);
+        tc_fence_after();
+        if (__all_sync(0xffffffffu, ok && !*abort_flag)) {  // warp-uniform: the TMEM loads are collective
+            const uint32_t quarter = warp & 3u;
+            const uint32_t m = m_tile * kGemmBM + quarter * 32 + lane;
+            const bool valid = m < p.rows;
+            const uint32_t b = valid ? m / p.Sl : 0, t = valid ? m - b * p.Sl : 0;
+            const uint32_t pos = r * p.Sl + t;
+            const uint32_t HD = p.H * kGemmHeadDim;
+#pragma unroll 1
+            for (uint32_t j = 0; j < kGemmBN / kGemmHeadDim; ++j) {
+                const uint32_t f = n_tile * kGemmBN + j * kGemmHeadDim;
+                const uint32_t sec = f / HD;
+                const uint32_t h = (f - sec * HD) / kGemmHeadDim;
+                const uint32_t g = h / p.Hl, hh = h - g * p.Hl;
+                uint8_t* dst_row = p.dst[sec][g] + int64_t(b) * p.d_b + int64_t(pos) * p.d_t + int64_t(hh) * p.d_h;
+                const bool norm = kFusedT && sec < 2;
+                const uint32_t* wp = norm ? static_cast<const uint32_t*>(p.weight[sec]) : nullptr;
+                const float* tab = norm ? p.table + size_t(pos) * kGemmHeadDim : nullptr;
+                epilogue_head<kFusedT, kNeox>(tmem + ((quarter * 32u) << 16) + j * kGemmHeadDim, valid, norm, wp, tab,
+                                              p.eps, dst_row);
+            }
+        }
+    }
+    // teardown: all MMAs have completed (the epilogue saw acc_full, or warp 1 waits
+    // for it below) and every TMEM read has finished before the columns are freed
+    if (warp == 1 && lane == 0) drain_phase(acc_full, 0);
+    __syncwarp();  // the single-lane roles rejoin their warps before the CTA barrier
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+template <bool kFusedT, bool kNeox>
+cudaError_t launch_variant(const GemmParams& p, cudaStream_t stream) {
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        e = cudaFuncSetAttribute(qkv_gemm_kernel<kFusedT, kNeox>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(kSmemG));
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    const uint64_t tiles = uint64_t(p.P) * p.m_tiles * p.n_tiles;
+    qkv_gemm_kernel<kFusedT, kNeox><<<unsigned(tiles), kThreadsG, kSmemG, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
+                          uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t gdim[2] = {cols, rows};
+    const cuuint64_t gstride[1] = {row_bytes};
+    const cuuint32_t box[2] = {uint32_t(kGemmBK), box_rows};
+    const cuuint32_t estride[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_qkv_gemm(const GemmParams& p, bool fused, bool neox, cudaStream_t stream) {
+    if (uint64_t(p.P) * p.m_tiles * p.n_tiles == 0) return cudaSuccess;
+    if (!fused) return launch_variant<false, false>(p, stream);
+    return neox ? launch_variant<true, true>(p, stream) : launch_variant<true, false>(p, stream);
+}
+
+cudaError_t read_gemm_status(unsigned* out, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_gemm_status, sizeof(unsigned));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_gemm_status, &zero, sizeof(unsigned));
+}
+
+}  // namespace tfu

@@ -21,6 +21,7 @@
 
 #include <cuda_runtime.h>
 
+#include "gemm.h"
 #include "noalloc.h"
 #include "relayout.h"
 #include "tf_ulysses.h"
@@ -798,6 +799,122 @@ TF_API tf_status tf_ulysses_exchange_chunks(const void* const* src, void* const*
                           static_cast<cudaStream_t>(stream));
 }
 
+// Fused QKV projection: the tcgen05 GEMM whose epilogue applies the Q/K
+// RMSNorm + RoPE and stores every head row into its head-group target.
+TF_API tf_status tf_ulysses_project_qkv_into(const void* const* x, int64_t x_row_stride, const void* w_qkv,
+                                             int64_t w_row_stride, int P, int B, int S_local, int hidden, int H,
+                                             int D, tf_dtype dtype, tf_mode mode, const tf_norm_rope* nr,
+                                             void* const* q_out, void* const* k_out, void* const* v_out,
+                                             void* stream) {
+    Shape sh;
+    tf_status s = check_shape(P, B, S_local, H, D, dtype, &sh);
+    if (s != TF_OK) return s;
+    if (dtype != TF_BF16) return fail(TF_ERR_UNSUPPORTED, "the projection is built for bf16 (dtype %d)", int(dtype));
+    if (D != tfu::kGemmHeadDim) return fail(TF_ERR_UNSUPPORTED, "the projection is built for D = 128, not %d", D);
+    if (H % 2 != 0) return fail(TF_ERR_UNSUPPORTED, "the projection needs an even H (two heads per tile), not %d", H);
+    if (hidden <= 0 || hidden % tfu::kGemmBK != 0)
+        return fail(TF_ERR_UNSUPPORTED, "hidden=%d must be a positive multiple of %d", hidden, tfu::kGemmBK);
+    const int base = int(mode) & kModeBase, flags = int(mode) & ~kModeBase;
+    if (base != TF_MODE_SCATTER && base != TF_MODE_SCATTER_NORM_ROPE)
+        return fail(TF_ERR_INVALID, "mode %d is not a scatter mode", int(mode));
+    if (flags & ~kModeFlags) return fail(TF_ERR_INVALID, "unknown mode flags 0x%x", unsigned(flags & ~kModeFlags));
+    const bool fused = base == TF_MODE_SCATTER_NORM_ROPE, neox = (flags & TF_MODE_FLAG_ROPE_NEOX) != 0;
+    const bool fused_layout = (flags & TF_MODE_FLAG_FUSED_LAYOUT) != 0;
+    if (neox && !fused) return fail(TF_ERR_INVALID, "TF_MODE_FLAG_ROPE_NEOX needs TF_MODE_SCATTER_NORM_ROPE");
+    const bool empty = B == 0 || S_local == 0;
+    if (!x || !w_qkv) return fail(TF_ERR_INVALID, "x or w_qkv is NULL");
+    if (!empty && (s = check_ptrs("x", x, P)) != TF_OK) return s;
+    if (!aligned16(w_qkv)) return fail(TF_ERR_ALIGNMENT, "w_qkv is not 16-byte aligned");
+    if (x_row_stride < hidden || (x_row_stride * 2) % 16 != 0)
+        return fail(TF_ERR_ALIGNMENT, "x_row_stride=%lld must be >= hidden and a multiple of 8 elements",
+                    (long long)x_row_stride);
+    if (w_row_stride < hidden || (w_row_stride * 2) % 16 != 0)
+        return fail(TF_ERR_ALIGNMENT, "w_row_stride=%lld must be >= hidden and a multiple of 8 elements",
+                    (long long)w_row_stride);
+    if (fused) {
+        if (!nr) return fail(TF_ERR_INVALID, "the fused mode needs norm/rope parameters");
+        if (!nr->q_weight || !aligned16(nr->q_weight) || !nr->k_weight || !aligned16(nr->k_weight))
+            return fail(TF_ERR_ALIGNMENT, "q_weight/k_weight NULL or misaligned");
+        if (!std::isfinite(nr->eps) || nr->eps < 0) return fail(TF_ERR_INVALID, "eps must be finite and >= 0");
+        if (nr->cos_sin) {
+            if (!aligned16(nr->cos_sin)) return fail(TF_ERR_ALIGNMENT, "cos_sin is not 16-byte aligned");
+        } else if (!std::isfinite(nr->theta) || nr->theta <= 0) {
+            return fail(TF_ERR_INVALID, "theta must be finite and > 0");
+        }
+    }
+    // targets: as tf_ulysses_scatter_qkv_into (all three tensors are produced)
+    const int64_t rowb = int64_t(D) * 2, pitch = fused_layout ? 3 * rowb : rowb;
+    void* const* outs[3] = {q_out, k_out, v_out};
+    const char* names[3] = {"q_out", "k_out", "v_out"};
+    tfu::GemmParams p{};
+    if (fused_layout) {
+        if (!q_out) return fail(TF_ERR_INVALID, "q_out (the payloads) is NULL");
+        if (k_out || v_out) return fail(TF_ERR_INVALID, "the fused layout takes its payloads in q_out only");
+        if (!empty && (s = check_ptrs("q_out", q_out, P)) != TF_OK) return s;
+        for (int xi = 0; xi < 3; ++xi)
+            for (int g = 0; g < P; ++g)
+                p.dst[xi][g] = static_cast<uint8_t*>(q_out[g]) + (q_out[g] ? int64_t(xi) * rowb : 0);
+    } else {
+        for (int xi = 0; xi < 3; ++xi) {
+            if (!outs[xi]) return fail(TF_ERR_INVALID, "%s is NULL (the projection writes Q, K and V)", names[xi]);
+            if (!empty && (s = check_ptrs(names[xi], outs[xi], P)) != TF_OK) return s;
+            for (int g = 0; g < P; ++g) p.dst[xi][g] = static_cast<uint8_t*>(outs[xi][g]);
+        }
+    }
+    const uint64_t rows = uint64_t(B) * uint64_t(S_local);
+    const uint64_t m_tiles = (rows + tfu::kGemmBM - 1) / tfu::kGemmBM;
+    const uint64_t n_tiles = uint64_t(3) * H * D / tfu::kGemmBN;
+    if (rows >= (uint64_t(1) << 31) || uint64_t(P) * m_tiles * n_tiles >= (uint64_t(1) << 31))
+        return fail(TF_ERR_UNSUPPORTED, "problem exceeds 2^31 tiles or rows");
+    int device = 0;
+    if ((s = current_device(&device)) != TF_OK) return s;
+    if (empty) return TF_OK;
+    for (int r = 0; r < P; ++r)
+        if (!tfu::encode_tensor_map_2d(&p.tmap_x[r], x[r], uint64_t(hidden), rows, uint64_t(x_row_stride) * 2,
+                                       tfu::kGemmBM))
+            return fail(TF_ERR_UNSUPPORTED, "the driver refused the tensor map of x[%d]", r);
+    if (!tfu::encode_tensor_map_2d(&p.tmap_w, w_qkv, uint64_t(hidden), n_tiles * tfu::kGemmBN,
+                                   uint64_t(w_row_stride) * 2, tfu::kGemmBN))
+        return fail(TF_ERR_UNSUPPORTED, "the driver refused the tensor map of w_qkv");
+    p.d_h = pitch;
+    p.d_t = pitch * sh.Hl;
+    p.d_b = pitch * sh.Hl * int64_t(P) * S_local;
+    p.eps = fused ? nr->eps : 0.f;
+    p.weight[0] = fused ? nr->q_weight : nullptr;
+    p.weight[1] = fused ? nr->k_weight : nullptr;
+    p.P = uint32_t(P);
+    p.B = uint32_t(B);
+    p.Sl = uint32_t(S_local);
+    p.H = uint32_t(H);
+    p.Hl = uint32_t(sh.Hl);
+    p.K = uint32_t(hidden);
+    p.rows = uint32_t(rows);
+    p.m_tiles = uint32_t(m_tiles);
+    p.n_tiles = uint32_t(n_tiles);
+    // a pass over all row tiles reads n_group column tiles of the weight (~48 MB: L2-resident)
+    const uint64_t wbytes_tile = uint64_t(tfu::kGemmBN) * uint64_t(hidden) * 2;
+    uint64_t G = (uint64_t(48) << 20) / wbytes_tile;
+    p.n_group = uint32_t(G < 1 ? 1 : (G > n_tiles ? n_tiles : G));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    bool cap = false;
+    if ((s = capture_state(st, &cap)) != TF_OK) return s;
+    std::lock_guard<std::mutex> lock(g_mu);
+    Table* used = nullptr;
+    if (fused) {
+        if (nr->cos_sin) {
+            p.table = nr->cos_sin;
+        } else {
+            if ((s = get_table(nr->theta, P * S_local, D, device, st, cap, &used)) != TF_OK) return s;
+            p.table = used->ptr;
+        }
+    }
+    cudaError_t e = tfu::launch_qkv_gemm(p, fused, neox, st);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the projection kernel");
+    g_launches.fetch_add(1);
+    if (used) record_event(used->last_use, st, cap);
+    return TF_OK;
+}
+
 TF_API tf_status tf_ulysses_gather_out(const char* tag, const void* const* attn, const tf_strides* attn_strides,
                                        int P, int B, int S_local, int H, int D, tf_dtype dtype, void* const* dst,
                                        const tf_strides* dst_strides, void* stream, tf_targets* out) {
@@ -931,8 +1048,11 @@ TF_API void tf_ulysses_set_allocator(tf_alloc_fn alloc, tf_free_fn release, void
 
 TF_API tf_status tf_ulysses_device_status(int clear, unsigned* status) {
     if (!status) return fail(TF_ERR_INVALID, "status is NULL");
-    cudaError_t e = tfu::read_staged_status(status, clear != 0);
-    if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+    unsigned staged = 0, gemm = 0;
+    cudaError_t e = tfu::read_staged_status(&staged, clear != 0);
+    if (e == cudaSuccess) e = tfu::read_gemm_status(&gemm, clear != 0);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device status words");
+    *status = (staged ? 1u : 0u) | (gemm ? 2u : 0u);
     return TF_OK;
 }
 

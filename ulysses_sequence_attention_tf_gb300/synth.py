@@ -101,6 +101,32 @@ def qkv_shards(P, B, S_local, H, D, dtype, *, seed=0, device="cpu", layout="cont
     return dict(q=q, k=k, v=v, backing=backing)
 
 
+def projection_inputs(P, B, S_local, hidden, H, D, dtype, *, seed=0, device="cpu", x_pad=0, w_pad=0,
+                      dist="normal"):
+    """Hidden-state shards ``x[r]`` [B, S_local, hidden] and the QKV weight ``w``
+    [3*H*D, hidden] in the I/O type.  dist="normal": x ~ N(0, 1), w ~ N(0, 1/hidden)
+    (projected values ~N(0, 1)).  dist="dyadic": x = i/8 and w = j/16 for uniform
+    integers |i| <= 8, |j| <= 16, so every product is a multiple of 2^-7 of
+    magnitude <= 1 and every partial sum of up to 2^16 of them is exact in fp32.
+    ``x_pad`` / ``w_pad`` extra elements per row make the rows of x / w strided
+    views (row stride hidden + pad)."""
+    gen = make_generator(seed + 104729, device)
+
+    def draw(shape, scale):
+        if dist == "dyadic":
+            return torch.randint(-scale, scale + 1, shape, generator=gen, device=device).to(torch.float32) / scale
+        return torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+
+    xs = []
+    for _ in range(P):
+        xs.append(draw((B, S_local, hidden + x_pad), 8).to(dtype)[..., :hidden])
+    wb = draw((3 * H * D, hidden + w_pad), 16)
+    if dist != "dyadic":
+        wb = wb * hidden ** -0.5
+    w = wb.to(dtype)[:, :hidden]
+    return xs, w
+
+
 def norm_weights(D, dtype, *, seed=0, device="cpu"):
     """(w_q, w_k), each ``[D]`` ~ N(1, 0.1) in the I/O type."""
     gen = make_generator(seed + 7919, device)
