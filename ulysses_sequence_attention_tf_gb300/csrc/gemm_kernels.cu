@@ -13,14 +13,15 @@
 // lands in head group g = h / Hl at target row r*Sl + t, head h % Hl; Q and K rows
 // then get the RMSNorm + RoPE of tf_ulysses.h at global position p = r*Sl + t.
 //
-// Design (one CTA per 128 x 256 output tile, 192 threads):
+// Design (persistent: one CTA of 192 threads per SM walks 128 x 256 output tiles):
 //  * warp 0, one lane: TMA producer.  Each stage holds a 128 x 64 tile of X and a
 //    256 x 64 tile of W (bf16, 128-byte swizzle), loaded with
 //    cp.async.bulk.tensor onto the stage's mbarrier (transaction bytes).
-//  * warp 1: allocates 256 TMEM columns (the 128 x 256 fp32 accumulator), and one
-//    lane issues tcgen05.mma (kind::f16, M = 128, N = 256, K = 16, four per
-//    stage) from shared-memory descriptors, committing each stage back to the
-//    producer and the finished accumulator to the epilogue.
+//  * warp 1: allocates 512 TMEM columns (two 128 x 256 fp32 accumulators, so the
+//    epilogue of one tile overlaps the MMAs of the next), and one lane issues
+//    tcgen05.mma (kind::f16, M = 128, N = 256, K = 16, four per stage) from
+//    shared-memory descriptors, committing each stage back to the producer and
+//    each finished accumulator to the epilogue, which releases it when read.
 //  * warps 2-5: the epilogue.  Warp w reads TMEM lanes 32*(w%4).. with
 //    tcgen05.ld, so each thread holds one token row: per head, 128 fp32
 //    accumulators are rounded to bf16 (the projection's output), and for Q/K
@@ -301,27 +302,47 @@ __device__ __forceinline__ void epilogue_head(uint32_t taddr, bool valid, bool n
 }
 
 // ---------------------------------------------------------------- the kernel
+struct Tile {
+    uint32_t r, m_tile, n_tile;
+};
+
+// Tiles in passes of n_group column tiles; inside a pass, row tiles (over all
+// shards) outer and column tiles inner, so the CTAs running together share the
+// weight columns of the pass and the rows of a few row tiles.
+__device__ __forceinline__ Tile decode_tile(const GemmParams& p, uint32_t t) {
+    const uint32_t MT = p.P * p.m_tiles;
+    const uint32_t G = p.n_group;
+    const uint32_t pass = t / (G * MT);
+    const uint32_t within = t - pass * G * MT;
+    const uint32_t gw = min(G, p.n_tiles - pass * G);
+    const uint32_t mt = within / gw;
+    Tile tl;
+    tl.n_tile = pass * G + (within - mt * gw);
+    tl.r = mt / p.m_tiles;
+    tl.m_tile = mt - tl.r * p.m_tiles;
+    return tl;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+constexpr uint32_t kAccBufs = 2;  // TMEM accumulators: the epilogue of tile i overlaps the MMAs of tile i+1
+
+// Persistent: CTA c takes tiles c, c + gridDim.x, ...; the shared-memory stage
+// ring and the two TMEM accumulators carry on from tile to tile.
 template <bool kFusedT, bool kNeox>
 __global__ void __launch_bounds__(kThreadsG, 1) qkv_gemm_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kStagesG) * kStageBytesG);
-    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStagesG), acc_full = smem_u32(bars + 2 * kStagesG);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStagesG + 1);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStagesG);
+    const uint32_t acc_full0 = smem_u32(bars + 2 * kStagesG), acc_empty0 = smem_u32(bars + 2 * kStagesG + kAccBufs);
+    const uint32_t mma_done = smem_u32(bars + 2 * kStagesG + 2 * kAccBufs);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStagesG + 2 * kAccBufs + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-
-    // tile: passes of n_group column tiles; inside a pass, row tiles (over all
-    // shards) outer, column tiles inner
-    const uint32_t MT = p.P * p.m_tiles;
-    const uint32_t G = p.n_group;
-    const uint32_t pass = blockIdx.x / (G * MT);
-    const uint32_t within = blockIdx.x - pass * G * MT;
-    const uint32_t gw = min(G, p.n_tiles - pass * G);
-    const uint32_t mt = within / gw;
-    const uint32_t n_tile = pass * G + (within - mt * gw);
-    const uint32_t r = mt / p.m_tiles;
-    const uint32_t m_tile = mt - r * p.m_tiles;
+    const uint32_t tiles = p.P * p.m_tiles * p.n_tiles;
     const uint32_t KB = p.K / kGemmBK;
 
     if (threadIdx.x == 0) {
@@ -329,12 +350,16 @@ __global__ void __launch_bounds__(kThreadsG, 1) qkv_gemm_kernel(const __grid_con
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
         }
-        mbar_init(acc_full, 1);
+        for (uint32_t a = 0; a < kAccBufs; ++a) {
+            mbar_init(acc_full0 + 8 * a, 1);
+            mbar_init(acc_empty0 + 8 * a, 4);  // one arrival per epilogue warp
+        }
+        mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols * kAccBufs);
         tmem_relinquish();
     }
     __syncwarp();
@@ -344,49 +369,71 @@ __global__ void __launch_bounds__(kThreadsG, 1) qkv_gemm_kernel(const __grid_con
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0 && lane == 0) {
-        // ---------------- TMA producer
-        const CUtensorMap* mx = &p.tmap_x[r];
-        const CUtensorMap* mw = &p.tmap_w;
-        uint32_t issued = 0;
-        for (uint32_t kb = 0; kb < KB; ++kb) {
-            const uint32_t s = kb % kStagesG, use = kb / kStagesG;
-            if (use > 0 && !wait_phase(empty0 + 8 * s, (use - 1) & 1u, abort_flag)) break;
-            const uint32_t a = smem_u32(smem + size_t(s) * kStageBytesG);
-            mbar_expect_tx(full0 + 8 * s, kStageBytesG);
-            tma_load_2d(a, mx, int(kb * kGemmBK), int(m_tile * kGemmBM), full0 + 8 * s);
-            tma_load_2d(a + kABytes, mw, int(kb * kGemmBK), int(n_tile * kGemmBN), full0 + 8 * s);
-            issued = kb + 1;
+        // ---------------- TMA producer: one continuous stream of k-blocks
+        uint32_t q = 0;  // k-blocks issued by this CTA
+        bool ok = true;
+        for (uint32_t t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+            const Tile tl = decode_tile(p, t);
+            const CUtensorMap* mx = &p.tmap_x[tl.r];
+            for (uint32_t kb = 0; kb < KB; ++kb, ++q) {
+                const uint32_t s = q % kStagesG, use = q / kStagesG;
+                if (use > 0 && !wait_phase(empty0 + 8 * s, (use - 1) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t a = smem_u32(smem + size_t(s) * kStageBytesG);
+                mbar_expect_tx(full0 + 8 * s, kStageBytesG);
+                tma_load_2d(a, mx, int(kb * kGemmBK), int(tl.m_tile * kGemmBM), full0 + 8 * s);
+                tma_load_2d(a + kABytes, &p.tmap_w, int(kb * kGemmBK), int(tl.n_tile * kGemmBN), full0 + 8 * s);
+            }
         }
-        // drain: the last load issued into each stage has landed before the CTA exits
-        for (uint32_t kb = issued > uint32_t(kStagesG) ? issued - kStagesG : 0; kb < issued; ++kb)
-            drain_phase(full0 + 8 * (kb % kStagesG), (kb / kStagesG) & 1u);
+        // the last load issued into each stage has landed before the CTA exits
+        for (uint32_t k = q > uint32_t(kStagesG) ? q - kStagesG : 0; k < q; ++k)
+            drain_phase(full0 + 8 * (k % kStagesG), (k / kStagesG) & 1u);
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer
-        for (uint32_t kb = 0; kb < KB; ++kb) {
-            const uint32_t s = kb % kStagesG, use = kb / kStagesG;
-            if (!wait_phase(full0 + 8 * s, use & 1u, abort_flag)) break;
+        uint32_t q = 0, i = 0;
+        bool ok = true;
+        for (uint32_t t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++i) {
+            const uint32_t a = i % kAccBufs, u = i / kAccBufs;
+            if (u > 0 && !wait_phase(acc_empty0 + 8 * a, (u - 1) & 1u, abort_flag)) break;  // epilogue drained it
             tc_fence_after();
-            const uint32_t a = smem_u32(smem + size_t(s) * kStageBytesG);
+            const uint32_t d = tmem + a * kTmemCols;
+            for (uint32_t kb = 0; kb < KB; ++kb, ++q) {
+                const uint32_t s = q % kStagesG, use = q / kStagesG;
+                if (!wait_phase(full0 + 8 * s, use & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem + size_t(s) * kStageBytesG);
 #pragma unroll
-            for (uint32_t kk = 0; kk < kGemmBK / 16; ++kk)
-                tc_mma(tmem, sw128_desc(a + kk * 32), sw128_desc(a + kABytes + kk * 32), (kb | kk) != 0);
-            tc_commit(empty0 + 8 * s);  // the stage is free once these MMAs have read it
+                for (uint32_t kk = 0; kk < kGemmBK / 16; ++kk)
+                    tc_mma(d, sw128_desc(sa + kk * 32), sw128_desc(sa + kABytes + kk * 32), (kb | kk) != 0);
+                tc_commit(empty0 + 8 * s);  // the stage is free once these MMAs have read it
+            }
+            tc_commit(acc_full0 + 8 * a);  // the tile's accumulator is complete (or abandoned)
         }
-        tc_commit(acc_full);  // every MMA issued above has completed (also after an abort)
+        tc_commit(mma_done);
+        drain_phase(mma_done, 0);  // every MMA of this CTA has completed
     } else if (warp >= 2) {
         // ---------------- epilogue
-        const bool ok = wait_phase(acc_full, 0, abort_flag);
-        tc_fence_after();
-        if (__all_sync(0xffffffffu, ok && !*abort_flag)) {  // warp-uniform: the TMEM loads are collective
-            const uint32_t quarter = warp & 3u;
-            const uint32_t m = m_tile * kGemmBM + quarter * 32 + lane;
+        const uint32_t quarter = warp & 3u;
+        const uint32_t HD = p.H * kGemmHeadDim;
+        uint32_t i = 0;
+        for (uint32_t t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+            const uint32_t a = i % kAccBufs, u = i / kAccBufs;
+            const bool ok = wait_phase(acc_full0 + 8 * a, u & 1u, abort_flag);
+            tc_fence_after();
+            if (!__all_sync(0xffffffffu, ok && !*abort_flag)) break;  // warp-uniform: TMEM loads are collective
+            const Tile tl = decode_tile(p, t);
+            const uint32_t m = tl.m_tile * kGemmBM + quarter * 32 + lane;
             const bool valid = m < p.rows;
-            const uint32_t b = valid ? m / p.Sl : 0, t = valid ? m - b * p.Sl : 0;
-            const uint32_t pos = r * p.Sl + t;
-            const uint32_t HD = p.H * kGemmHeadDim;
+            const uint32_t b = valid ? m / p.Sl : 0, tt = valid ? m - b * p.Sl : 0;
+            const uint32_t pos = tl.r * p.Sl + tt;
 #pragma unroll 1
             for (uint32_t j = 0; j < kGemmBN / kGemmHeadDim; ++j) {
-                const uint32_t f = n_tile * kGemmBN + j * kGemmHeadDim;
+                const uint32_t f = tl.n_tile * kGemmBN + j * kGemmHeadDim;
                 const uint32_t sec = f / HD;
                 const uint32_t h = (f - sec * HD) / kGemmHeadDim;
                 const uint32_t g = h / p.Hl, hh = h - g * p.Hl;
@@ -394,20 +441,22 @@ __global__ void __launch_bounds__(kThreadsG, 1) qkv_gemm_kernel(const __grid_con
                 const bool norm = kFusedT && sec < 2;
                 const uint32_t* wp = norm ? static_cast<const uint32_t*>(p.weight[sec]) : nullptr;
                 const float* tab = norm ? p.table + size_t(pos) * kGemmHeadDim : nullptr;
-                epilogue_head<kFusedT, kNeox>(tmem + ((quarter * 32u) << 16) + j * kGemmHeadDim, valid, norm, wp, tab,
-                                              p.eps, dst_row);
+                epilogue_head<kFusedT, kNeox>(tmem + a * kTmemCols + ((quarter * 32u) << 16) + j * kGemmHeadDim, valid,
+                                              norm, wp, tab, p.eps, dst_row);
             }
+            tc_fence_before();  // this warp's TMEM reads are done (tcgen05.wait::ld) before the release
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty0 + 8 * a);
         }
     }
-    // teardown: all MMAs have completed (the epilogue saw acc_full, or warp 1 waits
-    // for it below) and every TMEM read has finished before the columns are freed
-    if (warp == 1 && lane == 0) drain_phase(acc_full, 0);
+    // teardown: every MMA has completed (warp 1 waited on mma_done) and every TMEM
+    // read has finished before the columns are freed
     __syncwarp();  // the single-lane roles rejoin their warps before the CTA barrier
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, kTmemCols * kAccBufs);
     }
 }
 
@@ -438,8 +487,12 @@ cudaError_t launch_variant(const GemmParams& p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
     const uint64_t tiles = uint64_t(p.P) * p.m_tiles * p.n_tiles;
-    qkv_gemm_kernel<kFusedT, kNeox><<<unsigned(tiles), kThreadsG, kSmemG, stream>>>(p);
+    const unsigned grid = unsigned(tiles < uint64_t(sms > 0 ? sms : 1) ? tiles : uint64_t(sms));  // one CTA per SM
+    qkv_gemm_kernel<kFusedT, kNeox><<<grid, kThreadsG, kSmemG, stream>>>(p);
     return cudaGetLastError();
 }
 
