@@ -56,6 +56,7 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=12)
     ap.add_argument("--sets", type=int, default=2, help="rotating input sets (each ~2 GB)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-projection", action="store_true", help="skip the fused QKV projection measurement")
     ap.add_argument("--cpu-tokens", type=int, default=4096, help="tokens per shard in the CPU-baseline sample")
     return ap.parse_args()
 
@@ -215,6 +216,49 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ our arm
+def measure_projection(torch, binding, synth, w, stream, dev, wq, wk, iters=10):
+    """The fused QKV projection (tcgen05 GEMM with the RMSNorm/RoPE/scatter
+    epilogue) on the workload's shape: hidden = H*D, weight [3*H*D, hidden]."""
+    P, B, S, H, D = w["P"], w["B"], w["S"], w["H"], w["D"]
+    Sl, Hl, hidden = S // P, H // P, H * D
+    xs, wqkv = synth.projection_inputs(P, B, Sl, hidden, H, D, torch.bfloat16, seed=11, device=dev)
+    outs = {k: [torch.empty((B, S, Hl, D), dtype=torch.bfloat16, device=dev) for _ in range(P)] for k in "qkv"}
+
+    def call():
+        binding.project_qkv_into(xs, wqkv, H, outs["q"], outs["k"], outs["v"], norm_rope=True, q_weight=wq,
+                                 k_weight=wk, eps=w["eps"], theta=w["theta"], stream=stream)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / iters
+    flops = 2.0 * B * S * 3 * H * D * hidden
+    tflops = flops / (ms / 1e3) / 1e12
+    peak, peak_sus, src = measured_tensor_peak()
+    return {"kernel": "qkv_gemm_kernel<fused, interleaved> (tcgen05, persistent, 128x256 tiles)",
+            "shape": f"M={B * S} (P={P} shards), N={3 * H * D}, K={hidden}, bf16", "ms": ms,
+            "TFLOP/s": tflops, "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak,
+                                             "unit": "TFLOP/s", "frac": tflops / peak,
+                                             "frac_of_sustained": tflops / peak_sus, "peak_source": src},
+            "iters": iters}
+
+
+def measured_tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured (MEASURED_PEAKS.json, cuBLAS bf16)"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 1700.0, "fallback (1.9 PF burst / 1.7 PF sustained, earlier GB300 measurement)"
+
+
 def run_e2e(args, torch, binding, src, wq, wk, w, stream, dev, world, step_payload):
     """The same step through the public API with the inputs in pinned host memory
     and the results read back, every step: host->device copies of Q/K/V and the
@@ -382,6 +426,10 @@ def main():
     if args.e2e_steps > 0:
         e2e = run_e2e(args, torch, binding, sets[0], wq, wk, w, stream, dev, world, sp + gp)
 
+    projection = None
+    if not args.no_projection:
+        projection = measure_projection(torch, binding, synth, w, stream, dev, wq, wk)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         Sl_cpu = min(args.cpu_tokens, Sl)
@@ -416,6 +464,7 @@ def main():
                          "kernel": FUSED_KERNEL},
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "qkv_projection": projection,
             "clocks": clocks,
             "gpu_launches": launches,
         }

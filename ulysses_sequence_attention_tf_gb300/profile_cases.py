@@ -1,0 +1,60 @@
+"""Small, self-contained launches of one library kernel each, for profilers
+(ncu captures one launch of a case run a few times).
+
+  python -m ulysses_sequence_attention_tf_gb300.profile_cases projection [--S 8192] [--iters 3]
+  python -m ulysses_sequence_attention_tf_gb300.profile_cases scatter_fused [--S 32760] [--iters 3]
+
+Inputs are the seeded synthetic ones of ``synth``; shapes default to the
+video-DiT workload's head geometry (P=4, H=40, D=128, bf16) with a smaller
+sequence for the projection, so a capture holds well under a few GB.
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+from . import binding, build, synth
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("case", choices=["projection", "scatter_fused", "gather"])
+    ap.add_argument("--P", type=int, default=4)
+    ap.add_argument("--S", type=int, default=None, help="global tokens (default 8192 projection, 32760 others)")
+    ap.add_argument("--H", type=int, default=40)
+    ap.add_argument("--iters", type=int, default=3)
+    args = ap.parse_args(argv)
+    P, H, D, B = args.P, args.H, 128, 1
+    S = args.S or (8192 if args.case == "projection" else 32760)
+    Sl, Hl = S // P, H // P
+    build.build()
+    binding.lib()
+    binding.use_torch_allocator(True)
+    dev = torch.device("cuda", 0)
+    wq, wk = synth.norm_weights(D, torch.bfloat16, seed=0, device=dev)
+    if args.case == "projection":
+        xs, w = synth.projection_inputs(P, B, Sl, H * D, H, D, torch.bfloat16, seed=1, device=dev)
+        outs = {k: [torch.empty((B, S, Hl, D), dtype=torch.bfloat16, device=dev) for _ in range(P)] for k in "qkv"}
+
+        def call():
+            binding.project_qkv_into(xs, w, H, outs["q"], outs["k"], outs["v"], norm_rope=True, q_weight=wq,
+                                     k_weight=wk)
+    elif args.case == "scatter_fused":
+        g = synth.qkv_shards(P, B, Sl, H, D, torch.bfloat16, seed=0, layout="v_strided", device=dev)
+
+        def call():
+            binding.scatter_qkv("profile", g["q"], g["k"], g["v"], norm_rope=True, q_weight=wq, k_weight=wk)
+    else:
+        attn = synth.attn_outputs(P, B, S, Hl, D, torch.bfloat16, seed=0, device=dev)
+
+        def call():
+            binding.gather_out("profile", attn)
+    for _ in range(args.iters):
+        call()
+    torch.cuda.synchronize()
+    print(f"{args.case}: {args.iters} launches, device status {binding.device_status()}")
+
+
+if __name__ == "__main__":
+    main()
