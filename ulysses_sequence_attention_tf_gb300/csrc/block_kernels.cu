@@ -56,17 +56,50 @@ __global__ void __launch_bounds__(kThreads, kNF > 0 ? TFU_FUSED_MIN_BLOCKS : TFU
     constexpr int kSlots = kCopy + kNF;
     constexpr int kDepth = kNF > 0 ? kBlockDepth : kCopyBlockDepth;
     constexpr int kRowFloats = kLanes * NP * 2;  // D floats per table row
-    constexpr int kCs = cs_vecs<kNeox, NP>();
+    constexpr int kCs = NP / 2;                   // (cos, sin) float4s of the lane's element pairs
     constexpr uint32_t kGroups = kThreads / kLanes;
+    constexpr uint32_t kHalf = kLanes * 16;       // bytes in half a head row
     static_assert(kSlots >= 1 && kSlots <= kMaxSlots && (kNF == 0) == (kF == Fused::kNone), "slot pattern");
     const uint32_t g_row = threadIdx.x / kLanes, dv = threadIdx.x % kLanes;
+    // Lane dv's bytes of a head row: one 32-byte vector at dv*32 -- or, for the
+    // fused slots of half-split RoPE, 16 bytes at dv*16 of each half, so that
+    // both elements of every rotation pair sit in the same lane.
+    auto is_split = [](int x) { return kNeox && x >= kCopy; };
+    const uint32_t lane_off[2] = {dv * VW, dv * 16};  // whole-vector slots, split slots
+    // `row` already holds the lane's offset (lane_off)
+    auto ld_lane = [&](const uint8_t* row, int x) {
+        if (!is_split(x)) return ld_stream<VW>(row);
+        const Vec<16> lo = ld_stream<16>(row), hi = ld_stream<16>(row + kHalf);
+        Vec<VW> v;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v.w[k] = lo.w[k];
+            v.w[4 + k] = hi.w[k];
+        }
+        return v;
+    };
+    auto st_lane = [&](uint8_t* row, int x, const Vec<VW>& v) {
+        if (!is_split(x)) {
+            st_stream<VW>(row, v);
+            return;
+        }
+        Vec<16> lo, hi;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            lo.w[k] = v.w[k];
+            hi.w[k] = v.w[4 + k];
+        }
+        st_stream<16>(row, lo);
+        st_stream<16>(row + kHalf, hi);
+    };
     uint32_t w[kNF > 0 ? kNF : 1][NP];  // this lane's weight pairs of each fused slot
 #pragma unroll
     for (int f = 0; f < kNF; ++f) {
-        const Vec<VW> wv =
-            *reinterpret_cast<const Vec<VW>*>(static_cast<const uint8_t*>(p.weight[kCopy + f]) + dv * VW);
-#pragma unroll
-        for (int j = 0; j < NP; ++j) w[f][j] = wv.w[j];
+        const uint8_t* wrow = static_cast<const uint8_t*>(p.weight[kCopy + f]);
+        const uint4 a = *reinterpret_cast<const uint4*>(wrow + (kNeox ? dv * 16 : dv * VW));
+        const uint4 b = *reinterpret_cast<const uint4*>(wrow + (kNeox ? kHalf + dv * 16 : dv * VW + 16));
+        w[f][0] = a.x, w[f][1] = a.y, w[f][2] = a.z, w[f][3] = a.w;
+        w[f][4] = b.x, w[f][5] = b.y, w[f][6] = b.z, w[f][7] = b.w;
     }
 #pragma unroll 1
     for (uint32_t u = blockIdx.x; u < p.n_units; u += gridDim.x) {
@@ -79,16 +112,17 @@ __global__ void __launch_bounds__(kThreads, kNF > 0 ? TFU_FUSED_MIN_BLOCKS : TFU
         uint8_t* dst[kSlots];
 #pragma unroll
         for (int x = 0; x < kSlots; ++x) {
-            src[x] = p.src[x][r] + int64_t(b) * p.s_b[x] + int64_t(g) * p.Hg * p.s_h[x] + int64_t(dv) * VW;
-            dst[x] = p.dst[x][g] + int64_t(b) * p.d_b[x] + int64_t(r) * p.Sl * p.d_t[x] + int64_t(dv) * VW;
+            const uint32_t lo = lane_off[is_split(x) ? 1 : 0];
+            src[x] = p.src[x][r] + int64_t(b) * p.s_b[x] + int64_t(g) * p.Hg * p.s_h[x] + lo;
+            dst[x] = p.dst[x][g] + int64_t(b) * p.d_b[x] + int64_t(r) * p.Sl * p.d_t[x] + lo;
         }
         const uint32_t R0 = c * p.rpu;
         const uint32_t n_rows = min(R0 + p.rpu, p.plane_rows) - R0;
         const uint32_t per = (n_rows + kGroups - 1) / kGroups;  // rows per group, the same for every lane
         const uint32_t r_beg = R0 + g_row * per;                 // first plane row of this group
         const uint32_t r_end = min(r_beg + per, R0 + n_rows);    // may be <= r_beg for trailing groups
-        const float* tab_lane =
-            kNF > 0 ? p.table + size_t(r) * p.Sl * kRowFloats + cs_lane_offset<kNeox, kLanes, NP>(dv) : nullptr;
+        // the lane's element pairs use table entries [dv*NP, dv*NP + NP) in both mappings
+        const float* tab_lane = kNF > 0 ? p.table + size_t(r) * p.Sl * kRowFloats + dv * (2 * NP) : nullptr;
         float4 cs[kCs];
 #pragma unroll
         for (int k = 0; k < kCs; ++k) cs[k] = make_float4(1.f, 0.f, 1.f, 0.f);
@@ -102,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, kNF > 0 ? TFU_FUSED_MIN_BLOCKS : TFU
 #pragma unroll
                     for (int k = 0; k < NP; ++k) buf[x].w[k] = 0u;
                 }
-                if (R < r_end) buf[x] = ld_stream<VW>(src[x] + int64_t(t) * p.s_t[x] + int64_t(h) * p.s_h[x]);
+                if (R < r_end) buf[x] = ld_lane(src[x] + int64_t(t) * p.s_t[x] + int64_t(h) * p.s_h[x], x);
             }
         };
         auto compute_store = [&](Vec<VW>(&buf)[kSlots], uint32_t R) {
@@ -118,13 +152,18 @@ __global__ void __launch_bounds__(kThreads, kNF > 0 ? TFU_FUSED_MIN_BLOCKS : TFU
                 }
                 // every lane runs the row reductions (they shuffle); only valid rows are written
 #pragma unroll
-                for (int f = 0; f < kNF; ++f)
-                    norm_rope_core<kF, kLanes, NP, kNeox>(buf[kCopy + f].w, w[f], cs, p.eps);
+                for (int f = 0; f < kNF; ++f) {
+                    if constexpr (kNeox) {
+                        norm_rope_core_split<kF, kLanes, NP>(buf[kCopy + f].w, w[f], cs, p.eps);
+                    } else {
+                        norm_rope_core<kF, kLanes, NP>(buf[kCopy + f].w, w[f], cs, p.eps);
+                    }
+                }
             }
-            if (valid) {
+            if (valid) {  // the scatter targets of one launch share their strides (slot 0's)
+                const int64_t off = int64_t(t) * p.d_t[0] + int64_t(h) * p.d_h[0];
 #pragma unroll
-                for (int x = 0; x < kSlots; ++x)
-                    st_stream<VW>(dst[x] + int64_t(t) * p.d_t[x] + int64_t(h) * p.d_h[x], buf[x]);
+                for (int x = 0; x < kSlots; ++x) st_lane(dst[x] + off, x, buf[x]);
             }
         };
         Vec<VW> bufs[kDepth][kSlots];

@@ -297,5 +297,68 @@ __device__ __forceinline__ void norm_rope_core(uint32_t (&xw)[NP], const uint32_
     }
 }
 
+// Half-split RoPE on a row whose lanes hold matching halves: words [0, NP/2) are
+// the lane's elements of the first half of the row, words [NP/2, NP) their
+// partners D/2 further on; cs[j] holds the (cos, sin) entries of the elements
+// of word j.  RMSNorm and weight scale as in norm_rope_core; the rotation pairs
+// never leave the lane.
+template <Fused kF, int kLanes, int NP>
+__device__ __forceinline__ void norm_rope_core_split(uint32_t (&xw)[NP], const uint32_t (&wpk)[NP],
+                                                     const float4 (&cs)[NP / 2], float eps) {
+    constexpr float kInvD = 1.0f / float(kLanes * NP * 2);
+    uint64_t x2[NP];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        float a, b;
+        unpack2<kF>(xw[j], a, b);
+        x2[j] = f2_pack(a, b);
+    }
+    uint64_t hi2 = f2_mul(x2[0], x2[0]), lo2 = 0;
+#pragma unroll
+    for (int j = 1; j < NP; ++j) {
+        uint64_t s2, e2;
+        f2_two_sum(hi2, f2_mul(x2[j], x2[j]), s2, e2);
+        hi2 = s2;
+        lo2 = f2_add(lo2, e2);
+    }
+    float hi, lo;
+    {
+        float he, ho, le, lo_, e;
+        f2_unpack(hi2, he, ho);
+        f2_unpack(lo2, le, lo_);
+        two_sum(he, ho, hi, e);
+        lo = __fadd_rn(__fadd_rn(le, lo_), e);
+    }
+#pragma unroll
+    for (int m = 1; m < kLanes; m <<= 1) {
+        const float ohi = __shfl_xor_sync(0xffffffffu, hi, m);
+        const float olo = __shfl_xor_sync(0xffffffffu, lo, m);
+        float s, e;
+        two_sum(hi, ohi, s, e);
+        lo = __fadd_rn(__fadd_rn(lo, olo), e);
+        hi = s;
+    }
+    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(__fadd_rn(hi, lo), kInvD), eps)));
+    const uint64_t inv2 = f2_pack(inv, inv);
+    uint32_t z[NP];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        float a, b;
+        f2_unpack(f2_mul(x2[j], inv2), a, b);
+        z[j] = mul2<kF>(pack2<kF>(a, b), wpk[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < NP / 2; ++j) {
+        const float4 c4 = cs[j];
+        float a0, a1, b0, b1;
+        unpack2<kF>(z[j], a0, a1);
+        unpack2<kF>(z[j + NP / 2], b0, b1);
+        xw[j] = pack2<kF>(__fsub_rn(__fmul_rn(a0, c4.x), __fmul_rn(b0, c4.y)),
+                          __fsub_rn(__fmul_rn(a1, c4.z), __fmul_rn(b1, c4.w)));
+        xw[j + NP / 2] = pack2<kF>(__fadd_rn(__fmul_rn(a0, c4.y), __fmul_rn(b0, c4.x)),
+                                   __fadd_rn(__fmul_rn(a1, c4.w), __fmul_rn(b1, c4.z)));
+    }
+}
+
 }  // namespace dev
 }  // namespace tfu

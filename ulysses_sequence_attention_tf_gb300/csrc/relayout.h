@@ -69,7 +69,7 @@ struct RelayoutParams {
     const uint8_t* src[kMaxSlots][kMaxShards];
     uint8_t* dst[kMaxSlots][kMaxShards];
     int64_t s_b[kMaxSlots], s_t[kMaxSlots], s_h[kMaxSlots];  // byte strides
-    int64_t d_b[kMaxSlots], d_t[kMaxSlots], d_h[kMaxSlots];  // byte strides
+    int64_t d_b[kMaxSlots], d_t[kMaxSlots], d_h[kMaxSlots];  // byte strides (a scatter's slots share them)
     const void* weight[kMaxSlots];  // per slot RMSNorm weight [D] (fused slots only)
     const float* table;             // [>= P*S_local][D/2][2] fp32 (fused only)
     float eps;

@@ -255,8 +255,12 @@ tf_status launch_planned(RelayoutParams& p, const Shape& sh, tfu::Dir dir, tfu::
     tf_status s;
     cudaError_t e;
     bool dst_rows_packed = true;  // scatter target rows adjacent (else the fused receive layout)
-    for (uint32_t x = 0; x < p.nx; ++x) dst_rows_packed = dst_rows_packed && p.d_h[x] == int64_t(rb);
-    const bool block_ok = dir == tfu::Dir::kScatter && (rb == 64 || rb == 128 || rb == 256 || rb == 512) &&
+    bool dst_shared = true;       // every slot's targets have the same strides (the block kernel's assumption)
+    for (uint32_t x = 0; x < p.nx; ++x) {
+        dst_rows_packed = dst_rows_packed && p.d_h[x] == int64_t(rb);
+        dst_shared = dst_shared && p.d_t[x] == p.d_t[0] && p.d_h[x] == p.d_h[0];
+    }
+    const bool block_ok = dir == tfu::Dir::kScatter && dst_shared && (rb == 64 || rb == 128 || rb == 256 || rb == 512) &&
                           (fused != tfu::Fused::kNone ? TFU_FUSED_BLOCKS : (TFU_COPY_BLOCKS || !dst_rows_packed));
     const uint32_t vec = pick_vec_bytes(p, sh, src_tokens, dst_tokens);
     const uint32_t rpu = tfu::tma_rows_per_unit(uint32_t(sh.Hl), rb);
