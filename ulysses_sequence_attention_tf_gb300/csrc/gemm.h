@@ -13,12 +13,17 @@ namespace tfu {
 
 constexpr int kGemmBM = 128;  // tile rows (tokens) = TMEM lanes
 constexpr int kGemmBN = 256;  // tile columns (features) = two heads of D = 128
-constexpr int kGemmBK = 64;   // K per stage: one 128-byte swizzle row of bf16
+#ifndef TFU_GEMM_BK
+#define TFU_GEMM_BK 64  // K per stage: 64 (128-byte rows, 128-byte swizzle) or 32 (64-byte rows and swizzle)
+#endif
+constexpr int kGemmBK = TFU_GEMM_BK;
+static_assert(kGemmBK == 64 || kGemmBK == 32, "a stage row is one 128- or 64-byte swizzle span");
 constexpr int kGemmHeadDim = 128;
 
 struct GemmParams {
     CUtensorMap tmap_x[kMaxShards];  // shard r's hidden states [rows = B*Sl][K], box 64 x 128, 128B swizzle
     CUtensorMap tmap_w;              // weight [N = 3*H*D][K], box 64 x 256, 128B swizzle
+    CUtensorMap tmap_w_part;         // the same weight, box 64 x 128: a CTA pair's halves of a weight tile
     uint8_t* dst[3][kMaxShards];     // tensor x (Q, K, V), head group g: target base (layout offset applied)
     int64_t d_b, d_t, d_h;           // target byte strides (batch, token, head)
     const void* weight[2];           // RMSNorm weights of Q and K ([D] bf16), fused mode

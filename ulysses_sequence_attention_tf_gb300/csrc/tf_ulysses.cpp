@@ -878,7 +878,9 @@ TF_API tf_status tf_ulysses_project_qkv_into(const void* const* x, int64_t x_row
                                        tfu::kGemmBM))
             return fail(TF_ERR_UNSUPPORTED, "the driver refused the tensor map of x[%d]", r);
     if (!tfu::encode_tensor_map_2d(&p.tmap_w, w_qkv, uint64_t(hidden), n_tiles * tfu::kGemmBN,
-                                   uint64_t(w_row_stride) * 2, tfu::kGemmBN))
+                                   uint64_t(w_row_stride) * 2, tfu::kGemmBN) ||
+        !tfu::encode_tensor_map_2d(&p.tmap_w_part, w_qkv, uint64_t(hidden), n_tiles * tfu::kGemmBN,
+                                   uint64_t(w_row_stride) * 2, tfu::kGemmBN / 2))
         return fail(TF_ERR_UNSUPPORTED, "the driver refused the tensor map of w_qkv");
     p.d_h = pitch;
     p.d_t = pitch * sh.Hl;
