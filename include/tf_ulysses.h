@@ -389,6 +389,16 @@ TF_API tf_status tf_ulysses_set_slots(const char *tag, int num_slots);
  * made in this process: unchanged across calls that hit the cache. */
 TF_API uint64_t tf_ulysses_alloc_count(void);
 
+/*
+ * tf_ulysses_selftest_wait -- failure-detection self-test of the in-kernel
+ * bounded waits: one thread waits, on `stream`, for a phase of an mbarrier that
+ * nothing ever arrives on, with a budget of `cycles` SM clock cycles (1..1e9).
+ * The wait gives up, the kernel returns, and tf_ulysses_device_status then
+ * reports bit 1 (clear it with clear != 0).  Nothing faults or hangs; the
+ * context stays usable.  Errors: TF_ERR_INVALID for cycles out of range.
+ */
+TF_API tf_status tf_ulysses_selftest_wait(unsigned long long cycles, void *stream);
+
 /* One-line reason for the calling thread's last non-TF_OK status ("" if none). */
 TF_API const char *tf_ulysses_last_error(void);
 

@@ -139,6 +139,8 @@ def test_slot_configuration_checked(tf):
     assert lib.tf_ulysses_set_slots(b"x" * 64, 2) == 1
     assert lib.tf_ulysses_set_slots(b"rot", 2) == 0  # configuration only: no CUDA call
     assert lib.tf_ulysses_alloc_count() == 0
+    assert lib.tf_ulysses_selftest_wait(0, None) == 1
+    assert lib.tf_ulysses_selftest_wait(2_000_000_000, None) == 1
 
 
 def test_gather_rejects_before_any_cuda_call(tf):

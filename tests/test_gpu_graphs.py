@@ -214,3 +214,21 @@ def test_capture_head_chunks_and_exchange(tf):
 def test_device_status_clean(tf):
     torch.cuda.synchronize()
     assert tf.device_status(clear=False) == 0
+
+
+def test_bounded_wait_gives_up_and_reports(tf):
+    """Failure detection without a fault: a wait on an mbarrier that nothing
+    arrives on gives up after its budget, the status word reports it, and the
+    context keeps working."""
+    torch.cuda.synchronize()
+    assert tf.device_status(clear=True) == 0
+    tf.selftest_wait(2_000_000)  # ~1 ms at 2 GHz
+    torch.cuda.synchronize()
+    assert tf.device_status(clear=True) == 2  # bit 1: the projection kernel's bounded waits
+    assert tf.device_status(clear=False) == 0
+    x = _static_inputs(70)
+    tq, _, _, _ = tf.scatter_qkv("after_selftest", x["q"], x["k"], x["v"])
+    torch.cuda.synchronize()
+    assert bits_equal(tq[1].cpu(), oracle.scatter([t.cpu() for t in x["q"]], P)[1])
+    with pytest.raises(tf.TfUlyssesError):
+        tf.selftest_wait(0)

@@ -96,6 +96,8 @@ def _declare(lib):
     lib.tf_ulysses_last_error.restype = ctypes.c_char_p
     lib.tf_ulysses_launch_count.argtypes = []
     lib.tf_ulysses_launch_count.restype = ctypes.c_uint64
+    lib.tf_ulysses_selftest_wait.argtypes = [ctypes.c_ulonglong, vp]
+    lib.tf_ulysses_selftest_wait.restype = i32
     lib.tf_ulysses_set_slots.argtypes = [ctypes.c_char_p, i32]
     lib.tf_ulysses_set_slots.restype = i32
     lib.tf_ulysses_alloc_count.argtypes = []
@@ -398,6 +400,12 @@ def device_status(clear: bool = False) -> int:
     v = ctypes.c_uint()
     _check(lib().tf_ulysses_device_status(1 if clear else 0, ctypes.byref(v)))
     return int(v.value)
+
+
+def selftest_wait(cycles: int, *, stream=None):
+    """Launch the bounded-wait self-test (a wait nothing satisfies, given up after
+    ``cycles`` clock cycles); ``device_status()`` then has bit 1 set."""
+    _check(lib().tf_ulysses_selftest_wait(int(cycles), _stream_handle(stream)))
 
 
 def set_slots(tag, num_slots: int):

@@ -49,8 +49,17 @@ int block_device_sms() {
     return sms > 0 ? sms : 1;
 }
 
+#ifndef TFU_QK_MIN_BLOCKS
+#define TFU_QK_MIN_BLOCKS TFU_FUSED_MIN_BLOCKS  // resident CTAs per SM for fused launches without a copied slot
+#endif
+
+template <int kCopy, int kNF>
+__host__ __device__ constexpr int block_min_blocks() {
+    return kNF == 0 ? TFU_COPY_BLOCK_MIN_BLOCKS : (kCopy == 0 ? TFU_QK_MIN_BLOCKS : TFU_FUSED_MIN_BLOCKS);
+}
+
 template <Fused kF, int kLanes, int kCopy, int kNF, bool kNeox>
-__global__ void __launch_bounds__(kThreads, kNF > 0 ? TFU_FUSED_MIN_BLOCKS : TFU_COPY_BLOCK_MIN_BLOCKS)
+__global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
     block_kernel(const __grid_constant__ RelayoutParams p) {
     constexpr int VW = 32, NP = 8;                // 32 bytes = 8 element pairs per lane
     constexpr int kSlots = kCopy + kNF;

@@ -40,6 +40,10 @@ struct GemmParams {
 // fused: RMSNorm + RoPE on the Q and K sections; neox: half-split pairs.
 cudaError_t launch_qkv_gemm(const GemmParams& p, bool fused, bool neox, cudaStream_t stream);
 
+// One thread waits (bounded by `cycles` clock cycles) on an mbarrier nothing
+// arrives on: the projection kernel's bounded wait must give up and report.
+cudaError_t launch_wait_selftest(long long cycles, cudaStream_t stream);
+
 // Device status word of the GEMM kernel: 0, or bit 0 when a bounded wait gave up.
 cudaError_t read_gemm_status(unsigned* out, bool clear);
 

@@ -93,14 +93,15 @@ __device__ __forceinline__ void fence_barrier_init() {
 
 // Wait for the phase of `bar` with parity `parity`; false if the abort flag is
 // raised or the budget runs out (then records the status and raises the flag).
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           long long budget = kWaitCyclesG) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (*abort_flag) return false;
-            if (clock64() - t0 > kWaitCyclesG) {
+            if (clock64() - t0 > budget) {
                 atomicOr(&g_gemm_status, kStatusWait);
                 *abort_flag = 1;
                 return false;
@@ -531,6 +532,20 @@ __global__ void __launch_bounds__(kThreadsG, 1) qkv_gemm_kernel(const __grid_con
     }
 }
 
+// Self-test of the bounded wait: one thread waits on a phase of an mbarrier that
+// nothing ever arrives on, with a budget of `budget` clock cycles; the wait gives
+// up, records the status bit and raises the abort flag, and the kernel returns.
+__global__ void wait_selftest_kernel(long long budget) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    const bool ok = wait_phase(smem_u32(&bar), 0, &abort_flag, budget);
+    if (ok || !abort_flag) atomicOr(&g_gemm_status, 0x80000000u);  // would mean the wait returned wrongly
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static bool tried = false;
@@ -608,6 +623,11 @@ cudaError_t launch_qkv_gemm(const GemmParams& p, bool fused, bool neox, cudaStre
     constexpr int C = TFU_GEMM_CLUSTER;
     if (!fused) return launch_variant<false, false, C>(p, stream);
     return neox ? launch_variant<true, true, C>(p, stream) : launch_variant<true, false, C>(p, stream);
+}
+
+cudaError_t launch_wait_selftest(long long cycles, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(cycles);
+    return cudaGetLastError();
 }
 
 cudaError_t read_gemm_status(unsigned* out, bool clear) {

@@ -1062,6 +1062,15 @@ TF_API tf_status tf_ulysses_device_status(int clear, unsigned* status) {
     return TF_OK;
 }
 
+TF_API tf_status tf_ulysses_selftest_wait(unsigned long long cycles, void* stream) {
+    if (cycles == 0 || cycles > 1000000000ull)
+        return fail(TF_ERR_INVALID, "cycles=%llu outside [1, 1e9]", (unsigned long long)cycles);
+    cudaError_t e = tfu::launch_wait_selftest((long long)cycles, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "launching the bounded-wait self-test");
+    g_launches.fetch_add(1);
+    return TF_OK;
+}
+
 TF_API const char* tf_ulysses_last_error(void) { return g_last_error.c_str(); }
 
 TF_API uint64_t tf_ulysses_launch_count(void) { return g_launches.load(); }
