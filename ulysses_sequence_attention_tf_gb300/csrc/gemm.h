@@ -36,6 +36,43 @@ struct GemmParams {
     uint32_t n_group;                // rasterisation: n-tiles that share a pass over the rows
 };
 
+// One output tile of the projection: shard r, row tile m_tile (128 rows of the
+// shard), column tile n_tile (256 features).
+struct GemmTile {
+    uint32_t r, m_tile, n_tile;
+};
+
+// Tile order: passes of n_group column tiles; inside a pass, row tiles (over all
+// shards) outer and column tiles inner, so the CTAs running together share the
+// weight columns of the pass and the rows of a few row tiles.  With clusters of
+// kCluster CTAs, unit t is a group of kCluster consecutive row tiles of one
+// column tile and cluster rank `rank` takes row tile kCluster*mg + rank; a rank
+// past the last row tile gets m_tile = m_tiles (rows that do not exist: loads
+// fill zeros, nothing is stored), so every CTA of a cluster walks the same units.
+// Units: ceil(P*m_tiles / kCluster) * n_tiles.
+template <int kCluster>
+__host__ __device__ inline GemmTile gemm_tile(uint32_t P, uint32_t m_tiles, uint32_t n_tiles, uint32_t n_group,
+                                              uint32_t t, uint32_t rank) {
+    const uint32_t MT = P * m_tiles;
+    const uint32_t MG = (MT + kCluster - 1) / kCluster;  // row-tile groups
+    const uint32_t pass = t / (n_group * MG);
+    const uint32_t within = t - pass * n_group * MG;
+    const uint32_t rest = n_tiles - pass * n_group;
+    const uint32_t gw = n_group < rest ? n_group : rest;  // column tiles in this pass
+    const uint32_t mg = within / gw;
+    GemmTile tl;
+    tl.n_tile = pass * n_group + (within - mg * gw);
+    const uint32_t mt = mg * kCluster + rank;
+    if (mt < MT) {
+        tl.r = mt / m_tiles;
+        tl.m_tile = mt - tl.r * m_tiles;
+    } else {
+        tl.r = 0;
+        tl.m_tile = m_tiles;
+    }
+    return tl;
+}
+
 // Launch the projection + epilogue for every (shard, row tile, column tile).
 // fused: RMSNorm + RoPE on the Q and K sections; neox: half-split pairs.
 cudaError_t launch_qkv_gemm(const GemmParams& p, bool fused, bool neox, cudaStream_t stream);

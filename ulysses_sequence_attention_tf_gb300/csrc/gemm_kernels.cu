@@ -309,37 +309,11 @@ __device__ __forceinline__ void epilogue_head(uint32_t taddr, bool valid, bool n
 }
 
 // ---------------------------------------------------------------- the kernel
-struct Tile {
-    uint32_t r, m_tile, n_tile;
-};
+using Tile = GemmTile;
 
-// Tiles in passes of n_group column tiles; inside a pass, row tiles (over all
-// shards) outer and column tiles inner, so the CTAs running together share the
-// weight columns of the pass and the rows of a few row tiles.  With clusters of
-// kCluster CTAs, unit t is a group of kCluster consecutive row tiles of one
-// column tile and cluster rank `rank` takes row tile kCluster*mt + rank; a rank
-// past the last row tile gets a tile beyond the rows (loads fill zeros, nothing
-// is stored), so both CTAs of a cluster always walk the same units.
 template <int kCluster>
 __device__ __forceinline__ Tile decode_tile(const GemmParams& p, uint32_t t, uint32_t rank) {
-    const uint32_t MT = p.P * p.m_tiles;
-    const uint32_t MG = (MT + kCluster - 1) / kCluster;  // row-tile groups
-    const uint32_t G = p.n_group;
-    const uint32_t pass = t / (G * MG);
-    const uint32_t within = t - pass * G * MG;
-    const uint32_t gw = min(G, p.n_tiles - pass * G);
-    const uint32_t mg = within / gw;
-    Tile tl;
-    tl.n_tile = pass * G + (within - mg * gw);
-    const uint32_t mt = mg * kCluster + rank;
-    if (mt < MT) {
-        tl.r = mt / p.m_tiles;
-        tl.m_tile = mt - tl.r * p.m_tiles;
-    } else {
-        tl.r = 0;
-        tl.m_tile = p.m_tiles;  // rows m_tiles*128.. do not exist
-    }
-    return tl;
+    return gemm_tile<kCluster>(p.P, p.m_tiles, p.n_tiles, p.n_group, t, rank);
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
