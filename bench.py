@@ -259,6 +259,19 @@ def measured_tensor_peak():
         return 1900.0, 1700.0, "fallback (1.9 PF burst / 1.7 PF sustained, earlier GB300 measurement)"
 
 
+def max_over_ranks(torch, dist, ms, dev):
+    """The slowest rank's time: replicas finish when the last one does."""
+    t = torch.tensor([float(ms)], device=dev, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(world, payload_bytes_per_step, steps, max_ms):
+    """Whole-job GB/s of N replicas: every rank moves the per-step payload each
+    step, and the job takes the slowest rank's time."""
+    return world * payload_bytes_per_step * steps / (max_ms / 1e3) / 1e9
+
+
 def run_e2e(args, torch, binding, src, wq, wk, w, stream, dev, world, step_payload):
     """The same step through the public API with the inputs in pinned host memory
     and the results read back, every step: host->device copies of Q/K/V and the
@@ -324,10 +337,8 @@ def run_e2e(args, torch, binding, src, wq, wk, w, stream, dev, world, step_paylo
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
     if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    return {"value": world * step_payload * args.e2e_steps / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+        e2e_ms = max_over_ranks(torch, dist, e2e_ms, dev)
+    return {"value": aggregate_gbs(world, step_payload, args.e2e_steps, e2e_ms), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.e2e_steps,
             "steps": args.e2e_steps,
             "note": "pinned host Q/K/V/attention inputs copied in, all targets and outputs copied out, every "
@@ -408,14 +419,12 @@ def main():
     scat_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
     gath_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
     if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(torch, dist, total_ms, dev)
         dist.barrier()
 
     sp, sx, gp = step_bytes(w)
     ms_per_step = total_ms / K
-    value = world * (sp + gp) * K / (total_ms / 1e3) / 1e9
+    value = aggregate_gbs(world, sp + gp, K, total_ms)
     scat_avg = sum(scat_ms) / K
     gath_avg = sum(gath_ms) / K
     peak, peak_src = measured_peak()
