@@ -215,6 +215,29 @@ def test_portfolio_small_vs_oracle(tf, P):
             assert bits_equal(outs[r].cpu(), want[r]), (P, dtype, r)
 
 
+@pytest.mark.parametrize("P", [2, 4, 6, 8])
+@pytest.mark.parametrize("D", [64, 128])
+def test_portfolio_fused_vs_oracle(tf, P, D):
+    """The portfolio shapes through the fused scatter (RMSNorm + RoPE on Q/K,
+    V copied), fp16 and bf16, S=601 padded to a multiple of P, B=2."""
+    B, H, S0 = 2, 48, 601
+    for dtype in (torch.float16, torch.bfloat16):
+        S = synth.padded_seq(S0, P)
+        d = synth.qkv_shards(P, B, S // P, H, D, dtype, seed=100 + P * D, layout="fused", pad_from=S0)
+        wq, wk = synth.norm_weights(D, dtype, seed=P)
+        g = to_device_like(d)
+        tq, tk, tv, _ = tf.scatter_qkv(f"pf_fused{D}", g["q"], g["k"], g["v"], norm_rope=True, q_weight=wq.cuda(),
+                                       k_weight=wk.cuda(), eps=EPS, theta=THETA)
+        table = oracle.rope_table(THETA, S, D)
+        for key, tg, w in (("q", tq, wq), ("k", tk, wk)):
+            want = oracle.scatter_norm_rope(d[key], P, w, EPS, table)
+            for i in range(P):
+                assert_fused_ok(tg[i], want[i])
+        want_v = oracle.scatter(d["v"], P)
+        for i in range(P):
+            assert bits_equal(tv[i].cpu(), want_v[i]), (P, D, dtype, i)
+
+
 # ------------------------------------------------------------------ bandwidth sweep, bf16, single tensor
 @pytest.mark.parametrize("P", [2, 4, 8])
 def test_sweep_single_tensor(tf, P):
