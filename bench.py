@@ -241,7 +241,8 @@ def measure_projection(torch, binding, synth, w, stream, dev, wq, wk, iters=10):
     flops = 2.0 * B * S * 3 * H * D * hidden
     tflops = flops / (ms / 1e3) / 1e12
     peak, peak_sus, src = measured_tensor_peak()
-    return {"kernel": "qkv_gemm_kernel<fused, interleaved> (tcgen05, persistent, 128x256 tiles)",
+    return {"kernel": "qkv_gemm_pair_kernel<fused, interleaved> (tcgen05 cta_group::2, persistent CTA pairs, "
+                      "256x256 tiles)",
             "shape": f"M={B * S} (P={P} shards), N={3 * H * D}, K={hidden}, bf16", "ms": ms,
             "TFLOP/s": tflops, "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak,
                                              "unit": "TFLOP/s", "frac": tflops / peak,

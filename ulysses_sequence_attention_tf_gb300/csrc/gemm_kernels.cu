@@ -13,7 +13,11 @@
 // lands in head group g = h / Hl at target row r*Sl + t, head h % Hl; Q and K rows
 // then get the RMSNorm + RoPE of tf_ulysses.h at global position p = r*Sl + t.
 //
-// Design (persistent: one CTA of 192 threads per SM walks 128 x 256 output tiles):
+// Two forms of one design.  The default, qkv_gemm_pair_kernel (below), runs CTA
+// pairs on the 2-SM MMA over 256 x 256 tiles; the single-CTA form described here
+// is the fallback (build option TFU_GEMM_PAIR=0, or no pair cluster fits) and
+// shares its epilogue, raster and failure handling.
+// Single-CTA form (persistent: one CTA of 192 threads per SM walks 128 x 256 output tiles):
 //  * warp 0, one lane: TMA producer.  Each stage holds a 128 x 64 tile of X and a
 //    256 x 64 tile of W (bf16, 128-byte swizzle), loaded with
 //    cp.async.bulk.tensor onto the stage's mbarrier (transaction bytes).
@@ -76,15 +80,27 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
+// kCS: acquire at cluster scope (arrivals and copies of the other CTA of a pair).
+template <bool kCS = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
+    if constexpr (kCS) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+    }
     return ok != 0;
 }
 __device__ __forceinline__ void fence_barrier_init() {
@@ -92,18 +108,22 @@ __device__ __forceinline__ void fence_barrier_init() {
 }
 
 // Wait for the phase of `bar` with parity `parity`; false if the abort flag is
-// raised or the budget runs out (then records the status and raises the flag).
+// raised or the budget runs out (then records the status and raises the flag,
+// and also the flag at shared::cluster address `peer_flag` of the other CTA of a
+// pair when it is not 0).
+template <bool kCS = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                           long long budget = kWaitCyclesG) {
-    if (mbar_try_wait(bar, parity)) return true;
+                                           long long budget = kWaitCyclesG, uint32_t peer_flag = 0) {
+    if (mbar_try_wait<kCS>(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait<kCS>(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (*abort_flag) return false;
             if (clock64() - t0 > budget) {
                 atomicOr(&g_gemm_status, kStatusWait);
                 *abort_flag = 1;
+                if (peer_flag) asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_flag), "r"(1u) : "memory");
                 return false;
             }
         }
@@ -111,9 +131,10 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 }
 
 // The same without the abort flag (draining after an abort): bounded only.
+template <bool kCS = false>
 __device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity) {
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait<kCS>(bar, parity)) {
         if (clock64() - t0 > kWaitCyclesG) return;
     }
 }
@@ -506,6 +527,244 @@ __global__ void __launch_bounds__(kThreadsG, 1) qkv_gemm_kernel(const __grid_con
     }
 }
 
+// ---------------------------------------------------------------- CTA pairs (cta_group::2)
+// The pair form of the projection: the two CTAs of a cluster compute one
+// 256 x 256 tile with tcgen05.mma.cta_group::2 (M = 256), issued by the even CTA.
+// Each CTA stages its own 128 rows of X and one 128-row half of the weight tile
+// (the lower CTA the first half), so a stage is 32 KiB instead of 48 KiB and the
+// ring holds more k-blocks; the MMA reads both CTAs' stages and writes each CTA's
+// 128 rows x 256 columns into that CTA's TMEM, where its own epilogue reads them.
+//  * both CTAs' loads complete on the even CTA's stage barrier (cp.async.bulk.tensor
+//    .cta_group::2 signals a barrier of either CTA of the pair); the even CTA's
+//    producer posts the transaction bytes of the whole pair;
+//  * the MMA thread's commits arrive on both CTAs' stage and accumulator barriers
+//    (multicast), so each producer refills its stage, and each epilogue starts, on
+//    its own barriers;
+//  * both CTAs' epilogue warps release an accumulator on the even CTA's barrier;
+//  * TMEM is allocated and freed by one warp of each CTA together (cta_group::2).
+#ifndef TFU_GEMM_PAIR_STAGES
+#define TFU_GEMM_PAIR_STAGES 6
+#endif
+constexpr int kStagesP = TFU_GEMM_PAIR_STAGES;
+constexpr uint32_t kBHalfBytes = kBBytes / 2;
+constexpr uint32_t kStageBytesP = kABytes + kBHalfBytes;
+constexpr size_t kSmemP = size_t(kStagesP) * kStageBytesP + 256 + 1024;
+static_assert(kSmemP <= 232448, "the pair stage ring exceeds 227 KiB of shared memory");
+// M = 256 (two CTAs of 128 rows), N = 256, otherwise as kIdesc.
+constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kGemmBN >> 3) << 17) |
+                                (uint32_t((2 * kGemmBM) >> 4) << 24);
+
+// shared::cluster address of the object at this CTA's shared address `local` in CTA `rank`.
+__device__ __forceinline__ uint32_t map_rank(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+// Load into this CTA's shared memory; the transaction bytes complete on `bar`, a
+// shared::cluster address of a barrier in either CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t smem_dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, "
+        "{%2, %3}], [%4];" ::"r"(smem_dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+#ifndef TFU_GEMM_HINTS
+// 1: the pair's weight loads carry the L2 evict_last policy, so the weight columns
+// of a raster pass outlive the streaming rows and targets in L2 (0: no policy).
+#define TFU_GEMM_HINTS 1
+#endif
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t smem_dst, const CUtensorMap* map, int x, int y,
+                                                      uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t smem_result, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_result), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D[tmem of both CTAs] (+)= A[smem of both] * B[smem of both]^T, one M=256 x N=256 x K=16 step.
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kIdescPair), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t mask) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
+                     "r"(bar),
+                 "h"(mask)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+template <bool kFusedT, bool kNeox>
+__global__ void __launch_bounds__(kThreadsG, 1) qkv_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kStagesP) * kStageBytesP);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStagesP);
+    const uint32_t acc_full0 = smem_u32(bars + 2 * kStagesP), acc_empty0 = smem_u32(bars + 2 * kStagesP + kAccBufs);
+    const uint32_t mma_done = smem_u32(bars + 2 * kStagesP + 2 * kAccBufs);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStagesP + 2 * kAccBufs + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_rank();  // 0: the CTA that issues the pair's MMAs
+    const uint32_t cid = blockIdx.x / 2, clusters = gridDim.x / 2;
+    const uint32_t units = (p.P * p.m_tiles + 1) / 2 * p.n_tiles;
+    const uint32_t KB = p.K / kGemmBK;
+    const uint32_t full0_lead = map_rank(full0, 0);            // stage barriers the loads of both CTAs complete on
+    const uint32_t acc_empty0_lead = map_rank(acc_empty0, 0);  // accumulator releases of both CTAs
+    const uint32_t peer_flag = map_rank(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u);
+    constexpr uint16_t kBoth = 3;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStagesP; ++s) {
+            mbar_init(full0 + 8 * s, 1);   // the even CTA's producer; bytes of both CTAs
+            mbar_init(empty0 + 8 * s, 1);  // the pair's MMA commit
+        }
+        for (uint32_t a = 0; a < kAccBufs; ++a) {
+            mbar_init(acc_full0 + 8 * a, 1);
+            mbar_init(acc_empty0 + 8 * a, 8);  // the epilogue warps of both CTAs
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols * kAccBufs);
+        tmem_relinquish_pair();
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before either signals the other
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer (both CTAs): this CTA's rows and weight half
+        const uint64_t pol_w = TFU_GEMM_HINTS ? l2_policy_evict_last() : 0;
+        (void)pol_w;
+        uint32_t q = 0;
+        bool ok = true;
+        for (uint32_t t = cid; ok && t < units; t += clusters) {
+            const Tile tl = decode_tile<2>(p, t, rank);
+            const CUtensorMap* mx = &p.tmap_x[tl.r];
+            for (uint32_t kb = 0; kb < KB; ++kb, ++q) {
+                const uint32_t s = q % kStagesP, use = q / kStagesP;
+                if (use > 0 && !wait_phase<true>(empty0 + 8 * s, (use - 1) & 1u, abort_flag, kWaitCyclesG, peer_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t a = smem_u32(smem + size_t(s) * kStageBytesP);
+                if (rank == 0) mbar_expect_tx(full0 + 8 * s, 2 * kStageBytesP);
+                tma_load_2d_pair(a, mx, int(kb * kGemmBK), int(tl.m_tile * kGemmBM), full0_lead + 8 * s);
+                const int wy = int(tl.n_tile * kGemmBN + rank * (kGemmBN / 2));
+                if constexpr (TFU_GEMM_HINTS != 0) {
+                    tma_load_2d_pair_hint(a + kABytes, &p.tmap_w_part, int(kb * kGemmBK), wy, full0_lead + 8 * s, pol_w);
+                } else {
+                    tma_load_2d_pair(a + kABytes, &p.tmap_w_part, int(kb * kGemmBK), wy, full0_lead + 8 * s);
+                }
+            }
+        }
+        // the MMAs that read the last fill of each stage have completed (their commit
+        // arrives on this CTA's stage barriers), so this CTA's loads have all landed
+        for (uint32_t k = q > uint32_t(kStagesP) ? q - kStagesP : 0; k < q; ++k)
+            drain_phase<true>(empty0 + 8 * (k % kStagesP), (k / kStagesP) & 1u);
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer (the even CTA)
+        if (rank == 0) {
+            uint32_t q = 0, i = 0;
+            bool ok = true;
+            for (uint32_t t = cid; ok && t < units; t += clusters, ++i) {
+                const uint32_t a = i % kAccBufs, u = i / kAccBufs;
+                if (u > 0 && !wait_phase<true>(acc_empty0 + 8 * a, (u - 1) & 1u, abort_flag, kWaitCyclesG, peer_flag))
+                    break;  // both epilogues drained it
+                tc_fence_after();
+                const uint32_t d = tmem + a * kTmemCols;
+                for (uint32_t kb = 0; kb < KB; ++kb, ++q) {
+                    const uint32_t s = q % kStagesP, use = q / kStagesP;
+                    if (!wait_phase<true>(full0 + 8 * s, use & 1u, abort_flag, kWaitCyclesG, peer_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + size_t(s) * kStageBytesP);
+#pragma unroll
+                    for (uint32_t kk = 0; kk < kGemmBK / 16; ++kk)
+                        tc_mma_pair(d, sw128_desc(sa + kk * 32), sw128_desc(sa + kABytes + kk * 32), (kb | kk) != 0);
+                    tc_commit_pair(empty0 + 8 * s, kBoth);  // both CTAs' stages are free once read
+                }
+                tc_commit_pair(acc_full0 + 8 * a, kBoth);  // the tile's accumulators are complete (or abandoned)
+            }
+            tc_commit_pair(mma_done, kBoth);
+        }
+        drain_phase<true>(mma_done, 0);  // every MMA of the pair has completed
+    } else if (warp >= 2) {
+        // ---------------- epilogue (both CTAs): this CTA's 128 rows of the pair's tile
+        const uint32_t quarter = warp & 3u;
+        const uint32_t HD = p.H * kGemmHeadDim;
+        uint32_t i = 0;
+        for (uint32_t t = cid; t < units; t += clusters, ++i) {
+            const uint32_t a = i % kAccBufs, u = i / kAccBufs;
+            const bool ok = wait_phase<true>(acc_full0 + 8 * a, u & 1u, abort_flag, kWaitCyclesG, peer_flag);
+            tc_fence_after();
+            if (!__all_sync(0xffffffffu, ok && !*abort_flag)) break;  // warp-uniform: TMEM loads are collective
+            const Tile tl = decode_tile<2>(p, t, rank);
+            const uint32_t m = tl.m_tile * kGemmBM + quarter * 32 + lane;
+            const bool valid = tl.m_tile < p.m_tiles && m < p.rows;
+            const uint32_t b = valid ? m / p.Sl : 0, tt = valid ? m - b * p.Sl : 0;
+            const uint32_t pos = tl.r * p.Sl + tt;
+#pragma unroll 1
+            for (uint32_t j = 0; j < kGemmBN / kGemmHeadDim; ++j) {
+                const uint32_t f = tl.n_tile * kGemmBN + j * kGemmHeadDim;
+                const uint32_t sec = f / HD;
+                const uint32_t h = (f - sec * HD) / kGemmHeadDim;
+                const uint32_t g = h / p.Hl, hh = h - g * p.Hl;
+                uint8_t* dst_row = p.dst[sec][g] + int64_t(b) * p.d_b + int64_t(pos) * p.d_t + int64_t(hh) * p.d_h;
+                const bool norm = kFusedT && sec < 2;
+                const uint32_t* wp = norm ? static_cast<const uint32_t*>(p.weight[sec]) : nullptr;
+                const float* tab = norm ? p.table + size_t(pos) * kGemmHeadDim : nullptr;
+                epilogue_head<kFusedT, kNeox>(tmem + a * kTmemCols + ((quarter * 32u) << 16) + j * kGemmHeadDim, valid,
+                                              norm, wp, tab, p.eps, dst_row);
+            }
+            tc_fence_before();  // this warp's TMEM reads are done before the release
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_empty0_lead + 8 * a);
+        }
+    }
+    // teardown: the pair's MMAs have completed and both CTAs' TMEM reads have
+    // finished; the CTAs leave together and free their TMEM together
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, kTmemCols * kAccBufs);
+    }
+}
+
 // Self-test of the bounded wait: one thread waits on a phase of an mbarrier that
 // nothing ever arrives on, with a budget of `budget` clock cycles; the wait gives
 // up, records the status bit and raises the abort flag, and the kernel returns.
@@ -569,6 +828,55 @@ cudaError_t launch_variant(const GemmParams& p, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
+// The pair form: clusters of two CTAs, as many as can be resident at once (at most
+// one per unit); 0 clusters fit -> cudaErrorNotSupported (the caller falls back).
+template <bool kFusedT, bool kNeox>
+cudaError_t launch_pair_variant(const GemmParams& p, cudaStream_t stream) {
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    auto kernel = qkv_gemm_pair_kernel<kFusedT, kNeox>;
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemP));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(unsigned(sms > 1 ? sms / 2 * 2 : 2));
+    cfg.blockDim = dim3(kThreadsG);
+    cfg.dynamicSmemBytes = kSmemP;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int fit = 0;
+    e = cudaOccupancyMaxActiveClusters(&fit, kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (fit < 1) return cudaErrorNotSupported;
+    const uint64_t units = (uint64_t(p.P) * p.m_tiles + 1) / 2 * p.n_tiles;
+    const uint64_t clusters = uint64_t(fit) < units ? uint64_t(fit) : units;
+    cfg.gridDim = dim3(unsigned(clusters * 2));
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+#ifndef TFU_GEMM_PAIR
+// 1: CTA pairs with the 2-SM MMA (qkv_gemm_pair_kernel; on the video-DiT projection
+// 1666-1692 TFLOP/s fused where the single-CTA kernel gives 1537-1570 on the same
+// GPU, before the 32 MB raster pass and the L2 policy); 0: single CTAs, or the
+// multicast pairs of TFU_GEMM_CLUSTER.
+#define TFU_GEMM_PAIR 1
+#endif
+
 #ifndef TFU_GEMM_CLUSTER
 // 1: single CTAs.  2: CTA pairs share each weight tile by TMA multicast (a third
 // less L2 traffic per CTA; measured equal on the video-DiT projection, where the
@@ -595,6 +903,13 @@ bool encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t cols, uin
 cudaError_t launch_qkv_gemm(const GemmParams& p, bool fused, bool neox, cudaStream_t stream) {
     if (uint64_t(p.P) * p.m_tiles * p.n_tiles == 0) return cudaSuccess;
     constexpr int C = TFU_GEMM_CLUSTER;
+    if (TFU_GEMM_PAIR) {
+        const cudaError_t e = !fused ? launch_pair_variant<false, false>(p, stream)
+                              : neox ? launch_pair_variant<true, true>(p, stream)
+                                     : launch_pair_variant<true, false>(p, stream);
+        if (e != cudaErrorNotSupported) return e;
+        (void)cudaGetLastError();
+    }
     if (!fused) return launch_variant<false, false, C>(p, stream);
     return neox ? launch_variant<true, true, C>(p, stream) : launch_variant<true, false, C>(p, stream);
 }

@@ -805,6 +805,14 @@ TF_API tf_status tf_ulysses_exchange_chunks(const void* const* src, void* const*
 
 // Fused QKV projection: the tcgen05 GEMM whose epilogue applies the Q/K
 // RMSNorm + RoPE and stores every head row into its head-group target.
+#ifndef TFU_GEMM_PASS_MB
+// Weight bytes per raster pass of the projection, kept in L2 while the rows stream
+// past: small enough that the pass's weight columns and the row slabs in flight
+// share L2 (32 MB: 1880-1900 TFLOP/s on the video-DiT projection; 48 MB 1700-1800,
+// 96 MB 1670-1700, 16 MB 1710-1750).
+#define TFU_GEMM_PASS_MB 32
+#endif
+
 TF_API tf_status tf_ulysses_project_qkv_into(const void* const* x, int64_t x_row_stride, const void* w_qkv,
                                              int64_t w_row_stride, int P, int B, int S_local, int hidden, int H,
                                              int D, tf_dtype dtype, tf_mode mode, const tf_norm_rope* nr,
@@ -897,9 +905,9 @@ TF_API tf_status tf_ulysses_project_qkv_into(const void* const* x, int64_t x_row
     p.rows = uint32_t(rows);
     p.m_tiles = uint32_t(m_tiles);
     p.n_tiles = uint32_t(n_tiles);
-    // a pass over all row tiles reads n_group column tiles of the weight (~48 MB: L2-resident)
+    // a pass over all row tiles reads n_group column tiles of the weight (L2-resident)
     const uint64_t wbytes_tile = uint64_t(tfu::kGemmBN) * uint64_t(hidden) * 2;
-    uint64_t G = (uint64_t(48) << 20) / wbytes_tile;
+    uint64_t G = (uint64_t(TFU_GEMM_PASS_MB) << 20) / wbytes_tile;
     p.n_group = uint32_t(G < 1 ? 1 : (G > n_tiles ? n_tiles : G));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     bool cap = false;
