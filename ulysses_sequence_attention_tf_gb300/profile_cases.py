@@ -3,6 +3,7 @@
 
   python -m ulysses_sequence_attention_tf_gb300.profile_cases projection [--S 8192] [--iters 3]
   python -m ulysses_sequence_attention_tf_gb300.profile_cases scatter_fused [--S 32760] [--iters 3]
+  python -m ulysses_sequence_attention_tf_gb300.profile_cases scatter_fused_qk [--S 32760] [--iters 3]
 
 Inputs are the seeded synthetic ones of ``synth``; shapes default to the
 video-DiT workload's head geometry (P=4, H=40, D=128, bf16) with a smaller
@@ -19,7 +20,7 @@ from . import binding, build, synth
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("case", choices=["projection", "scatter_fused", "gather"])
+    ap.add_argument("case", choices=["projection", "scatter_fused", "scatter_fused_qk", "gather"])
     ap.add_argument("--P", type=int, default=4)
     ap.add_argument("--S", type=int, default=None, help="global tokens (default 8192 projection, 32760 others)")
     ap.add_argument("--H", type=int, default=40)
@@ -40,11 +41,12 @@ def main(argv=None):
         def call():
             binding.project_qkv_into(xs, w, H, outs["q"], outs["k"], outs["v"], norm_rope=True, q_weight=wq,
                                      k_weight=wk)
-    elif args.case == "scatter_fused":
+    elif args.case in ("scatter_fused", "scatter_fused_qk"):
         g = synth.qkv_shards(P, B, Sl, H, D, torch.bfloat16, seed=0, layout="v_strided", device=dev)
+        v = g["v"] if args.case == "scatter_fused" else None  # Q/K only: V moves elsewhere
 
         def call():
-            binding.scatter_qkv("profile", g["q"], g["k"], g["v"], norm_rope=True, q_weight=wq, k_weight=wk)
+            binding.scatter_qkv("profile", g["q"], g["k"], v, norm_rope=True, q_weight=wq, k_weight=wk)
     else:
         attn = synth.attn_outputs(P, B, S, Hl, D, torch.bfloat16, seed=0, device=dev)
 
