@@ -25,6 +25,7 @@ def main(argv=None):
     ap.add_argument("--S", type=int, default=None, help="global tokens (default 8192 projection, 32760 others)")
     ap.add_argument("--H", type=int, default=40)
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--rope", choices=["interleaved", "neox"], default="interleaved")
     args = ap.parse_args(argv)
     P, H, D, B = args.P, args.H, 128, 1
     S = args.S or (8192 if args.case == "projection" else 32760)
@@ -40,13 +41,14 @@ def main(argv=None):
 
         def call():
             binding.project_qkv_into(xs, w, H, outs["q"], outs["k"], outs["v"], norm_rope=True, q_weight=wq,
-                                     k_weight=wk)
+                                     k_weight=wk, rope=args.rope)
     elif args.case in ("scatter_fused", "scatter_fused_qk"):
         g = synth.qkv_shards(P, B, Sl, H, D, torch.bfloat16, seed=0, layout="v_strided", device=dev)
         v = g["v"] if args.case == "scatter_fused" else None  # Q/K only: V moves elsewhere
 
         def call():
-            binding.scatter_qkv("profile", g["q"], g["k"], v, norm_rope=True, q_weight=wq, k_weight=wk)
+            binding.scatter_qkv("profile", g["q"], g["k"], v, norm_rope=True, q_weight=wq, k_weight=wk,
+                                rope=args.rope)
     else:
         attn = synth.attn_outputs(P, B, S, Hl, D, torch.bfloat16, seed=0, device=dev)
 
