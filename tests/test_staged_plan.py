@@ -2,7 +2,9 @@
 same code the kernel runs: for many shapes and strides, every unit fits one
 shared-memory stage, its bulk-copy runs tile the unit's rows exactly and in
 order, every run is really contiguous under the strides, stays inside the
-plane, and has 16-byte aligned offsets and sizes."""
+plane, and has 16-byte aligned offsets and sizes; and the same runs dealt out
+to the lanes of a warp (for_each_run_lane) are, over all lanes, exactly those
+runs."""
 import os
 import subprocess
 
@@ -12,13 +14,15 @@ CSRC = os.path.join(ROOT, "ulysses_sequence_attention_tf_gb300", "csrc")
 HARNESS = r'''
 #include <cstdio>
 #include <cstdint>
+#include <algorithm>
+#include <utility>
 #include <vector>
 #include "tma_plan.h"
 using namespace tfu;
 static uint64_t x = 0x9E3779B97F4A7C15ull;
 static uint32_t rnd(uint32_t n) { x ^= x << 13; x ^= x >> 7; x ^= x << 17; return uint32_t(x % n); }
 int main() {
-  long bad = 0, cases = 0;
+  long bad = 0, cases = 0, lane_checks = 0;
   for (int it = 0; it < 4000; ++it) {
     const uint32_t Sl = 1 + rnd(300), Hl = rnd(4) == 0 ? 1 : 1 + rnd(70);
     const uint32_t rb = 16 * (1 + rnd(40));            // D * esize, a multiple of 16
@@ -47,11 +51,24 @@ int main() {
         next = i + n;
       });
       if (next != R1 - R0) ++bad;
+      // the same runs dealt out to lanes: their union is exactly for_each_run's runs
+      std::vector<std::pair<uint32_t, std::pair<uint32_t, int64_t>>> want, got;
+      for_each_run(R0, R1, Hl, st, sh, rb, [&](uint32_t i, uint32_t n, int64_t off) { want.push_back({i, {n, off}}); });
+      for (uint32_t lanes : {32u, 7u, 1u})
+        for (uint32_t min_split : {1u, 17u, 1000u}) {
+          got.clear();
+          for (uint32_t lane = 0; lane < lanes; ++lane)
+            for_each_run_lane(R0, R1, Hl, st, sh, rb, lane, lanes, min_split,
+                              [&](uint32_t i, uint32_t n, int64_t off) { got.push_back({i, {n, off}}); });
+          std::sort(got.begin(), got.end());
+          if (got != want) ++bad;
+          ++lane_checks;
+        }
     }
   }
   // a row larger than a stage is refused
   if (tma_rows_per_unit(4, kStageBytes + 16) != 0) ++bad;
-  std::printf("%ld %ld\n", bad, cases);
+  std::printf("%ld %ld %ld\n", bad, cases, lane_checks);
   return bad != 0;
 }
 '''
@@ -63,6 +80,6 @@ def test_staged_plan_runs_tile_units_exactly(tmp_path):
     exe = tmp_path / "plan"
     subprocess.run(["g++", "-O2", "-std=c++17", f"-I{CSRC}", str(src), "-o", str(exe)], check=True)
     r = subprocess.run([str(exe)], capture_output=True, text=True)
-    bad, cases = r.stdout.split()
+    bad, cases, lane_checks = r.stdout.split()
     assert r.returncode == 0 and bad == "0", r.stdout
-    assert int(cases) > 10000
+    assert int(cases) > 10000 and int(lane_checks) > 10000

@@ -157,14 +157,32 @@ class _DeviceBuffer:
                                          "version": 2, "strides": None}
 
 
+# Flat tensors over library-owned memory, by (address, elements, dtype, device).
+# Cached targets come back at the same addresses call after call, so their views
+# are cut from a cached flat tensor instead of being built from the array
+# interface each time; a view owns no memory, so an entry whose memory was freed
+# and reused still views exactly that address range.
+_WRAP_CACHE = {}
+_WRAP_CACHE_MAX = 4096
+
+
 def _wrap(ptr, shape, dtype, device):
     if not ptr or 0 in shape:
         return torch.empty(shape, dtype=dtype, device=device)
-    esize = torch.empty((), dtype=dtype).element_size()
-    typestr = {1: "|u1", 2: "<i2", 4: "<i4", 8: "<i8"}[esize]
-    with torch.cuda.device(device):
-        t = torch.as_tensor(_DeviceBuffer(ptr, shape, typestr), device=device)
-    return t.view(dtype)
+    numel = 1
+    for n in shape:
+        numel *= n
+    key = (ptr, numel, dtype, device)
+    flat = _WRAP_CACHE.get(key)
+    if flat is None:
+        esize = torch.empty((), dtype=dtype).element_size()
+        typestr = {1: "|u1", 2: "<i2", 4: "<i4", 8: "<i8"}[esize]
+        with torch.cuda.device(device):
+            flat = torch.as_tensor(_DeviceBuffer(ptr, (numel,), typestr), device=device).view(dtype)
+        if len(_WRAP_CACHE) >= _WRAP_CACHE_MAX:
+            _WRAP_CACHE.clear()
+        _WRAP_CACHE[key] = flat
+    return flat.view(shape)
 
 
 def _dtype_code(dtype):

@@ -5,13 +5,15 @@
 // "Communication Architecture", "Sequence Parallel Communication / Ulysses"),
 // organised around the Blackwell bulk-copy engine instead of per-lane loads:
 //
-//  * Persistent grid, one CTA (one warp) per SM.  One lane issues
+//  * Persistent grid, one CTA (one warp) per SM.  The warp issues
 //    cp.async.bulk global->shared loads for a unit (a row range of one plane,
 //    <= 32 KiB, see tma_plan.h) into a ring of shared-memory stages, a few units
 //    ahead, each completing on the stage's mbarrier with a transaction count;
 //    it then issues the unit's bulk shared->global stores and reuses a stage
-//    only after the store's reads of it have finished
-//    (cp.async.bulk.wait_group.read).  The data never enters registers.
+//    only after the stores' reads of it have finished
+//    (cp.async.bulk.wait_group.read).  A unit's copies (one per contiguous run:
+//    a token's head band, a head row, or the whole unit) are spread over the 32
+//    lanes.  The data never enters registers.
 //  * Every wait is bounded (clock64 budget).  A wait that gives up sets a bit in
 //    a device status word and a shared abort flag; the kernel then drains the
 //    copies it issued (bounded as well) and returns.  No trap, no endless loop.
@@ -25,6 +27,19 @@
 #endif
 #ifndef TFU_LAG
 #define TFU_LAG 2  // copy kernel: units loaded ahead of the store
+#endif
+// A unit's loads are spread over the warp's lanes from this many runs up, its
+// stores from this many up (fewer go from lane 0 in order).  Measured on GB300
+// (fractions of the copy peak): spreading loads gains at every run size (1.5 KiB
+// bands 0.91 against 0.63 from one lane; 2 KiB 0.94 against 0.79); spreading
+// stores gains from 16 runs per unit (21 runs of 1.5 KiB: 0.85 against 0.67; 16
+// of 2 KiB: 0.84-0.96 against 0.78-0.91) and loses below (the video-DiT gather's
+// 12 runs of 2.5 KiB: 0.91 against 0.93; 10 of 3 KiB: 0.84 against 0.87).
+#ifndef TFU_LOAD_SPLIT_RUNS
+#define TFU_LOAD_SPLIT_RUNS 1
+#endif
+#ifndef TFU_STORE_SPLIT_RUNS
+#define TFU_STORE_SPLIT_RUNS 16
 #endif
 
 namespace tfu {
@@ -150,14 +165,19 @@ __device__ __forceinline__ Unit decode_unit(const RelayoutParams& p, uint32_t u)
     return un;
 }
 
-// The data-movement lane: for each of this CTA's units k, load it kLag units
-// ahead of its store.  Barrier protocol: full[s] completes once per unit loaded
-// into stage s (arrive + bytes); the store of unit j waits full[j % kStages] for
-// the phase of j, so every phase is observed in order; a stage is reloaded only
-// after the store that last read it has finished reading (bulk wait_group.read).
+// The data-movement warp: for each of this CTA's units k, load it kLag units
+// ahead of its store.  The bulk copies of a unit made of many small runs are
+// dealt out to the 32 lanes (for_each_run_lane: one copy per token band or row),
+// so they are not bound by one lane's issue rate.  Barrier protocol: full[s]
+// completes once per unit loaded into stage s (lane 0's arrive + the bytes of
+// every lane's loads); the store of unit j waits full[j % kStages] for the phase
+// of j (every lane observes it), so every phase is observed in order; each lane
+// commits one bulk group per unit stored, and a stage is reloaded only after every
+// lane's stores that last read it have finished reading (each lane's bulk
+// wait_group.read, then a warp barrier).
 template <Dir kDir>
 __device__ void copy_dma_loop(const RelayoutParams& p, uint8_t* ring, uint64_t* full, volatile int* abort_flag,
-                              uint32_t n_my) {
+                              uint32_t n_my, uint32_t lane) {
     using R = CopyRing;
     const uint32_t rb = p.row_bytes;
     uint32_t issued = 0, consumed = 0;
@@ -166,26 +186,29 @@ __device__ void copy_dma_loop(const RelayoutParams& p, uint8_t* ring, uint64_t* 
         if (k < n_my) {
             const uint32_t s = k % R::kStages;
             const Unit un = decode_unit<kDir>(p, blockIdx.x + k * gridDim.x);
-            // stage s last held unit k - kStages, whose store was committed
-            // kStages - kLag - 1 groups ago: wait until it has read the stage
+            // stage s last held unit k - kStages, whose stores were committed
+            // kStages - kLag - 1 groups ago: wait until they have read the stage
             if (k >= uint32_t(R::kStages)) bulk_wait_read<R::kStages - R::kLag - 1>();
+            __syncwarp();
             uint8_t* stage = ring + size_t(s) * R::kStride;
-            mbar_arrive_expect_tx(&full[s], (un.R1 - un.R0) * rb);
-            for_each_run(un.R0, un.R1, p.Hl, un.pl.st, un.pl.sh, rb, [&](uint32_t i, uint32_t n, int64_t off) {
-                bulk_load(stage + size_t(i) * rb, un.pl.src + off, n * rb, &full[s]);
-            });
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], (un.R1 - un.R0) * rb);
+            for_each_run_lane(un.R0, un.R1, p.Hl, un.pl.st, un.pl.sh, rb, lane, 32u, TFU_LOAD_SPLIT_RUNS,
+                              [&](uint32_t i, uint32_t n, int64_t off) {
+                                  bulk_load(stage + size_t(i) * rb, un.pl.src + off, n * rb, &full[s]);
+                              });
             issued = k + 1;
         }
         if (k >= uint32_t(R::kLag)) {
             const uint32_t j = k - R::kLag;
             const uint32_t s = j % R::kStages;
             const Unit un = decode_unit<kDir>(p, blockIdx.x + j * gridDim.x);
-            ok = bounded_wait(&full[s], (j / R::kStages) & 1u, abort_flag, kStatusLoadWait);
+            ok = __all_sync(0xffffffffu, bounded_wait(&full[s], (j / R::kStages) & 1u, abort_flag, kStatusLoadWait));
             if (!ok) break;
             const uint8_t* stage = ring + size_t(s) * R::kStride;
-            for_each_run(un.R0, un.R1, p.Hl, un.pl.dt, un.pl.dh, rb, [&](uint32_t i, uint32_t n, int64_t off) {
-                bulk_store(un.pl.dst + off, stage + size_t(i) * rb, n * rb);
-            });
+            for_each_run_lane(un.R0, un.R1, p.Hl, un.pl.dt, un.pl.dh, rb, lane, 32u, TFU_STORE_SPLIT_RUNS,
+                              [&](uint32_t i, uint32_t n, int64_t off) {
+                                  bulk_store(un.pl.dst + off, stage + size_t(i) * rb, n * rb);
+                              });
             bulk_commit();
             consumed = j + 1;
         }
@@ -194,6 +217,7 @@ __device__ void copy_dma_loop(const RelayoutParams& p, uint8_t* ring, uint64_t* 
     if (!ok) {  // drain the loads still in flight into this CTA's shared memory
         for (uint32_t j = consumed; j < issued; ++j) drain_wait(&full[j % R::kStages], (j / R::kStages) & 1u);
     }
+    __syncwarp();
 }
 
 // Pure relayout (copy scatter, gather): one warp, one ring, all units.
@@ -203,12 +227,15 @@ __global__ void __launch_bounds__(32, 1) copy_staged_kernel(const __grid_constan
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(R::kStages) * R::kStride);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(full + R::kStages);
-    if (threadIdx.x != 0) return;
-    for (int s = 0; s < R::kStages; ++s) mbar_init(&full[s], 1);
-    *abort_flag = 0;
-    fence_barrier_init();
+    const uint32_t lane = threadIdx.x;
+    if (lane == 0) {
+        for (int s = 0; s < R::kStages; ++s) mbar_init(&full[s], 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncwarp();
     const uint32_t n_my = blockIdx.x < p.n_units ? (p.n_units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-    copy_dma_loop<kDir>(p, smem, full, abort_flag, n_my);
+    copy_dma_loop<kDir>(p, smem, full, abort_flag, n_my, lane);
 }
 
 template <Dir kDir>

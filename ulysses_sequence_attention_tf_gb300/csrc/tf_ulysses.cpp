@@ -217,16 +217,25 @@ tf_status plan_units(RelayoutParams& p, const Shape& sh) {
 #ifndef TFU_COPY_BLOCKS
 #define TFU_COPY_BLOCKS 0  // the same single pass for copy scatters (else the staged kernel)
 #endif
+#ifndef TFU_SMALL_BAND
+// Token head bands (Hl * D * esize bytes) up to this size take the register paths
+// for pure relayouts: the block kernel for copy scatters, the register kernel for
+// gathers (measured on GB300: 768-byte bands gather at 0.77-0.78 of the copy peak
+// by registers against 0.58 by bulk copies, and scatter at 0.85-0.86 against 0.73).
+#define TFU_SMALL_BAND 1024
+#endif
+constexpr uint64_t kSmallBandBytes = TFU_SMALL_BAND;
 #ifndef TFU_BLOCK_PASSES
 #define TFU_BLOCK_PASSES 0  // pipeline passes per row group and unit of the block kernel; 0: by slot count
 #endif
 
 // Plan and launch one relayout:
 //  * scatters with 32-byte vectors and D * esize in {64, 128, 256, 512} bytes
-//    (fused always; copies into the fused receive layout, or all copies when
-//    TFU_COPY_BLOCKS): the block kernel, all slots of a token block in one pass;
-//  * other pure relayouts whose head row fits a stage: the shared-memory-staged
-//    (bulk-copy) kernel;
+//    (fused always; copies into the fused receive layout, copies whose token head
+//    band is small, or all copies when TFU_COPY_BLOCKS): the block kernel, all
+//    slots of a token block in one pass;
+//  * other pure relayouts whose head row fits a stage, except gathers of small
+//    bands or 128-byte rows: the shared-memory-staged (bulk-copy) kernel;
 //  * the rest: the register kernel with 32- or 16-byte vectors.
 tf_status launch_planned(RelayoutParams& p, const Shape& sh, tfu::Dir dir, tfu::Fused fused, int64_t src_tokens,
                          int64_t dst_tokens, cudaStream_t stream) {
@@ -260,8 +269,15 @@ tf_status launch_planned(RelayoutParams& p, const Shape& sh, tfu::Dir dir, tfu::
         dst_rows_packed = dst_rows_packed && p.d_h[x] == int64_t(rb);
         dst_shared = dst_shared && p.d_t[x] == p.d_t[0] && p.d_h[x] == p.d_h[0];
     }
+    // a token's head band: the contiguous piece of the strided side (the scatter's
+    // source, the gather's destination); the bulk-copy engine moves pieces of a KiB
+    // or less, and gathers of 128-byte rows, slower than the register paths
+    const bool small_band = uint64_t(sh.Hl) * rb <= kSmallBandBytes;
     const bool block_ok = dir == tfu::Dir::kScatter && dst_shared && (rb == 64 || rb == 128 || rb == 256 || rb == 512) &&
-                          (fused != tfu::Fused::kNone ? TFU_FUSED_BLOCKS : (TFU_COPY_BLOCKS || !dst_rows_packed));
+                          (fused != tfu::Fused::kNone ? TFU_FUSED_BLOCKS
+                                                      : (TFU_COPY_BLOCKS || !dst_rows_packed || small_band));
+    const bool staged_ok = TFU_USE_STAGED && fused == tfu::Fused::kNone &&
+                           !(dir == tfu::Dir::kGather && (small_band || rb <= 128));
     const uint32_t vec = pick_vec_bytes(p, sh, src_tokens, dst_tokens);
     const uint32_t rpu = tfu::tma_rows_per_unit(uint32_t(sh.Hl), rb);
     if (block_ok && vec == 32) {
@@ -274,7 +290,7 @@ tf_status launch_planned(RelayoutParams& p, const Shape& sh, tfu::Dir dir, tfu::
         const uint32_t unit_rows = uint32_t(tfu::kThreads) / p.vpr * depth * passes;
         if ((s = plan_rows(uint64_t(sh.B) * sh.P * sh.P, unit_rows)) != TF_OK) return s;
         e = tfu::launch_blocks(p, fused, stream);
-    } else if (TFU_USE_STAGED && rpu > 0 && fused == tfu::Fused::kNone) {
+    } else if (staged_ok && rpu > 0) {
         if ((s = plan_rows(uint64_t(sh.B) * sh.P * p.nx * sh.P, rpu)) != TF_OK) return s;
         e = tfu::launch_relayout_staged(p, dir, fused, stream);
     } else {

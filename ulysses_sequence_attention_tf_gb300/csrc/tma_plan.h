@@ -59,4 +59,41 @@ __host__ __device__ inline void for_each_run(uint32_t R0, uint32_t R1, uint32_t 
     }
 }
 
+// The runs of for_each_run(R0, R1, ...) dealt out to `lanes` workers, for one
+// worker `lane`: a range of whole tokens with packed heads is one run per token,
+// token k to worker k % lanes; a range with unpacked heads is one run per row,
+// row i to worker i % lanes; a range of fewer than `min_split` such runs, a
+// contiguous range (one run), or any other range (a token larger than a stage,
+// cut by the unit bounds) goes to worker 0 in order.  Over all workers the runs
+// are exactly those of for_each_run.
+template <class F>
+__host__ __device__ inline void for_each_run_lane(uint32_t R0, uint32_t R1, uint32_t Hl, int64_t st, int64_t sh,
+                                                  uint32_t row_bytes, uint32_t lane, uint32_t lanes,
+                                                  uint32_t min_split, F&& f) {
+    if (R1 <= R0) return;
+    const bool heads_packed = Hl == 1 || sh == int64_t(row_bytes);
+    if (heads_packed && st == int64_t(Hl) * row_bytes) {
+        if (lane == 0) f(0u, R1 - R0, int64_t(R0) * row_bytes);
+        return;
+    }
+    if (heads_packed) {
+        const uint32_t nt = (R1 - R0) / Hl;
+        if (R0 % Hl == 0 && R1 % Hl == 0 && nt >= min_split) {
+            const uint32_t t0 = R0 / Hl;
+            for (uint32_t k = lane; k < nt; k += lanes) f(k * Hl, Hl, int64_t(t0 + k) * st);
+        } else if (lane == 0) {
+            for_each_run(R0, R1, Hl, st, sh, row_bytes, f);
+        }
+        return;
+    }
+    if (R1 - R0 < min_split) {
+        if (lane == 0) for_each_run(R0, R1, Hl, st, sh, row_bytes, f);
+        return;
+    }
+    for (uint32_t i = lane; i < R1 - R0; i += lanes) {
+        const uint32_t R = R0 + i, t = R / Hl, h = R - t * Hl;
+        f(i, 1u, int64_t(t) * st + int64_t(h) * sh);
+    }
+}
+
 }  // namespace tfu
