@@ -4,7 +4,8 @@ shared-memory stage, its bulk-copy runs tile the unit's rows exactly and in
 order, every run is really contiguous under the strides, stays inside the
 plane, and has 16-byte aligned offsets and sizes; and the same runs dealt out
 to the lanes of a warp (for_each_run_lane) are, over all lanes, exactly those
-runs."""
+runs, and no lane but the first gets a run of a side whose full units have
+fewer runs than the split threshold (unit_split_runs)."""
 import os
 import subprocess
 
@@ -63,6 +64,11 @@ int main() {
           std::sort(got.begin(), got.end());
           if (got != want) ++bad;
           ++lane_checks;
+          // a side whose full units give fewer runs than min_split stays on worker 0
+          if (unit_split_runs(rpu, Hl, st, sh, rb) < min_split)
+            for (uint32_t lane = 1; lane < lanes; ++lane)
+              for_each_run_lane(R0, R1, Hl, st, sh, rb, lane, lanes, min_split,
+                                [&](uint32_t, uint32_t, int64_t) { ++bad; });
         }
     }
   }

@@ -28,20 +28,6 @@
 #ifndef TFU_LAG
 #define TFU_LAG 2  // copy kernel: units loaded ahead of the store
 #endif
-// A unit's loads are spread over the warp's lanes from this many runs up, its
-// stores from this many up (fewer go from lane 0 in order).  Measured on GB300
-// (fractions of the copy peak): spreading loads gains at every run size (1.5 KiB
-// bands 0.91 against 0.63 from one lane; 2 KiB 0.94 against 0.79); spreading
-// stores gains from 16 runs per unit (21 runs of 1.5 KiB: 0.85 against 0.67; 16
-// of 2 KiB: 0.84-0.96 against 0.78-0.91) and loses below (the video-DiT gather's
-// 12 runs of 2.5 KiB: 0.91 against 0.93; 10 of 3 KiB: 0.84 against 0.87).
-#ifndef TFU_LOAD_SPLIT_RUNS
-#define TFU_LOAD_SPLIT_RUNS 1
-#endif
-#ifndef TFU_STORE_SPLIT_RUNS
-#define TFU_STORE_SPLIT_RUNS 16
-#endif
-
 namespace tfu {
 
 // Reasons a bounded wait gave up (bitwise OR); zero when the library loads.
@@ -165,21 +151,26 @@ __device__ __forceinline__ Unit decode_unit(const RelayoutParams& p, uint32_t u)
     return un;
 }
 
-// The data-movement warp: for each of this CTA's units k, load it kLag units
-// ahead of its store.  The bulk copies of a unit made of many small runs are
-// dealt out to the 32 lanes (for_each_run_lane: one copy per token band or row),
-// so they are not bound by one lane's issue rate.  Barrier protocol: full[s]
-// completes once per unit loaded into stage s (lane 0's arrive + the bytes of
-// every lane's loads); the store of unit j waits full[j % kStages] for the phase
-// of j (every lane observes it), so every phase is observed in order; each lane
-// commits one bulk group per unit stored, and a stage is reloaded only after every
-// lane's stores that last read it have finished reading (each lane's bulk
-// wait_group.read, then a warp barrier).
-template <Dir kDir>
+// The data-movement loop: for each of this CTA's units k, load it kLag units
+// ahead of its store.  kWarp = false: lane 0 alone issues every copy in order.
+// kWarp = true: the whole warp runs the loop, and the copies of a unit made of
+// many small runs are dealt out to the 32 lanes (for_each_run_lane: one copy per
+// token band or row), so they are not bound by one lane's issue rate; `split_st`
+// (uniform over the launch) says whether any unit deals out its stores, and only
+// then do lanes other than 0 commit and wait on bulk groups.
+// Barrier protocol: full[s] completes once per unit loaded into stage s (lane 0's
+// arrive + the bytes of every lane's loads); the store of unit j waits
+// full[j % kStages] for the phase of j (every active lane observes it), so every
+// phase is observed in order; a lane that stores commits one bulk group per unit
+// stored, and a stage is reloaded only after every store that last read it has
+// finished reading (each storing lane's bulk wait_group.read, then a warp barrier).
+template <Dir kDir, bool kWarp>
 __device__ void copy_dma_loop(const RelayoutParams& p, uint8_t* ring, uint64_t* full, volatile int* abort_flag,
-                              uint32_t n_my, uint32_t lane) {
+                              uint32_t n_my, uint32_t lane, bool split_st) {
     using R = CopyRing;
     const uint32_t rb = p.row_bytes;
+    const uint32_t lanes = kWarp ? 32u : 1u;
+    const bool stores = !kWarp || split_st || lane == 0;  // this lane may issue stores
     uint32_t issued = 0, consumed = 0;
     bool ok = true;
     for (uint32_t k = 0; ok && k < n_my + R::kLag; ++k) {
@@ -188,11 +179,11 @@ __device__ void copy_dma_loop(const RelayoutParams& p, uint8_t* ring, uint64_t* 
             const Unit un = decode_unit<kDir>(p, blockIdx.x + k * gridDim.x);
             // stage s last held unit k - kStages, whose stores were committed
             // kStages - kLag - 1 groups ago: wait until they have read the stage
-            if (k >= uint32_t(R::kStages)) bulk_wait_read<R::kStages - R::kLag - 1>();
-            __syncwarp();
+            if (k >= uint32_t(R::kStages) && stores) bulk_wait_read<R::kStages - R::kLag - 1>();
+            if constexpr (kWarp) __syncwarp();
             uint8_t* stage = ring + size_t(s) * R::kStride;
             if (lane == 0) mbar_arrive_expect_tx(&full[s], (un.R1 - un.R0) * rb);
-            for_each_run_lane(un.R0, un.R1, p.Hl, un.pl.st, un.pl.sh, rb, lane, 32u, TFU_LOAD_SPLIT_RUNS,
+            for_each_run_lane(un.R0, un.R1, p.Hl, un.pl.st, un.pl.sh, rb, lane, lanes, kLoadSplitRuns,
                               [&](uint32_t i, uint32_t n, int64_t off) {
                                   bulk_load(stage + size_t(i) * rb, un.pl.src + off, n * rb, &full[s]);
                               });
@@ -202,14 +193,15 @@ __device__ void copy_dma_loop(const RelayoutParams& p, uint8_t* ring, uint64_t* 
             const uint32_t j = k - R::kLag;
             const uint32_t s = j % R::kStages;
             const Unit un = decode_unit<kDir>(p, blockIdx.x + j * gridDim.x);
-            ok = __all_sync(0xffffffffu, bounded_wait(&full[s], (j / R::kStages) & 1u, abort_flag, kStatusLoadWait));
+            ok = bounded_wait(&full[s], (j / R::kStages) & 1u, abort_flag, kStatusLoadWait);
+            if constexpr (kWarp) ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             const uint8_t* stage = ring + size_t(s) * R::kStride;
-            for_each_run_lane(un.R0, un.R1, p.Hl, un.pl.dt, un.pl.dh, rb, lane, 32u, TFU_STORE_SPLIT_RUNS,
+            for_each_run_lane(un.R0, un.R1, p.Hl, un.pl.dt, un.pl.dh, rb, lane, lanes, kStoreSplitRuns,
                               [&](uint32_t i, uint32_t n, int64_t off) {
                                   bulk_store(un.pl.dst + off, stage + size_t(i) * rb, n * rb);
                               });
-            bulk_commit();
+            if (stores) bulk_commit();
             consumed = j + 1;
         }
     }
@@ -217,10 +209,12 @@ __device__ void copy_dma_loop(const RelayoutParams& p, uint8_t* ring, uint64_t* 
     if (!ok) {  // drain the loads still in flight into this CTA's shared memory
         for (uint32_t j = consumed; j < issued; ++j) drain_wait(&full[j % R::kStages], (j / R::kStages) & 1u);
     }
-    __syncwarp();
+    if constexpr (kWarp) __syncwarp();
 }
 
-// Pure relayout (copy scatter, gather): one warp, one ring, all units.
+// Pure relayout (copy scatter, gather): one warp, one ring, all units.  The warp
+// deals out copies only when some slot's units are made of enough runs (the
+// same decision for every CTA of the launch); otherwise lane 0 works alone.
 template <Dir kDir>
 __global__ void __launch_bounds__(32, 1) copy_staged_kernel(const __grid_constant__ RelayoutParams p) {
     using R = CopyRing;
@@ -233,9 +227,18 @@ __global__ void __launch_bounds__(32, 1) copy_staged_kernel(const __grid_constan
         *abort_flag = 0;
         fence_barrier_init();
     }
-    __syncwarp();
+    bool split_ld = false, split_st = false;
+    for (uint32_t x = 0; x < p.nx; ++x) {
+        split_ld = split_ld || unit_split_runs(p.rpu, p.Hl, p.s_t[x], p.s_h[x], p.row_bytes) >= kLoadSplitRuns;
+        split_st = split_st || unit_split_runs(p.rpu, p.Hl, p.d_t[x], p.d_h[x], p.row_bytes) >= kStoreSplitRuns;
+    }
     const uint32_t n_my = blockIdx.x < p.n_units ? (p.n_units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-    copy_dma_loop<kDir>(p, smem, full, abort_flag, n_my, lane);
+    if (!split_ld && !split_st) {
+        if (lane == 0) copy_dma_loop<kDir, false>(p, smem, full, abort_flag, n_my, 0, false);
+        return;
+    }
+    __syncwarp();  // the barriers are initialised before any lane uses them
+    copy_dma_loop<kDir, true>(p, smem, full, abort_flag, n_my, lane, split_st);
 }
 
 template <Dir kDir>

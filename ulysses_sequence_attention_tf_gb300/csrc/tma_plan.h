@@ -24,6 +24,23 @@ namespace tfu {
 
 constexpr uint32_t kStageBytes = 32768;  // bytes of one shared-memory stage
 
+// A unit's loads are dealt out to the warp's lanes from this many runs up, its
+// stores from this many up (fewer go from lane 0 in order).  Measured on GB300
+// (fractions of the copy peak): dealing out loads gains at every run size
+// (1.5 KiB bands 0.91 against 0.63 from one lane; 2 KiB 0.94 against 0.79);
+// dealing out stores gains from 16 runs per unit (21 runs of 1.5 KiB: 0.85
+// against 0.67; 16 of 2 KiB: 0.84-0.96 against 0.78-0.91) and loses below (the
+// video-DiT gather's 12 runs of 2.5 KiB: 0.91 against 0.93; 10 of 3 KiB: 0.84
+// against 0.87).
+#ifndef TFU_LOAD_SPLIT_RUNS
+#define TFU_LOAD_SPLIT_RUNS 1
+#endif
+#ifndef TFU_STORE_SPLIT_RUNS
+#define TFU_STORE_SPLIT_RUNS 16
+#endif
+constexpr uint32_t kLoadSplitRuns = TFU_LOAD_SPLIT_RUNS;
+constexpr uint32_t kStoreSplitRuns = TFU_STORE_SPLIT_RUNS;
+
 // Rows per unit: whole tokens (all Hl heads) when a token's head band fits a
 // stage, else as many rows as fit.  0 if a single row does not fit.
 __host__ __device__ inline uint32_t tma_rows_per_unit(uint32_t Hl, uint32_t row_bytes) {
@@ -94,6 +111,19 @@ __host__ __device__ inline void for_each_run_lane(uint32_t R0, uint32_t R1, uint
         const uint32_t R = R0 + i, t = R / Hl, h = R - t * Hl;
         f(i, 1u, int64_t(t) * st + int64_t(h) * sh);
     }
+}
+
+// The number of runs that for_each_run_lane can deal out for a unit of `rows`
+// rows starting at a token boundary: one per token (packed heads, whole tokens),
+// one per row (unpacked heads), or 0 where every run goes to worker 0 (a
+// contiguous side, or units that cut tokens).  No unit of at most `rows` rows has
+// more, so a side whose full units give fewer than min_split never deals out.
+__host__ __device__ inline uint32_t unit_split_runs(uint32_t rows, uint32_t Hl, int64_t st, int64_t sh,
+                                                    uint32_t row_bytes) {
+    const bool heads_packed = Hl == 1 || sh == int64_t(row_bytes);
+    if (heads_packed && st == int64_t(Hl) * row_bytes) return 0;
+    if (heads_packed) return rows % Hl == 0 ? rows / Hl : 0;
+    return rows;
 }
 
 }  // namespace tfu
