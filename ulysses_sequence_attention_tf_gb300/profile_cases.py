@@ -4,6 +4,10 @@
   python -m ulysses_sequence_attention_tf_gb300.profile_cases projection [--S 8192] [--iters 3]
   python -m ulysses_sequence_attention_tf_gb300.profile_cases scatter_fused [--S 32760] [--iters 3]
   python -m ulysses_sequence_attention_tf_gb300.profile_cases scatter_fused_qk [--S 32760] [--iters 3]
+  python -m ulysses_sequence_attention_tf_gb300.profile_cases scatter --S 4096 --H 24 --layout fused
+
+``--layout``: v_strided (Q/K contiguous, V a view into a fused projection; the
+default), fused (Q/K/V all views of one fused projection), contiguous.
 
 Inputs are the seeded synthetic ones of ``synth``; shapes default to the
 video-DiT workload's head geometry (P=4, H=40, D=128, bf16) with a smaller
@@ -20,12 +24,13 @@ from . import binding, build, synth
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("case", choices=["projection", "scatter_fused", "scatter_fused_qk", "gather"])
+    ap.add_argument("case", choices=["projection", "scatter", "scatter_fused", "scatter_fused_qk", "gather"])
     ap.add_argument("--P", type=int, default=4)
     ap.add_argument("--S", type=int, default=None, help="global tokens (default 8192 projection, 32760 others)")
     ap.add_argument("--H", type=int, default=40)
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--rope", choices=["interleaved", "neox"], default="interleaved")
+    ap.add_argument("--layout", choices=["v_strided", "fused", "contiguous"], default="v_strided")
     args = ap.parse_args(argv)
     P, H, D, B = args.P, args.H, 128, 1
     S = args.S or (8192 if args.case == "projection" else 32760)
@@ -42,13 +47,17 @@ def main(argv=None):
         def call():
             binding.project_qkv_into(xs, w, H, outs["q"], outs["k"], outs["v"], norm_rope=True, q_weight=wq,
                                      k_weight=wk, rope=args.rope)
-    elif args.case in ("scatter_fused", "scatter_fused_qk"):
-        g = synth.qkv_shards(P, B, Sl, H, D, torch.bfloat16, seed=0, layout="v_strided", device=dev)
-        v = g["v"] if args.case == "scatter_fused" else None  # Q/K only: V moves elsewhere
+    elif args.case in ("scatter", "scatter_fused", "scatter_fused_qk"):
+        g = synth.qkv_shards(P, B, Sl, H, D, torch.bfloat16, seed=0, layout=args.layout, device=dev)
+        v = None if args.case == "scatter_fused_qk" else g["v"]  # Q/K only: V moves elsewhere
+        fused = args.case != "scatter"
 
         def call():
-            binding.scatter_qkv("profile", g["q"], g["k"], v, norm_rope=True, q_weight=wq, k_weight=wk,
-                                rope=args.rope)
+            if fused:
+                binding.scatter_qkv("profile", g["q"], g["k"], v, norm_rope=True, q_weight=wq, k_weight=wk,
+                                    rope=args.rope)
+            else:
+                binding.scatter_qkv("profile", g["q"], g["k"], v)
     else:
         attn = synth.attn_outputs(P, B, S, Hl, D, torch.bfloat16, seed=0, device=dev)
 

@@ -16,10 +16,14 @@ Every point prints one JSON line:
     the fused points add the cos/sin rows and the RMSNorm weights);
   * the median and best over ``--iters`` CUDA-event-timed replays (after
     ``--warmup``) of a CUDA graph holding the call, so that the GPU's time is
-    measured rather than the host's per-call work, without and with an L2 flush
-    (a 256 MiB write) before each replay; and the eager calls' flushed median;
+    measured rather than the host's per-call work: without a flush, after an L2
+    flush by writing 256 MiB, and after one by reading 256 MiB; and the eager
+    calls' median after the write flush.  The write flush leaves L2 full of
+    dirty lines, so the timed launch also pays for writing back up to the L2's
+    size of the flush's data; the read flush leaves clean lines, so the launch
+    starts from a cold L2 and owes nothing.  The gate uses the read flush;
   * the fraction of the measured HBM copy peak, and for messages of 64 MiB or more
-    whether the flushed median clears 0.8 of it;
+    whether the read-flushed median clears 0.8 of it (and the write-flushed one);
   * the same measurement of one contiguous copy of the same bytes by the
     library's bulk-copy kernel (the ceiling at that size, launch, fill and drain
     included).
@@ -77,6 +81,16 @@ def _cudart():
 class Timer:
     def __init__(self, iters, warmup, flush_buf):
         self.iters, self.warmup, self.flush_buf = iters, warmup, flush_buf
+        self.flush_sink = torch.empty((), dtype=torch.int64, device=flush_buf.device)
+
+    def flush(self, mode):
+        """Evict L2 before a timed launch.  "write": write a 256 MiB buffer (L2 is then
+        full of dirty lines, whose write-back the timed launch pays for); "read": read
+        it (L2 is left holding clean lines, so the launch starts cold and owes nothing)."""
+        if mode == "write":
+            self.flush_buf.zero_()
+        elif mode == "read":
+            torch.sum(self.flush_buf.view(torch.int64), dim=0, out=self.flush_sink)
 
     def run(self, fn, flush):
         for _ in range(self.warmup):
@@ -84,8 +98,7 @@ class Timer:
         torch.cuda.synchronize()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(self.iters)]
         for a, b in ev:
-            if flush:
-                self.flush_buf.zero_()
+            self.flush(flush)
             a.record()
             fn()
             b.record()
@@ -118,13 +131,16 @@ def _stats(timer, fn, nbytes, peak):
     except Exception:  # a call that cannot be captured is timed eagerly, and says so
         torch.cuda.synchronize()
         g, replay, timing = None, fn, "eager"
-    med, best = timer.run(replay, flush=False)
-    fmed, fbest = timer.run(replay, flush=True)
-    emed, _ = timer.run(fn, flush=True)
+    med, best = timer.run(replay, flush=None)
+    fmed, fbest = timer.run(replay, flush="write")
+    rmed, rbest = timer.run(replay, flush="read")
+    emed, _ = timer.run(fn, flush="write")
     del g
     return {"gbs_median": _gbs(nbytes, med), "gbs_best": _gbs(nbytes, best),
             "gbs_median_flushed": _gbs(nbytes, fmed), "gbs_best_flushed": _gbs(nbytes, fbest),
             "frac_median_flushed": _gbs(nbytes, fmed) / peak, "ms_median": med, "ms_median_flushed": fmed,
+            "gbs_median_read_flushed": _gbs(nbytes, rmed), "gbs_best_read_flushed": _gbs(nbytes, rbest),
+            "frac_median_read_flushed": _gbs(nbytes, rmed) / peak,
             "eager_gbs_median_flushed": _gbs(nbytes, emed), "timing": timing}
 
 
@@ -200,7 +216,7 @@ def same_size_copy(timer, nbytes, peak):
     b = torch.empty_like(a)
     st = _stats(timer, lambda: binding.exchange_chunks([a], [b]), 2 * half, peak)
     del a, b
-    return st["gbs_median_flushed"]
+    return st["gbs_median_flushed"], st["gbs_median_read_flushed"]
 
 
 # ---------------------------------------------------------------- points
@@ -233,10 +249,12 @@ def point_relayout(name, timer, peak, cudart, P, B, S, H, D, dtype, ntensors, di
            "dtype": str(dtype).replace("torch.", ""), "tensors": ntensors, "bytes": nbytes,
            "bytes_per_direction": nbytes // 2}
     rec.update(_stats(timer, ours, nbytes, peak))
-    rec["contiguous_copy_gbs_median_flushed"] = same_size_copy(timer, nbytes, peak)
+    rec["contiguous_copy_gbs_median_flushed"], rec["contiguous_copy_gbs_median_read_flushed"] = \
+        same_size_copy(timer, nbytes, peak)
     gated = nbytes // 2 >= GATE_BYTES
-    rec["gate"] = f">= {GATE_FRAC} of peak (flushed median)" if gated else None
-    rec["pass"] = (rec["frac_median_flushed"] >= GATE_FRAC) if gated else None
+    rec["gate"] = f">= {GATE_FRAC} of peak (read-flushed median)" if gated else None
+    rec["pass"] = (rec["frac_median_read_flushed"] >= GATE_FRAC) if gated else None
+    rec["pass_write_flushed"] = (rec["frac_median_flushed"] >= GATE_FRAC) if gated else None
     if with_baselines:
         if direction == "scatter":
             dsts = [[torch.empty((B, S, Hl, D), dtype=dtype, device=dev) for _ in range(P)] for _ in srcs]
@@ -266,10 +284,12 @@ def point_fused(name, timer, peak, P, B, S, H, D, dtype, layout, seed=0):
            "dtype": str(dtype).replace("torch.", ""), "tensors": 3, "layout": layout, "bytes": nbytes,
            "bytes_per_direction": nbytes // 2}
     rec.update(_stats(timer, ours, nbytes, peak))
-    rec["contiguous_copy_gbs_median_flushed"] = same_size_copy(timer, nbytes, peak)
+    rec["contiguous_copy_gbs_median_flushed"], rec["contiguous_copy_gbs_median_read_flushed"] = \
+        same_size_copy(timer, nbytes, peak)
     gated = nbytes // 2 >= GATE_BYTES
-    rec["gate"] = f">= {GATE_FRAC} of peak (flushed median)" if gated else None
-    rec["pass"] = (rec["frac_median_flushed"] >= GATE_FRAC) if gated else None
+    rec["gate"] = f">= {GATE_FRAC} of peak (read-flushed median)" if gated else None
+    rec["pass"] = (rec["frac_median_read_flushed"] >= GATE_FRAC) if gated else None
+    rec["pass_write_flushed"] = (rec["frac_median_flushed"] >= GATE_FRAC) if gated else None
     emit(rec)
     del g
     binding.cache_clear()
@@ -332,7 +352,8 @@ def main(argv=None):
                                                base and S >= 2048))
     gated = [r for r in recs if r["pass"] is not None]
     emit({"summary": {"points": len(recs), "gated_points": len(gated), "gated_pass": sum(r["pass"] for r in gated),
-                      "min_frac_gated": min((r["frac_median_flushed"] for r in gated), default=None),
+                      "gated_pass_write_flushed": sum(r["pass_write_flushed"] for r in gated),
+                      "min_frac_gated": min((r["frac_median_read_flushed"] for r in gated), default=None),
                       "peak_gbs": peak, "peak_source": peak_src, "sm_clock_mhz_now_max": sm_clock(),
                       "iters": args.iters, "warmup": args.warmup}})
 
