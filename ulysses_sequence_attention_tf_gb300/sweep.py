@@ -27,7 +27,8 @@ Every point prints one JSON line:
   * the same measurement of one contiguous copy of the same bytes by the
     library's bulk-copy kernel (the ceiling at that size, launch, fill and drain
     included).
-For the pure relayouts it also prints the same movement done by:
+For the pure relayouts it also prints the same movement (medians after either
+flush, and whether the call could be captured in a graph) done by:
   * ``torch_copy``: a strided ``copy_`` per (shard, head group) and tensor;
   * ``torch_permute``: ``stack`` of the shards, then ``permute(...).contiguous()``;
   * ``memcpy2d``: ``cudaMemcpy2DAsync`` per (shard, head group, batch) and tensor.
@@ -182,7 +183,8 @@ def baselines(timer, tensors_src, tensors_dst, P, B, Sl, Hl, D, direction, nbyte
                 torch.stack(src).view(P, B, P, Sl, Hl, D).permute(2, 1, 3, 0, 4, 5).contiguous()
 
     def keep(st):
-        return st["gbs_median_flushed"] if st["timing"] == "graph" else {"eager": st["gbs_median_flushed"]}
+        return {"read_flushed": st["gbs_median_read_flushed"], "write_flushed": st["gbs_median_flushed"],
+                "timing": st["timing"]}
 
     out["torch_copy"] = keep(_stats(timer, torch_copy, nbytes, peak))
     out["torch_permute"] = keep(_stats(timer, torch_permute, nbytes, peak))
@@ -260,7 +262,7 @@ def point_relayout(name, timer, peak, cudart, P, B, S, H, D, dtype, ntensors, di
             dsts = [[torch.empty((B, S, Hl, D), dtype=dtype, device=dev) for _ in range(P)] for _ in srcs]
         else:
             dsts = [[torch.empty((B, Sl, H, D), dtype=dtype, device=dev) for _ in range(P)] for _ in srcs]
-        rec["baselines_gbs_median_flushed"] = baselines(timer, srcs, dsts, P, B, Sl, Hl, D, direction, nbytes, peak,
+        rec["baselines_gbs_median"] = baselines(timer, srcs, dsts, P, B, Sl, Hl, D, direction, nbytes, peak,
                                                         cudart)
         del dsts
     emit(rec)
