@@ -227,8 +227,8 @@ TF_API tf_status tf_ulysses_scatter_qkv_into(const void *const *q, const void *c
  * budget reserved up front (another allocator already owns the GPU's free
  * memory, so a cudaMalloc may fail or break that accounting), and latency-bound
  * loops where the implicit device synchronisation of cudaMalloc/cudaFree is not
- * acceptable.  The paper has no counterpart; this is an interface of this
- * library only.
+ * acceptable.  None of the cited pages describes a counterpart; this is an
+ * interface of this library only.
  *
  * Arguments, layouts and errors are those of tf_ulysses_scatter_qkv_into; the
  * caller passes the inputs and the targets.  When mode is
