@@ -130,3 +130,66 @@ def test_random_case_vs_oracle(tf, case):
             outside = torch.cat([got_full[:, :, :h0], got_full[:, :, h1:]], dim=2)
             if outside.numel():
                 assert bool((outside == fill).all()), (c, key, gi)
+
+
+N_GATHER = 60
+
+
+def _draw_gather(rng):
+    dtype = rng.choice([torch.bfloat16, torch.float16, torch.bfloat16, torch.float32, torch.uint8])
+    esize = torch.empty((), dtype=dtype).element_size()
+    sizes = [d for d in (8, 16, 24, 32, 48, 64, 96, 128, 256) if (d * esize) % 16 == 0]
+    D = rng.choice(sizes) if rng.random() < 0.4 else rng.choice([d for d in sizes if d * esize >= 256] or sizes)
+    P = rng.randint(1, 8)
+    Hl = rng.randint(1, 12)
+    Sl = rng.choice([1, 7, 33, 64, 129, rng.randint(1, 200)])
+    if rng.random() < 0.3:  # head bands of 1-2 KiB over many tokens: bulk copies with stores dealt to lanes
+        rb = rng.choice([r for r in (256, 512) if r // esize in sizes] or [D * esize])
+        D = rb // esize
+        Hl = rng.randint(1024 // rb + 1, max(1024 // rb + 1, 2048 // rb))
+        Sl = rng.randint(16, 200)
+    return dict(P=P, B=rng.randint(1, 3), Sl=Sl, Hl=Hl, D=D, dtype=dtype, src=rng.choice(["contiguous", "padded"]),
+                out=rng.choice(["cached", "own", "padded"]))
+
+
+@pytest.mark.parametrize("case", range(N_GATHER))
+def test_random_gather_vs_oracle(tf, case):
+    """Head->sequence gather over random shapes, element types and strides: the
+    host picks the register or the bulk-copy kernel by the size of the shards'
+    head bands, and the bulk-copy kernel deals its stores out to the warp's lanes
+    for units of many runs; every choice must give the oracle's bits."""
+    rng = random.Random(3000 + case)
+    c = _draw_gather(rng)
+    P, B, Sl, Hl, D, dtype = c["P"], c["B"], c["Sl"], c["Hl"], c["D"], c["dtype"]
+    S, H = P * Sl, P * Hl
+    esize = torch.empty((), dtype=dtype).element_size()
+    pad = 16 // esize
+    gen = torch.Generator().manual_seed(4000 + case)
+
+    def block(shape):
+        if dtype == torch.uint8:
+            return torch.randint(0, 256, shape, generator=gen, dtype=torch.uint8)
+        return torch.randn(shape, generator=gen).to(dtype)
+
+    if c["src"] == "padded":  # head rows padded: a strided view
+        attn = [block((B, S, Hl, D + pad))[..., :D] for _ in range(P)]
+    else:
+        attn = [block((B, S, Hl, D)) for _ in range(P)]
+    g_attn = []
+    for t in attn:
+        base = torch.empty(t.untyped_storage().nbytes() // t.element_size(), dtype=dtype, device="cuda")
+        g_attn.append(torch.as_strided(base, t.shape, t.stride()).copy_(t))
+    want = oracle.gather(attn, P)
+    fill = 5 if dtype == torch.uint8 else -2
+    if c["out"] == "cached":
+        outs, _ = tf.gather_out(f"fuzz_gather_{case}", g_attn)
+    else:
+        width = H * D + (pad if c["out"] == "padded" else 0)  # padded token rows
+        slabs = [torch.full((B, Sl, width), fill, dtype=dtype, device="cuda") for _ in range(P)]
+        outs = [s[..., :H * D].unflatten(-1, (H, D)) for s in slabs]
+        tf.gather_out(f"fuzz_gather_{case}", g_attn, outs)
+    torch.cuda.synchronize()
+    for r in range(P):
+        assert bits_equal(outs[r].cpu(), want[r]), (c, r)
+        if c["out"] == "padded":
+            assert bool((slabs[r][..., H * D:] == fill).all()), (c, r)
