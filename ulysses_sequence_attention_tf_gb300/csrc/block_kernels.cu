@@ -58,6 +58,15 @@ __host__ __device__ constexpr int block_min_blocks() {
     return kNF == 0 ? TFU_COPY_BLOCK_MIN_BLOCKS : (kCopy == 0 ? TFU_QK_MIN_BLOCKS : TFU_FUSED_MIN_BLOCKS);
 }
 
+#ifndef TFU_BLOCK_SMEM_WEIGHTS
+// 1: each fused slot's RMSNorm weights by lane position in 512 bytes of shared
+// memory rather than 16 registers per lane -- the V+Q+K kernel then fits 126
+// registers without spilling (128 with 24 bytes spilled from registers), and
+// measured 6432-6452 GB/s fused (6383), 6336-6340 half-split (6182) on the
+// video-DiT scatter.  0: registers.
+#define TFU_BLOCK_SMEM_WEIGHTS 1
+#endif
+
 template <Fused kF, int kLanes, int kCopy, int kNF, bool kNeox>
 __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
     block_kernel(const __grid_constant__ RelayoutParams p) {
@@ -101,15 +110,34 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
         st_stream<16>(row, lo);
         st_stream<16>(row + kHalf, hi);
     };
-    uint32_t w[kNF > 0 ? kNF : 1][NP];  // this lane's weight pairs of each fused slot
+#if TFU_BLOCK_SMEM_WEIGHTS
+    // the weight pairs of each fused slot by lane position, in shared memory
+    __shared__ uint32_t w_all[kNF > 0 ? kNF : 1][kLanes][NP];
+    if (threadIdx.x < kLanes) {
+        const uint32_t lp = threadIdx.x;
+#pragma unroll
+        for (int f = 0; f < kNF; ++f) {
+            const uint8_t* wrow = static_cast<const uint8_t*>(p.weight[kCopy + f]);
+            const uint4 a = *reinterpret_cast<const uint4*>(wrow + (kNeox ? lp * 16 : lp * VW));
+            const uint4 b = *reinterpret_cast<const uint4*>(wrow + (kNeox ? kHalf + lp * 16 : lp * VW + 16));
+            w_all[f][lp][0] = a.x, w_all[f][lp][1] = a.y, w_all[f][lp][2] = a.z, w_all[f][lp][3] = a.w;
+            w_all[f][lp][4] = b.x, w_all[f][lp][5] = b.y, w_all[f][lp][6] = b.z, w_all[f][lp][7] = b.w;
+        }
+    }
+    __syncthreads();
+    auto w = [&](int f) -> const uint32_t(&)[NP] { return w_all[f][dv]; };
+#else
+    uint32_t w_reg[kNF > 0 ? kNF : 1][NP];  // this lane's weight pairs of each fused slot
 #pragma unroll
     for (int f = 0; f < kNF; ++f) {
         const uint8_t* wrow = static_cast<const uint8_t*>(p.weight[kCopy + f]);
         const uint4 a = *reinterpret_cast<const uint4*>(wrow + (kNeox ? dv * 16 : dv * VW));
         const uint4 b = *reinterpret_cast<const uint4*>(wrow + (kNeox ? kHalf + dv * 16 : dv * VW + 16));
-        w[f][0] = a.x, w[f][1] = a.y, w[f][2] = a.z, w[f][3] = a.w;
-        w[f][4] = b.x, w[f][5] = b.y, w[f][6] = b.z, w[f][7] = b.w;
+        w_reg[f][0] = a.x, w_reg[f][1] = a.y, w_reg[f][2] = a.z, w_reg[f][3] = a.w;
+        w_reg[f][4] = b.x, w_reg[f][5] = b.y, w_reg[f][6] = b.z, w_reg[f][7] = b.w;
     }
+    auto w = [&](int f) -> const uint32_t(&)[NP] { return w_reg[f]; };
+#endif
 #pragma unroll 1
     for (uint32_t u = blockIdx.x; u < p.n_units; u += gridDim.x) {
         const uint32_t c = fastdiv(u, p.div_planes);
@@ -163,9 +191,9 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
 #pragma unroll
                 for (int f = 0; f < kNF; ++f) {
                     if constexpr (kNeox) {
-                        norm_rope_core_split<kF, kLanes, NP>(buf[kCopy + f].w, w[f], cs, p.eps);
+                        norm_rope_core_split<kF, kLanes, NP>(buf[kCopy + f].w, w(f), cs, p.eps);
                     } else {
-                        norm_rope_core<kF, kLanes, NP>(buf[kCopy + f].w, w[f], cs, p.eps);
+                        norm_rope_core<kF, kLanes, NP>(buf[kCopy + f].w, w(f), cs, p.eps);
                     }
                 }
             }
