@@ -10,6 +10,9 @@ Configurations (seeded synthetic inputs from ``synth``):
       of P: Q/K/V scatter and the output gather (one tensor, as the attention output)
   C5  bf16, P in {2,4,8}, D=128, H=32, B=1, one tensor, 64 KiB .. 2 GiB per direction
       (S = 8, 32, .., 131072 and 262144): scatter and gather
+  F   the fused scatter across shapes: P in {2,4,8} x D in {64,128} x {bf16, fp16},
+      H=48, B=1, S=32760 padded to a multiple of P, V a view into a fused projection,
+      RMSNorm + interleaved RoPE on Q/K
 
 Every point prints one JSON line:
   * GB/s over algorithmic bytes (each payload element read once and written once;
@@ -312,7 +315,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--only", default=None, help="comma-separated subset of C1..C5")
+    ap.add_argument("--only", default=None, help="comma-separated subset of C1..C5, F")
     ap.add_argument("--no-baselines", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3 or args.iters < 20:
@@ -325,7 +328,7 @@ def main(argv=None):
     peak, peak_src = measured_peak()
     timer = Timer(args.iters, args.warmup, torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda"))
     cudart = None if args.no_baselines else _cudart()
-    only = set(args.only.split(",")) if args.only else {"C1", "C2", "C3", "C4", "C5"}
+    only = set(args.only.split(",")) if args.only else {"C1", "C2", "C3", "C4", "C5", "F"}
     base = not args.no_baselines
     recs = []
     bf16, fp16 = torch.bfloat16, torch.float16
@@ -352,6 +355,11 @@ def main(argv=None):
                 for d in ("scatter", "gather"):
                     recs.append(point_relayout("C5", timer, peak, cudart, P, 1, S, 32, 128, bf16, 1, d,
                                                base and S >= 2048))
+    if "F" in only:
+        for P in (2, 4, 8):
+            for D in (64, 128):
+                for dt in (bf16, fp16):
+                    recs.append(point_fused("F", timer, peak, P, 1, synth.padded_seq(32760, P), 48, D, dt, "v_strided"))
     gated = [r for r in recs if r["pass"] is not None]
     emit({"summary": {"points": len(recs), "gated_points": len(gated), "gated_pass": sum(r["pass"] for r in gated),
                       "gated_pass_write_flushed": sum(r["pass_write_flushed"] for r in gated),
