@@ -1,6 +1,7 @@
 """Host check of the staged kernel's work decomposition (csrc/tma_plan.h), the
-same code the kernel runs: for many shapes and strides, every unit fits one
-shared-memory stage, its bulk-copy runs tile the unit's rows exactly and in
+same code the kernel runs: for many shapes and strides and both stage rings,
+every unit fits one shared-memory stage, the planner's stage choice follows its
+rule, its bulk-copy runs tile the unit's rows exactly and in
 order, every run is really contiguous under the strides, stays inside the
 plane, and has 16-byte aligned offsets and sizes; and the same runs dealt out
 to the lanes of a warp (for_each_run_lane) are, over all lanes, exactly those
@@ -32,10 +33,16 @@ int main() {
     const int64_t sh = packed ? rb : int64_t(rb) + 16 * (1 + rnd(8));
     const int64_t band = int64_t(Hl - 1) * sh + rb;
     const int64_t st = rnd(3) == 0 && packed ? int64_t(Hl) * rb : band + 16 * rnd(64);
-    const uint32_t rpu = tma_rows_per_unit(Hl, rb);
+    const uint32_t stage = (it & 1) ? kStageBytes : kStageBytesSmall;  // both rings
+    const uint32_t rpu = tma_rows_per_unit(Hl, rb, stage);
     const uint32_t rows = Sl * Hl;
-    if (rpu == 0 || uint64_t(rpu) * rb > kStageBytes) { ++bad; continue; }
-    if (uint64_t(Hl) * rb <= kStageBytes && rpu % Hl != 0) { ++bad; continue; }  // whole tokens
+    if (rb > stage) { if (rpu != 0) ++bad; continue; }
+    if (rpu == 0 || uint64_t(rpu) * rb > stage) { ++bad; continue; }
+    if (uint64_t(Hl) * rb <= stage && rpu % Hl != 0) { ++bad; continue; }  // whole tokens
+    // the stage choice: the small ring only for bands under 3 KiB on launches over 128 MiB
+    const uint32_t big = staged_stage_bytes(uint64_t(Hl) * rb, rb, uint64_t(200) << 20);
+    if (big != ((uint64_t(Hl) * rb >= 3072 || rb > kStageBytesSmall) ? kStageBytes : kStageBytesSmall)) ++bad;
+    if (staged_stage_bytes(uint64_t(Hl) * rb, rb, uint64_t(64) << 20) != kStageBytes) ++bad;
     const int64_t extent = int64_t(Sl - 1) * st + band;
     for (uint32_t R0 = 0; R0 < rows; R0 += rpu) {
       const uint32_t R1 = R0 + rpu < rows ? R0 + rpu : rows;
@@ -74,6 +81,7 @@ int main() {
   }
   // a row larger than a stage is refused
   if (tma_rows_per_unit(4, kStageBytes + 16) != 0) ++bad;
+  if (tma_rows_per_unit(4, kStageBytesSmall + 16, kStageBytesSmall) != 0) ++bad;
   std::printf("%ld %ld %ld\n", bad, cases, lane_checks);
   return bad != 0;
 }

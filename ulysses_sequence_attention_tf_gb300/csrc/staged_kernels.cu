@@ -7,8 +7,9 @@
 //
 //  * Persistent grid, one CTA (one warp) per SM.  The warp issues
 //    cp.async.bulk global->shared loads for a unit (a row range of one plane,
-//    <= 32 KiB, see tma_plan.h) into a ring of shared-memory stages, a few units
-//    ahead, each completing on the stage's mbarrier with a transaction count;
+//    <= 64 KiB, see tma_plan.h) into a ring of shared-memory stages (six of
+//    32 KiB, two units ahead, or three of 64 KiB, one ahead, as the planner
+//    sized the units), each completing on the stage's mbarrier with a transaction count;
 //    it then issues the unit's bulk shared->global stores and reuses a stage
 //    only after the stores' reads of it have finished
 //    (cp.async.bulk.wait_group.read).  A unit's copies (one per contiguous run:
@@ -22,11 +23,18 @@
 #include "tma_plan.h"
 
 // Tuning constants (compile-time; overridable with -D for measurement sweeps).
+// The two rings of tma_plan.h: stages, and units loaded ahead of the store.
 #ifndef TFU_STAGES
-#define TFU_STAGES 6  // copy kernel: stages of 32 KiB
+#define TFU_STAGES 3  // large ring: stages of kStageBytes (64 KiB)
 #endif
 #ifndef TFU_LAG
-#define TFU_LAG 2  // copy kernel: units loaded ahead of the store
+#define TFU_LAG 1  // large ring (two ahead measured lower with 64 KiB stages)
+#endif
+#ifndef TFU_STAGES_SMALL
+#define TFU_STAGES_SMALL 6  // small ring: stages of kStageBytesSmall (32 KiB)
+#endif
+#ifndef TFU_LAG_SMALL
+#define TFU_LAG_SMALL 2
 #endif
 namespace tfu {
 
@@ -39,15 +47,18 @@ using namespace dev;
 
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 
-// Copy kernel: one data-movement warp and a ring of 32 KiB stages.
+// Copy kernel: one data-movement warp and a ring of kStages stages of kStride bytes.
+template <int kStagesR, int kLagR, uint32_t kStrideR>
 struct CopyRing {
-    static constexpr int kStages = TFU_STAGES;
-    static constexpr int kLag = TFU_LAG;
-    static constexpr uint32_t kStride = kStageBytes;
+    static constexpr int kStages = kStagesR;
+    static constexpr int kLag = kLagR;
+    static constexpr uint32_t kStride = kStrideR;
     static constexpr size_t kSmem = size_t(kStages) * kStride + kStages * sizeof(uint64_t) + 16;
     static_assert(kLag >= 1 && kLag < kStages, "loads ahead must leave a stage for the store");
     static_assert(kSmem <= 227 * 1024, "stage ring exceeds shared memory");
 };
+using LargeRing = CopyRing<TFU_STAGES, TFU_LAG, kStageBytes>;
+using SmallRing = CopyRing<TFU_STAGES_SMALL, TFU_LAG_SMALL, kStageBytesSmall>;
 
 constexpr unsigned kStatusLoadWait = 1u;
 
@@ -164,10 +175,9 @@ __device__ __forceinline__ Unit decode_unit(const RelayoutParams& p, uint32_t u)
 // phase is observed in order; a lane that stores commits one bulk group per unit
 // stored, and a stage is reloaded only after every store that last read it has
 // finished reading (each storing lane's bulk wait_group.read, then a warp barrier).
-template <Dir kDir, bool kWarp>
+template <Dir kDir, bool kWarp, class R>
 __device__ void copy_dma_loop(const RelayoutParams& p, uint8_t* ring, uint64_t* full, volatile int* abort_flag,
                               uint32_t n_my, uint32_t lane, bool split_st) {
-    using R = CopyRing;
     const uint32_t rb = p.row_bytes;
     const uint32_t lanes = kWarp ? 32u : 1u;
     const bool stores = !kWarp || split_st || lane == 0;  // this lane may issue stores
@@ -215,9 +225,8 @@ __device__ void copy_dma_loop(const RelayoutParams& p, uint8_t* ring, uint64_t* 
 // Pure relayout (copy scatter, gather): one warp, one ring, all units.  The warp
 // deals out copies only when some slot's units are made of enough runs (the
 // same decision for every CTA of the launch); otherwise lane 0 works alone.
-template <Dir kDir>
+template <Dir kDir, class R>
 __global__ void __launch_bounds__(32, 1) copy_staged_kernel(const __grid_constant__ RelayoutParams p) {
-    using R = CopyRing;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(R::kStages) * R::kStride);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(full + R::kStages);
@@ -234,14 +243,14 @@ __global__ void __launch_bounds__(32, 1) copy_staged_kernel(const __grid_constan
     }
     const uint32_t n_my = blockIdx.x < p.n_units ? (p.n_units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     if (!split_ld && !split_st) {
-        if (lane == 0) copy_dma_loop<kDir, false>(p, smem, full, abort_flag, n_my, 0, false);
+        if (lane == 0) copy_dma_loop<kDir, false, R>(p, smem, full, abort_flag, n_my, 0, false);
         return;
     }
     __syncwarp();  // the barriers are initialised before any lane uses them
-    copy_dma_loop<kDir, true>(p, smem, full, abort_flag, n_my, lane, split_st);
+    copy_dma_loop<kDir, true, R>(p, smem, full, abort_flag, n_my, lane, split_st);
 }
 
-template <Dir kDir>
+template <Dir kDir, class R>
 cudaError_t launch_copy(const RelayoutParams& p, cudaStream_t stream) {
     static bool attr_done[64] = {};  // per device: the shared-memory opt-in
     int dev = 0, sms = 0;
@@ -249,14 +258,23 @@ cudaError_t launch_copy(const RelayoutParams& p, cudaStream_t stream) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 1;
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(copy_staged_kernel<kDir>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(CopyRing::kSmem));
+        cudaError_t e = cudaFuncSetAttribute(copy_staged_kernel<kDir, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(R::kSmem));
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
     const unsigned grid = unsigned(p.n_units < uint32_t(sms) ? p.n_units : uint32_t(sms));
-    copy_staged_kernel<kDir><<<grid, 32, CopyRing::kSmem, stream>>>(p);
+    copy_staged_kernel<kDir, R><<<grid, 32, R::kSmem, stream>>>(p);
     return cudaGetLastError();
+}
+
+// The ring whose stages fit the planned units: the small one when a unit fits
+// its stage, the large one otherwise (a unit never exceeds the large stage).
+template <Dir kDir>
+cudaError_t launch_copy_ring(const RelayoutParams& p, cudaStream_t stream) {
+    if (uint64_t(p.rpu) * p.row_bytes > kStageBytes) return cudaErrorInvalidValue;
+    if (uint64_t(p.rpu) * p.row_bytes <= kStageBytesSmall) return launch_copy<kDir, SmallRing>(p, stream);
+    return launch_copy<kDir, LargeRing>(p, stream);
 }
 
 }  // namespace
@@ -264,7 +282,7 @@ cudaError_t launch_copy(const RelayoutParams& p, cudaStream_t stream) {
 cudaError_t launch_relayout_staged(const RelayoutParams& p, Dir dir, Fused fused, cudaStream_t stream) {
     if (p.n_units == 0) return cudaSuccess;
     if (p.rpu == 0 || fused != Fused::kNone) return cudaErrorInvalidValue;
-    return dir == Dir::kGather ? launch_copy<Dir::kGather>(p, stream) : launch_copy<Dir::kScatter>(p, stream);
+    return dir == Dir::kGather ? launch_copy_ring<Dir::kGather>(p, stream) : launch_copy_ring<Dir::kScatter>(p, stream);
 }
 
 cudaError_t read_staged_status(unsigned* out, bool clear) {

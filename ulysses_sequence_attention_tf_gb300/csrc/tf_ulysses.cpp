@@ -279,7 +279,11 @@ tf_status launch_planned(RelayoutParams& p, const Shape& sh, tfu::Dir dir, tfu::
     const bool staged_ok = TFU_USE_STAGED && fused == tfu::Fused::kNone &&
                            !(dir == tfu::Dir::kGather && (small_band || rb <= 128));
     const uint32_t vec = pick_vec_bytes(p, sh, src_tokens, dst_tokens);
-    const uint32_t rpu = tfu::tma_rows_per_unit(uint32_t(sh.Hl), rb);
+    // staged units: the stage ring by head band and launch size (tma_plan.h)
+    const uint64_t band = uint64_t(sh.Hl) * rb;
+    const uint64_t bytes_per_direction = uint64_t(sh.B) * sh.P * p.nx * sh.P * rows * rb;
+    const uint32_t rpu = tfu::tma_rows_per_unit(uint32_t(sh.Hl), rb,
+                                                tfu::staged_stage_bytes(band, rb, bytes_per_direction));
     if (block_ok && vec == 32) {
         p.vec_bytes = 32;
         p.vpr = rb / 32;

@@ -22,16 +22,39 @@
 
 namespace tfu {
 
-constexpr uint32_t kStageBytes = 32768;  // bytes of one shared-memory stage
+// Two stage rings, chosen per launch by the planner (units of at most the ring's
+// stage size; the kernel takes the ring whose stages fit the planned unit):
+//  * kStageBytes (64 KiB) x 3, one unit loaded ahead: token head bands of 3 KiB
+//    or more, and launches of at most 128 MiB per direction;
+//  * kStageBytesSmall (32 KiB) x 6, two units ahead: the rest.
+// Measured on GB300 (fractions of the copy peak): 64 KiB units raise the 72 MB
+// FLUX-like copy scatter to 0.85 (0.77) and 64 MiB single-tensor relayouts to
+// 0.87 (0.80) after a read flush, and 4 KiB-band relayouts of 1-2 GiB to
+// 0.95-1.00 (0.89-0.97); on large launches of 1.5-2.5 KiB bands run back to
+// back, 32 KiB units keep more in flight (the video-DiT gather 0.961 against
+// 0.891; 16 KiB units are far lower everywhere).
+#ifndef TFU_STAGE_BYTES
+#define TFU_STAGE_BYTES 65536
+#endif
+#ifndef TFU_STAGE_BYTES_SMALL
+#define TFU_STAGE_BYTES_SMALL 32768
+#endif
+constexpr uint32_t kStageBytes = TFU_STAGE_BYTES;            // the large ring's stage: the largest unit
+constexpr uint32_t kStageBytesSmall = TFU_STAGE_BYTES_SMALL;  // the small ring's stage
+static_assert(kStageBytes >= 16 && (kStageBytes & (kStageBytes - 1)) == 0,
+              "a stage is a power of two bytes (the chunk exchange halves it to a row that divides the chunk)");
+static_assert(kStageBytesSmall >= 16 && kStageBytesSmall <= kStageBytes &&
+                  (kStageBytesSmall & (kStageBytesSmall - 1)) == 0,
+              "the small ring's stage is a power of two no larger than the large one");
 
 // A unit's loads are dealt out to the warp's lanes from this many runs up, its
 // stores from this many up (fewer go from lane 0 in order).  Measured on GB300
-// (fractions of the copy peak): dealing out loads gains at every run size
-// (1.5 KiB bands 0.91 against 0.63 from one lane; 2 KiB 0.94 against 0.79);
-// dealing out stores gains from 16 runs per unit (21 runs of 1.5 KiB: 0.85
-// against 0.67; 16 of 2 KiB: 0.84-0.96 against 0.78-0.91) and loses below (the
-// video-DiT gather's 12 runs of 2.5 KiB: 0.91 against 0.93; 10 of 3 KiB: 0.84
-// against 0.87).
+// with 32 KiB units (fractions of the copy peak): dealing out loads gains at
+// every run size (1.5 KiB bands 0.91 against 0.63 from one lane; 2 KiB 0.94
+// against 0.79); dealing out stores gains from 16 runs per unit (21 runs of
+// 1.5 KiB: 0.85 against 0.67; 16 of 2 KiB: 0.84-0.96 against 0.78-0.91) and
+// loses below (12 runs of 2.5 KiB: 0.91 against 0.93).  With 64 KiB units the
+// same 16-run threshold measured best (a 32-run one: mean 0.944 against 0.948).
 #ifndef TFU_LOAD_SPLIT_RUNS
 #define TFU_LOAD_SPLIT_RUNS 1
 #endif
@@ -41,13 +64,25 @@ constexpr uint32_t kStageBytes = 32768;  // bytes of one shared-memory stage
 constexpr uint32_t kLoadSplitRuns = TFU_LOAD_SPLIT_RUNS;
 constexpr uint32_t kStoreSplitRuns = TFU_STORE_SPLIT_RUNS;
 
-// Rows per unit: whole tokens (all Hl heads) when a token's head band fits a
-// stage, else as many rows as fit.  0 if a single row does not fit.
-__host__ __device__ inline uint32_t tma_rows_per_unit(uint32_t Hl, uint32_t row_bytes) {
-    if (row_bytes == 0 || row_bytes > kStageBytes || Hl == 0) return 0;
+// Rows per unit for stages of `stage` bytes: whole tokens (all Hl heads) when a
+// token's head band fits a stage, else as many rows as fit.  0 if a single row
+// does not fit.
+__host__ __device__ inline uint32_t tma_rows_per_unit(uint32_t Hl, uint32_t row_bytes, uint32_t stage = kStageBytes) {
+    if (row_bytes == 0 || row_bytes > stage || Hl == 0) return 0;
     const uint64_t token_bytes = uint64_t(Hl) * row_bytes;
-    if (token_bytes <= kStageBytes) return Hl * uint32_t(kStageBytes / token_bytes);
-    return uint32_t(kStageBytes / row_bytes);
+    if (token_bytes <= stage) return Hl * uint32_t(stage / token_bytes);
+    return uint32_t(stage / row_bytes);
+}
+
+// The stage size the planner uses for a pure relayout whose token head band is
+// `band` bytes, moving `bytes_per_direction` bytes: the large ring for bands of
+// 3 KiB or more, for launches of at most 128 MiB per direction, and for rows
+// that do not fit the small stage; the small ring otherwise.
+__host__ __device__ inline uint32_t staged_stage_bytes(uint64_t band, uint32_t row_bytes,
+                                                       uint64_t bytes_per_direction) {
+    if (band >= 3072 || bytes_per_direction <= (uint64_t(128) << 20) || row_bytes > kStageBytesSmall)
+        return kStageBytes;
+    return kStageBytesSmall;
 }
 
 // Calls f(first_row_in_unit, n_rows, byte_offset_in_plane) for each maximal run
