@@ -362,10 +362,10 @@ def run_e2e(args, torch, binding, src, wq, wk, w, stream, dev, world, step_paylo
         torch.cuda.synchronize(dev)
         return c0.elapsed_time(c1)
 
-    # three interleaved repeats of each; the medians are reported (the host link is
-    # shared with the rest of the machine, and one window can catch other traffic)
+    # five interleaved repeats of each; the medians are reported (the host link is
+    # shared with the rest of the machine, and a window can catch other traffic)
     e2e_runs, copy_runs = [], []
-    for _ in range(3):
+    for _ in range(5):
         e2e_runs.append(time_e2e())
         copy_runs.append(time_copies())
     e2e_ms, copy_ms = statistics.median(e2e_runs), statistics.median(copy_runs)
@@ -381,8 +381,8 @@ def run_e2e(args, torch, binding, src, wq, wk, w, stream, dev, world, step_paylo
                           "e2e_frac_of_copies_only": copy_ms / e2e_ms},
             "note": "pinned host Q/K/V/attention inputs copied in, all targets and outputs copied out, every "
                     "step; V uploaded contiguous; upload, calls and download of consecutive steps overlap on "
-                    "three streams (two buffer sets); median of three repeats of the timed steps, interleaved "
-                    "with three repeats of host_link: the same copies without the calls"}
+                    "three streams (two buffer sets); median of five repeats of the timed steps, interleaved "
+                    "with five repeats of host_link: the same copies without the calls"}
 
 
 def main():

@@ -225,6 +225,15 @@ tf_status plan_units(RelayoutParams& p, const Shape& sh) {
 #define TFU_SMALL_BAND 1024
 #endif
 constexpr uint64_t kSmallBandBytes = TFU_SMALL_BAND;
+#ifndef TFU_BLOCK_COPY_BAND
+// Copy scatters of head rows of 256 bytes or more take the block kernel up to this
+// band as well (GB300, fractions of the copy peak after a read flush: 72 MB
+// FLUX-like scatter, 1.5 KiB bands, 0.90 against 0.83 by bulk copies; 2 KiB bands
+// 0.97-0.98 against 0.94-0.96; the video-DiT copy scatter, 2.5 KiB, 6276 against
+// 6050 GB/s back to back).  Bands of 3 KiB or more stay on the bulk-copy kernel.
+#define TFU_BLOCK_COPY_BAND 2560
+#endif
+constexpr uint64_t kBlockCopyBandBytes = TFU_BLOCK_COPY_BAND;
 #ifndef TFU_BLOCK_PASSES
 #define TFU_BLOCK_PASSES 0  // pipeline passes per row group and unit of the block kernel; 0: by slot count
 #endif
@@ -232,8 +241,9 @@ constexpr uint64_t kSmallBandBytes = TFU_SMALL_BAND;
 // Plan and launch one relayout:
 //  * scatters with 32-byte vectors and D * esize in {64, 128, 256, 512} bytes
 //    (fused always; copies into the fused receive layout, copies whose token head
-//    band is small, or all copies when TFU_COPY_BLOCKS): the block kernel, all
-//    slots of a token block in one pass;
+//    band is at most 1 KiB -- or 2.5 KiB for head rows of 256 bytes or more --, or
+//    all copies when TFU_COPY_BLOCKS): the block kernel, all slots of a token
+//    block in one pass;
 //  * other pure relayouts whose head row fits a stage, except gathers of small
 //    bands or 128-byte rows: the shared-memory-staged (bulk-copy) kernel;
 //  * the rest: the register kernel with 32- or 16-byte vectors.
@@ -273,9 +283,12 @@ tf_status launch_planned(RelayoutParams& p, const Shape& sh, tfu::Dir dir, tfu::
     // source, the gather's destination); the bulk-copy engine moves pieces of a KiB
     // or less, and gathers of 128-byte rows, slower than the register paths
     const bool small_band = uint64_t(sh.Hl) * rb <= kSmallBandBytes;
+    // copy scatters of 256- or 512-byte head rows in bands up to 2.5 KiB also move
+    // faster through the registers than through the bulk-copy engine
+    const bool mid_band = rb >= 256 && uint64_t(sh.Hl) * rb <= kBlockCopyBandBytes;
     const bool block_ok = dir == tfu::Dir::kScatter && dst_shared && (rb == 64 || rb == 128 || rb == 256 || rb == 512) &&
                           (fused != tfu::Fused::kNone ? TFU_FUSED_BLOCKS
-                                                      : (TFU_COPY_BLOCKS || !dst_rows_packed || small_band));
+                                                      : (TFU_COPY_BLOCKS || !dst_rows_packed || small_band || mid_band));
     const bool staged_ok = TFU_USE_STAGED && fused == tfu::Fused::kNone &&
                            !(dir == tfu::Dir::kGather && (small_band || rb <= 128));
     const uint32_t vec = pick_vec_bytes(p, sh, src_tokens, dst_tokens);

@@ -78,9 +78,16 @@ __host__ __device__ inline uint32_t tma_rows_per_unit(uint32_t Hl, uint32_t row_
 // `band` bytes, moving `bytes_per_direction` bytes: the large ring for bands of
 // 3 KiB or more, for launches of at most 128 MiB per direction, and for rows
 // that do not fit the small stage; the small ring otherwise.
+#ifndef TFU_LARGE_RING_BAND
+#define TFU_LARGE_RING_BAND 3072  // head bands from this many bytes take the large ring
+#endif
+#ifndef TFU_LARGE_RING_MAX_MIB
+#define TFU_LARGE_RING_MAX_MIB 128  // launches up to this many MiB per direction take the large ring
+#endif
 __host__ __device__ inline uint32_t staged_stage_bytes(uint64_t band, uint32_t row_bytes,
                                                        uint64_t bytes_per_direction) {
-    if (band >= 3072 || bytes_per_direction <= (uint64_t(128) << 20) || row_bytes > kStageBytesSmall)
+    if (band >= TFU_LARGE_RING_BAND || bytes_per_direction <= (uint64_t(TFU_LARGE_RING_MAX_MIB) << 20) ||
+        row_bytes > kStageBytesSmall)
         return kStageBytes;
     return kStageBytesSmall;
 }
