@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
     block_kernel(const __grid_constant__ RelayoutParams p) {
     constexpr int VW = 32, NP = 8;                // 32 bytes = 8 element pairs per lane
     constexpr int kSlots = kCopy + kNF;
-    constexpr int kDepth = kNF > 0 ? kBlockDepth : kCopyBlockDepth;
+    constexpr int kDepth = kNF == 0 ? kCopyBlockDepth : (kCopy == 0 ? kQkBlockDepth : kBlockDepth);
     constexpr int kRowFloats = kLanes * NP * 2;  // D floats per table row
     constexpr int kCs = NP / 2;                   // (cos, sin) float4s of the lane's element pairs
     constexpr uint32_t kGroups = kThreads / kLanes;

@@ -26,8 +26,15 @@ __host__ __device__ constexpr int chunk_vecs(int vec_bytes) { return kChunkBytes
 #ifndef TFU_COPY_BLOCK_DEPTH
 #define TFU_COPY_BLOCK_DEPTH 4
 #endif
+#ifndef TFU_QK_BLOCK_DEPTH
+// fused launches without a copied slot (Q/K only): a third row in flight fits the
+// registers once the RMSNorm weights sit in shared memory (124, no spill) and
+// measured 5304 GB/s against 5158-5163 at depth 2 (depth 4: 5126-5128)
+#define TFU_QK_BLOCK_DEPTH 3
+#endif
 constexpr int kBlockDepth = TFU_BLOCK_DEPTH;
 constexpr int kCopyBlockDepth = TFU_COPY_BLOCK_DEPTH;
+constexpr int kQkBlockDepth = TFU_QK_BLOCK_DEPTH;
 
 // Unsigned 32-bit division by an invariant divisor as multiply-high, add and
 // shift (Granlund & Montgomery, "Division by invariant integers using

@@ -302,7 +302,9 @@ tf_status launch_planned(RelayoutParams& p, const Shape& sh, tfu::Dir dir, tfu::
         p.vpr = rb / 32;
         // a unit gives every row group of the CTA whole pipeline passes (kThreads / vpr
         // groups, depth rows each): one pass when three slots share the rows, else two
-        const uint32_t depth = fused != tfu::Fused::kNone ? tfu::kBlockDepth : tfu::kCopyBlockDepth;
+        const uint32_t depth = fused == tfu::Fused::kNone ? tfu::kCopyBlockDepth
+                               : (p.fused_mask & 1u)       ? tfu::kQkBlockDepth
+                                                           : tfu::kBlockDepth;
         const uint32_t passes = TFU_BLOCK_PASSES > 0 ? TFU_BLOCK_PASSES : (p.nx >= 3 ? 1u : 2u);
         const uint32_t unit_rows = uint32_t(tfu::kThreads) / p.vpr * depth * passes;
         if ((s = plan_rows(uint64_t(sh.B) * sh.P * sh.P, unit_rows)) != TF_OK) return s;
