@@ -20,8 +20,11 @@
 //    write all P head groups of a token block.
 //  * Each lane group of kLanes = D*2/32 lanes takes a contiguous run of the
 //    unit's rows and keeps kDepth rows (of every slot) loaded ahead of the one it
-//    computes.  One 32-byte vector per lane per row and slot; loads bypass L1,
-//    stores are evict-first.
+//    computes, across unit boundaries too: the last pass over a unit's rows
+//    already loads the group's rows of its next unit (V+Q+K launches of many
+//    rounds of units keep to one unit at a time, which measured faster there).
+//    One 32-byte vector per lane per row and slot; loads bypass L1, stores are
+//    evict-first.
 //  * The (cos, sin) entries are loaded once per token and reused across its
 //    heads and by Q and K.  Destination row (t, h) sits at t*d_t + h*d_h, so the
 //    same code writes the separate [B, S, Hl, D] targets, the fused receive
@@ -66,8 +69,20 @@ __host__ __device__ constexpr int block_min_blocks() {
 // video-DiT scatter.  0: registers.
 #define TFU_BLOCK_SMEM_WEIGHTS 1
 #endif
+#ifndef TFU_BLOCK_STREAM
+// 1: each row group streams the rows of all its units (next unit's loads during
+// the last pass of the one before); 0: one unit at a time
+#define TFU_BLOCK_STREAM 1
+#endif
+#ifndef TFU_STREAM_MAX_ROUNDS
+// V+Q+K fused launches stream only while the grid walks at most this many rounds
+// of units: streaming measured +7 % at 5 rounds (P=4, S=4096, H=24), +2 % at 20,
+// but -1.3 to -2 % at 40-81 rounds (video DiT, S=32760 at H=48); copy and
+// Q/K-only launches gained at every size (video-DiT copy scatter +2.6 %)
+#define TFU_STREAM_MAX_ROUNDS 24
+#endif
 
-template <Fused kF, int kLanes, int kCopy, int kNF, bool kNeox>
+template <Fused kF, int kLanes, int kCopy, int kNF, bool kNeox, bool kStream>
 __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
     block_kernel(const __grid_constant__ RelayoutParams p) {
     constexpr int VW = 32, NP = 8;                // 32 bytes = 8 element pairs per lane
@@ -138,33 +153,54 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
     }
     auto w = [&](int f) -> const uint32_t(&)[NP] { return w_reg[f]; };
 #endif
-#pragma unroll 1
-    for (uint32_t u = blockIdx.x; u < p.n_units; u += gridDim.x) {
-        const uint32_t c = fastdiv(u, p.div_planes);
-        const uint32_t q = u - c * p.n_planes;  // q = (b * P + r) * P + g
-        const uint32_t g = q % p.P;
-        const uint32_t r = (q / p.P) % p.P;
-        const uint32_t b = q / (p.P * p.P);
+    if constexpr (kStream) {
+        // Each row group walks the rows of all its units as one stream: during the
+        // last pipeline pass of a unit its loads already fetch the first rows of the
+        // group's next unit, so the loads of a new unit overlap the arithmetic of the
+        // one before.  (g, r, b) hold the coordinates of the unit being loaded.
+        struct Span {
+            uint32_t beg, end, slots;  // the group's plane rows [beg, end); pipeline slots (a multiple of kDepth)
+        };
+        auto span_of = [&](uint32_t c) -> Span {
+            const uint32_t R0 = c * p.rpu;
+            const uint32_t n_rows = min(R0 + p.rpu, p.plane_rows) - R0;
+            const uint32_t per = (n_rows + kGroups - 1) / kGroups;  // rows per group, the same for every lane
+            const uint32_t beg = R0 + g_row * per;
+            return Span{beg, min(beg + per, R0 + n_rows), (per + kDepth - 1) / kDepth * kDepth};
+        };
+        uint32_t g, r, b;
+        auto locate = [&](uint32_t u) -> Span {
+            const uint32_t c = fastdiv(u, p.div_planes);
+            const uint32_t q = u - c * p.n_planes;  // q = (b * P + r) * P + g
+            g = q % p.P;
+            r = (q / p.P) % p.P;
+            b = q / (p.P * p.P);
+            return span_of(c);
+        };
         const uint8_t* src[kSlots];
         uint8_t* dst[kSlots];
+        const float* tab_lane = nullptr;
+        auto set_src = [&]() {
 #pragma unroll
-        for (int x = 0; x < kSlots; ++x) {
-            const uint32_t lo = lane_off[is_split(x) ? 1 : 0];
-            src[x] = p.src[x][r] + int64_t(b) * p.s_b[x] + int64_t(g) * p.Hg * p.s_h[x] + lo;
-            dst[x] = p.dst[x][g] + int64_t(b) * p.d_b[x] + int64_t(r) * p.Sl * p.d_t[x] + lo;
-        }
-        const uint32_t R0 = c * p.rpu;
-        const uint32_t n_rows = min(R0 + p.rpu, p.plane_rows) - R0;
-        const uint32_t per = (n_rows + kGroups - 1) / kGroups;  // rows per group, the same for every lane
-        const uint32_t r_beg = R0 + g_row * per;                 // first plane row of this group
-        const uint32_t r_end = min(r_beg + per, R0 + n_rows);    // may be <= r_beg for trailing groups
-        // the lane's element pairs use table entries [dv*NP, dv*NP + NP) in both mappings
-        const float* tab_lane = kNF > 0 ? p.table + size_t(r) * p.Sl * kRowFloats + dv * (2 * NP) : nullptr;
+            for (int x = 0; x < kSlots; ++x) {
+                const uint32_t lo = lane_off[is_split(x) ? 1 : 0];
+                src[x] = p.src[x][r] + int64_t(b) * p.s_b[x] + int64_t(g) * p.Hg * p.s_h[x] + lo;
+            }
+        };
+        auto set_dst = [&]() {
+#pragma unroll
+            for (int x = 0; x < kSlots; ++x) {
+                const uint32_t lo = lane_off[is_split(x) ? 1 : 0];
+                dst[x] = p.dst[x][g] + int64_t(b) * p.d_b[x] + int64_t(r) * p.Sl * p.d_t[x] + lo;
+            }
+            // the lane's element pairs use table entries [dv*NP, dv*NP + NP) in both mappings
+            if constexpr (kNF > 0) tab_lane = p.table + size_t(r) * p.Sl * kRowFloats + dv * (2 * NP);
+        };
         float4 cs[kCs];
 #pragma unroll
         for (int k = 0; k < kCs; ++k) cs[k] = make_float4(1.f, 0.f, 1.f, 0.f);
         uint32_t t_cached = 0xffffffffu;
-        auto load = [&](Vec<VW>(&buf)[kSlots], uint32_t R) {
+        auto load = [&](Vec<VW>(&buf)[kSlots], uint32_t R, uint32_t end) {
             const uint32_t t = fastdiv(R, p.div_hl);
             const uint32_t h = R - t * p.Hl;
 #pragma unroll
@@ -173,11 +209,11 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
 #pragma unroll
                     for (int k = 0; k < NP; ++k) buf[x].w[k] = 0u;
                 }
-                if (R < r_end) buf[x] = ld_lane(src[x] + int64_t(t) * p.s_t[x] + int64_t(h) * p.s_h[x], x);
+                if (R < end) buf[x] = ld_lane(src[x] + int64_t(t) * p.s_t[x] + int64_t(h) * p.s_h[x], x);
             }
         };
-        auto compute_store = [&](Vec<VW>(&buf)[kSlots], uint32_t R) {
-            const bool valid = R < r_end;
+        auto compute_store = [&](Vec<VW>(&buf)[kSlots], uint32_t R, uint32_t end) {
+            const bool valid = R < end;
             const uint32_t t = fastdiv(R, p.div_hl);
             const uint32_t h = R - t * p.Hl;
             if constexpr (kNF > 0) {
@@ -203,34 +239,148 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
                 for (int x = 0; x < kSlots; ++x) st_lane(dst[x] + off, x, buf[x]);
             }
         };
+        uint32_t u = blockIdx.x;  // the grid never exceeds the unit count
+        Span ld = locate(u), st = ld;
+        set_src();
+        set_dst();
         Vec<VW> bufs[kDepth][kSlots];
 #pragma unroll
-        for (int d = 0; d < kDepth; ++d) load(bufs[d], r_beg + d);
+        for (int d = 0; d < kDepth; ++d) load(bufs[d], ld.beg + d, ld.end);
 #pragma unroll 1
-        for (uint32_t R = r_beg; R < r_beg + per; R += kDepth) {
+        for (;;) {
+#pragma unroll 1
+            for (uint32_t j = 0; j < st.slots; j += kDepth) {
+                uint32_t ld_row = ld.beg + j + kDepth;
+                if (j + kDepth >= st.slots) {  // last pass: load the next unit's first rows
+                    const uint32_t un = u + gridDim.x;
+                    if (un < p.n_units) {
+                        ld = locate(un);
+                        set_src();
+                    } else {
+                        ld.beg = ld.end = 0;  // nothing left: the loads below are masked
+                    }
+                    ld_row = ld.beg;
+                }
 #pragma unroll
-            for (int d = 0; d < kDepth; ++d) {
-                compute_store(bufs[d], R + d);
-                load(bufs[d], R + d + kDepth);
+                for (int d = 0; d < kDepth; ++d) {
+                    compute_store(bufs[d], st.beg + j + d, st.end);
+                    load(bufs[d], ld_row + d, ld.end);
+                }
+            }
+            u += gridDim.x;
+            if (u >= p.n_units) break;
+            st = ld;
+            set_dst();
+            t_cached = 0xffffffffu;  // a new shard r: another table block
+        }
+    } else {
+#pragma unroll 1
+        for (uint32_t u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+            const uint32_t c = fastdiv(u, p.div_planes);
+            const uint32_t q = u - c * p.n_planes;  // q = (b * P + r) * P + g
+            const uint32_t g = q % p.P;
+            const uint32_t r = (q / p.P) % p.P;
+            const uint32_t b = q / (p.P * p.P);
+            const uint8_t* src[kSlots];
+            uint8_t* dst[kSlots];
+#pragma unroll
+            for (int x = 0; x < kSlots; ++x) {
+                const uint32_t lo = lane_off[is_split(x) ? 1 : 0];
+                src[x] = p.src[x][r] + int64_t(b) * p.s_b[x] + int64_t(g) * p.Hg * p.s_h[x] + lo;
+                dst[x] = p.dst[x][g] + int64_t(b) * p.d_b[x] + int64_t(r) * p.Sl * p.d_t[x] + lo;
+            }
+            const uint32_t R0 = c * p.rpu;
+            const uint32_t n_rows = min(R0 + p.rpu, p.plane_rows) - R0;
+            const uint32_t per = (n_rows + kGroups - 1) / kGroups;  // rows per group, the same for every lane
+            const uint32_t r_beg = R0 + g_row * per;                 // first plane row of this group
+            const uint32_t r_end = min(r_beg + per, R0 + n_rows);    // may be <= r_beg for trailing groups
+            // the lane's element pairs use table entries [dv*NP, dv*NP + NP) in both mappings
+            const float* tab_lane = kNF > 0 ? p.table + size_t(r) * p.Sl * kRowFloats + dv * (2 * NP) : nullptr;
+            float4 cs[kCs];
+#pragma unroll
+            for (int k = 0; k < kCs; ++k) cs[k] = make_float4(1.f, 0.f, 1.f, 0.f);
+            uint32_t t_cached = 0xffffffffu;
+            auto load = [&](Vec<VW>(&buf)[kSlots], uint32_t R) {
+                const uint32_t t = fastdiv(R, p.div_hl);
+                const uint32_t h = R - t * p.Hl;
+#pragma unroll
+                for (int x = 0; x < kSlots; ++x) {
+                    if constexpr (kNF > 0) {  // masked rows still go through the row reduction
+#pragma unroll
+                        for (int k = 0; k < NP; ++k) buf[x].w[k] = 0u;
+                    }
+                    if (R < r_end) buf[x] = ld_lane(src[x] + int64_t(t) * p.s_t[x] + int64_t(h) * p.s_h[x], x);
+                }
+            };
+            auto compute_store = [&](Vec<VW>(&buf)[kSlots], uint32_t R) {
+                const bool valid = R < r_end;
+                const uint32_t t = fastdiv(R, p.div_hl);
+                const uint32_t h = R - t * p.Hl;
+                if constexpr (kNF > 0) {
+                    if (valid && t != t_cached) {
+                        const float* tab = tab_lane + size_t(t) * kRowFloats;
+#pragma unroll
+                        for (int k = 0; k < kCs; ++k) cs[k] = ld_table(tab + 4 * k);
+                        t_cached = t;
+                    }
+                    // every lane runs the row reductions (they shuffle); only valid rows are written
+#pragma unroll
+                    for (int f = 0; f < kNF; ++f) {
+                        if constexpr (kNeox) {
+                            norm_rope_core_split<kF, kLanes, NP>(buf[kCopy + f].w, w(f), cs, p.eps);
+                        } else {
+                            norm_rope_core<kF, kLanes, NP>(buf[kCopy + f].w, w(f), cs, p.eps);
+                        }
+                    }
+                }
+                if (valid) {  // the scatter targets of one launch share their strides (slot 0's)
+                    const int64_t off = int64_t(t) * p.d_t[0] + int64_t(h) * p.d_h[0];
+#pragma unroll
+                    for (int x = 0; x < kSlots; ++x) st_lane(dst[x] + off, x, buf[x]);
+                }
+            };
+            Vec<VW> bufs[kDepth][kSlots];
+#pragma unroll
+            for (int d = 0; d < kDepth; ++d) load(bufs[d], r_beg + d);
+#pragma unroll 1
+            for (uint32_t R = r_beg; R < r_beg + per; R += kDepth) {
+#pragma unroll
+                for (int d = 0; d < kDepth; ++d) {
+                    compute_store(bufs[d], R + d);
+                    load(bufs[d], R + d + kDepth);
+                }
             }
         }
     }
 }
 
-template <Fused kF, int kLanes, int kCopy, int kNF, bool kNeox>
-cudaError_t launch_block(const RelayoutParams& p, cudaStream_t stream) {
+template <Fused kF, int kLanes, int kCopy, int kNF, bool kNeox, bool kStream>
+cudaError_t launch_block_as(const RelayoutParams& p, cudaStream_t stream) {
     static int blocks_per_sm = 0;  // same for every device of one architecture
     if (blocks_per_sm == 0) {
         int bps = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &bps, block_kernel<kF, kLanes, kCopy, kNF, kNeox>, kThreads, 0);
+            &bps, block_kernel<kF, kLanes, kCopy, kNF, kNeox, kStream>, kThreads, 0);
         if (e != cudaSuccess) return e;
         blocks_per_sm = bps > 0 ? bps : 1;
     }
     const int64_t want = int64_t(block_device_sms()) * blocks_per_sm;
     const unsigned grid = unsigned(want < int64_t(p.n_units) ? want : int64_t(p.n_units));
-    block_kernel<kF, kLanes, kCopy, kNF, kNeox><<<grid, kThreads, 0, stream>>>(p);
+    block_kernel<kF, kLanes, kCopy, kNF, kNeox, kStream><<<grid, kThreads, 0, stream>>>(p);
     return cudaGetLastError();
+}
+
+template <Fused kF, int kLanes, int kCopy, int kNF, bool kNeox>
+cudaError_t launch_block(const RelayoutParams& p, cudaStream_t stream) {
+    if constexpr (kCopy == 1 && kNF == 2 && TFU_BLOCK_STREAM) {
+        // rounds of units = units / resident CTAs
+        const uint64_t resident = uint64_t(block_device_sms()) * block_min_blocks<kCopy, kNF>();
+        if (p.n_units > uint64_t(TFU_STREAM_MAX_ROUNDS) * resident)
+            return launch_block_as<kF, kLanes, kCopy, kNF, kNeox, false>(p, stream);
+    }
+    // Q/K-only half-split rows keep one unit at a time: streamed, they spill registers
+    constexpr bool kStreamed = TFU_BLOCK_STREAM != 0 && !(kCopy == 0 && kNF > 0 && kNeox);
+    return launch_block_as<kF, kLanes, kCopy, kNF, kNeox, kStreamed>(p, stream);
 }
 
 template <Fused kF, int kCopy, int kNF, bool kNeox>
