@@ -153,97 +153,101 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
     }
     auto w = [&](int f) -> const uint32_t(&)[NP] { return w_reg[f]; };
 #endif
+    // A group's rows of one unit: plane rows [beg, end) (empty for trailing
+    // groups) and the pipeline slots that walk them (a multiple of kDepth)
+    struct Span {
+        uint32_t beg, end, slots;
+    };
+    auto span_of = [&](uint32_t c) -> Span {
+        const uint32_t R0 = c * p.rpu;
+        const uint32_t n_rows = min(R0 + p.rpu, p.plane_rows) - R0;
+        const uint32_t per = (n_rows + kGroups - 1) / kGroups;  // rows per group, the same for every lane
+        const uint32_t beg = R0 + g_row * per;
+        return Span{beg, min(beg + per, R0 + n_rows), (per + kDepth - 1) / kDepth * kDepth};
+    };
+    uint32_t g, r, b;  // the (head group, shard, batch) of the unit located last
+    auto locate = [&](uint32_t u) -> Span {
+        const uint32_t c = fastdiv(u, p.div_planes);
+        const uint32_t q = u - c * p.n_planes;  // q = (b * P + r) * P + g
+        g = q % p.P;
+        r = (q / p.P) % p.P;
+        b = q / (p.P * p.P);
+        return span_of(c);
+    };
+    const uint8_t* src[kSlots];  // each slot's source block of the unit being loaded
+    uint8_t* dst[kSlots];        // each slot's target block of the unit being stored
+    const float* tab_lane = nullptr;
+    float4 cs[kCs];              // the lane's (cos, sin) entries of token t_cached
+#pragma unroll
+    for (int k = 0; k < kCs; ++k) cs[k] = make_float4(1.f, 0.f, 1.f, 0.f);
+    uint32_t t_cached = 0xffffffffu;
+    auto set_src = [&]() {
+#pragma unroll
+        for (int x = 0; x < kSlots; ++x) {
+            const uint32_t lo = lane_off[is_split(x) ? 1 : 0];
+            src[x] = p.src[x][r] + int64_t(b) * p.s_b[x] + int64_t(g) * p.Hg * p.s_h[x] + lo;
+        }
+    };
+    auto set_dst = [&]() {
+#pragma unroll
+        for (int x = 0; x < kSlots; ++x) {
+            const uint32_t lo = lane_off[is_split(x) ? 1 : 0];
+            dst[x] = p.dst[x][g] + int64_t(b) * p.d_b[x] + int64_t(r) * p.Sl * p.d_t[x] + lo;
+        }
+        // the lane's element pairs use table entries [dv*NP, dv*NP + NP) in both mappings
+        if constexpr (kNF > 0) tab_lane = p.table + size_t(r) * p.Sl * kRowFloats + dv * (2 * NP);
+        t_cached = 0xffffffffu;  // a new shard r: another table block
+    };
+    auto load = [&](Vec<VW>(&buf)[kSlots], uint32_t R, uint32_t end) {
+        const uint32_t t = fastdiv(R, p.div_hl);
+        const uint32_t h = R - t * p.Hl;
+#pragma unroll
+        for (int x = 0; x < kSlots; ++x) {
+            if constexpr (kNF > 0) {  // masked rows still go through the row reduction
+#pragma unroll
+                for (int k = 0; k < NP; ++k) buf[x].w[k] = 0u;
+            }
+            if (R < end) buf[x] = ld_lane(src[x] + int64_t(t) * p.s_t[x] + int64_t(h) * p.s_h[x], x);
+        }
+    };
+    auto compute_store = [&](Vec<VW>(&buf)[kSlots], uint32_t R, uint32_t end) {
+        const bool valid = R < end;
+        const uint32_t t = fastdiv(R, p.div_hl);
+        const uint32_t h = R - t * p.Hl;
+        if constexpr (kNF > 0) {
+            if (valid && t != t_cached) {
+                const float* tab = tab_lane + size_t(t) * kRowFloats;
+#pragma unroll
+                for (int k = 0; k < kCs; ++k) cs[k] = ld_table(tab + 4 * k);
+                t_cached = t;
+            }
+            // every lane runs the row reductions (they shuffle); only valid rows are written
+#pragma unroll
+            for (int f = 0; f < kNF; ++f) {
+                if constexpr (kNeox) {
+                    norm_rope_core_split<kF, kLanes, NP>(buf[kCopy + f].w, w(f), cs, p.eps);
+                } else {
+                    norm_rope_core<kF, kLanes, NP>(buf[kCopy + f].w, w(f), cs, p.eps);
+                }
+            }
+        }
+        if (valid) {  // the scatter targets of one launch share their strides (slot 0's)
+            const int64_t off = int64_t(t) * p.d_t[0] + int64_t(h) * p.d_h[0];
+#pragma unroll
+            for (int x = 0; x < kSlots; ++x) st_lane(dst[x] + off, x, buf[x]);
+        }
+    };
+    Vec<VW> bufs[kDepth][kSlots];
     if constexpr (kStream) {
         // Each row group walks the rows of all its units as one stream: during the
         // last pipeline pass of a unit its loads already fetch the first rows of the
         // group's next unit, so the loads of a new unit overlap the arithmetic of the
-        // one before.  (g, r, b) hold the coordinates of the unit being loaded.
-        struct Span {
-            uint32_t beg, end, slots;  // the group's plane rows [beg, end); pipeline slots (a multiple of kDepth)
-        };
-        auto span_of = [&](uint32_t c) -> Span {
-            const uint32_t R0 = c * p.rpu;
-            const uint32_t n_rows = min(R0 + p.rpu, p.plane_rows) - R0;
-            const uint32_t per = (n_rows + kGroups - 1) / kGroups;  // rows per group, the same for every lane
-            const uint32_t beg = R0 + g_row * per;
-            return Span{beg, min(beg + per, R0 + n_rows), (per + kDepth - 1) / kDepth * kDepth};
-        };
-        uint32_t g, r, b;
-        auto locate = [&](uint32_t u) -> Span {
-            const uint32_t c = fastdiv(u, p.div_planes);
-            const uint32_t q = u - c * p.n_planes;  // q = (b * P + r) * P + g
-            g = q % p.P;
-            r = (q / p.P) % p.P;
-            b = q / (p.P * p.P);
-            return span_of(c);
-        };
-        const uint8_t* src[kSlots];
-        uint8_t* dst[kSlots];
-        const float* tab_lane = nullptr;
-        auto set_src = [&]() {
-#pragma unroll
-            for (int x = 0; x < kSlots; ++x) {
-                const uint32_t lo = lane_off[is_split(x) ? 1 : 0];
-                src[x] = p.src[x][r] + int64_t(b) * p.s_b[x] + int64_t(g) * p.Hg * p.s_h[x] + lo;
-            }
-        };
-        auto set_dst = [&]() {
-#pragma unroll
-            for (int x = 0; x < kSlots; ++x) {
-                const uint32_t lo = lane_off[is_split(x) ? 1 : 0];
-                dst[x] = p.dst[x][g] + int64_t(b) * p.d_b[x] + int64_t(r) * p.Sl * p.d_t[x] + lo;
-            }
-            // the lane's element pairs use table entries [dv*NP, dv*NP + NP) in both mappings
-            if constexpr (kNF > 0) tab_lane = p.table + size_t(r) * p.Sl * kRowFloats + dv * (2 * NP);
-        };
-        float4 cs[kCs];
-#pragma unroll
-        for (int k = 0; k < kCs; ++k) cs[k] = make_float4(1.f, 0.f, 1.f, 0.f);
-        uint32_t t_cached = 0xffffffffu;
-        auto load = [&](Vec<VW>(&buf)[kSlots], uint32_t R, uint32_t end) {
-            const uint32_t t = fastdiv(R, p.div_hl);
-            const uint32_t h = R - t * p.Hl;
-#pragma unroll
-            for (int x = 0; x < kSlots; ++x) {
-                if constexpr (kNF > 0) {  // masked rows still go through the row reduction
-#pragma unroll
-                    for (int k = 0; k < NP; ++k) buf[x].w[k] = 0u;
-                }
-                if (R < end) buf[x] = ld_lane(src[x] + int64_t(t) * p.s_t[x] + int64_t(h) * p.s_h[x], x);
-            }
-        };
-        auto compute_store = [&](Vec<VW>(&buf)[kSlots], uint32_t R, uint32_t end) {
-            const bool valid = R < end;
-            const uint32_t t = fastdiv(R, p.div_hl);
-            const uint32_t h = R - t * p.Hl;
-            if constexpr (kNF > 0) {
-                if (valid && t != t_cached) {
-                    const float* tab = tab_lane + size_t(t) * kRowFloats;
-#pragma unroll
-                    for (int k = 0; k < kCs; ++k) cs[k] = ld_table(tab + 4 * k);
-                    t_cached = t;
-                }
-                // every lane runs the row reductions (they shuffle); only valid rows are written
-#pragma unroll
-                for (int f = 0; f < kNF; ++f) {
-                    if constexpr (kNeox) {
-                        norm_rope_core_split<kF, kLanes, NP>(buf[kCopy + f].w, w(f), cs, p.eps);
-                    } else {
-                        norm_rope_core<kF, kLanes, NP>(buf[kCopy + f].w, w(f), cs, p.eps);
-                    }
-                }
-            }
-            if (valid) {  // the scatter targets of one launch share their strides (slot 0's)
-                const int64_t off = int64_t(t) * p.d_t[0] + int64_t(h) * p.d_h[0];
-#pragma unroll
-                for (int x = 0; x < kSlots; ++x) st_lane(dst[x] + off, x, buf[x]);
-            }
-        };
+        // one before.  (g, r, b) and src then hold the unit being loaded, dst the
+        // unit being stored.
         uint32_t u = blockIdx.x;  // the grid never exceeds the unit count
         Span ld = locate(u), st = ld;
         set_src();
         set_dst();
-        Vec<VW> bufs[kDepth][kSlots];
 #pragma unroll
         for (int d = 0; d < kDepth; ++d) load(bufs[d], ld.beg + d, ld.end);
 #pragma unroll 1
@@ -271,83 +275,23 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
             if (u >= p.n_units) break;
             st = ld;
             set_dst();
-            t_cached = 0xffffffffu;  // a new shard r: another table block
         }
     } else {
+        // one unit at a time: its rows are loaded, computed and stored before the
+        // next unit's first loads
 #pragma unroll 1
         for (uint32_t u = blockIdx.x; u < p.n_units; u += gridDim.x) {
-            const uint32_t c = fastdiv(u, p.div_planes);
-            const uint32_t q = u - c * p.n_planes;  // q = (b * P + r) * P + g
-            const uint32_t g = q % p.P;
-            const uint32_t r = (q / p.P) % p.P;
-            const uint32_t b = q / (p.P * p.P);
-            const uint8_t* src[kSlots];
-            uint8_t* dst[kSlots];
+            const Span sp = locate(u);
+            set_src();
+            set_dst();
 #pragma unroll
-            for (int x = 0; x < kSlots; ++x) {
-                const uint32_t lo = lane_off[is_split(x) ? 1 : 0];
-                src[x] = p.src[x][r] + int64_t(b) * p.s_b[x] + int64_t(g) * p.Hg * p.s_h[x] + lo;
-                dst[x] = p.dst[x][g] + int64_t(b) * p.d_b[x] + int64_t(r) * p.Sl * p.d_t[x] + lo;
-            }
-            const uint32_t R0 = c * p.rpu;
-            const uint32_t n_rows = min(R0 + p.rpu, p.plane_rows) - R0;
-            const uint32_t per = (n_rows + kGroups - 1) / kGroups;  // rows per group, the same for every lane
-            const uint32_t r_beg = R0 + g_row * per;                 // first plane row of this group
-            const uint32_t r_end = min(r_beg + per, R0 + n_rows);    // may be <= r_beg for trailing groups
-            // the lane's element pairs use table entries [dv*NP, dv*NP + NP) in both mappings
-            const float* tab_lane = kNF > 0 ? p.table + size_t(r) * p.Sl * kRowFloats + dv * (2 * NP) : nullptr;
-            float4 cs[kCs];
-#pragma unroll
-            for (int k = 0; k < kCs; ++k) cs[k] = make_float4(1.f, 0.f, 1.f, 0.f);
-            uint32_t t_cached = 0xffffffffu;
-            auto load = [&](Vec<VW>(&buf)[kSlots], uint32_t R) {
-                const uint32_t t = fastdiv(R, p.div_hl);
-                const uint32_t h = R - t * p.Hl;
-#pragma unroll
-                for (int x = 0; x < kSlots; ++x) {
-                    if constexpr (kNF > 0) {  // masked rows still go through the row reduction
-#pragma unroll
-                        for (int k = 0; k < NP; ++k) buf[x].w[k] = 0u;
-                    }
-                    if (R < r_end) buf[x] = ld_lane(src[x] + int64_t(t) * p.s_t[x] + int64_t(h) * p.s_h[x], x);
-                }
-            };
-            auto compute_store = [&](Vec<VW>(&buf)[kSlots], uint32_t R) {
-                const bool valid = R < r_end;
-                const uint32_t t = fastdiv(R, p.div_hl);
-                const uint32_t h = R - t * p.Hl;
-                if constexpr (kNF > 0) {
-                    if (valid && t != t_cached) {
-                        const float* tab = tab_lane + size_t(t) * kRowFloats;
-#pragma unroll
-                        for (int k = 0; k < kCs; ++k) cs[k] = ld_table(tab + 4 * k);
-                        t_cached = t;
-                    }
-                    // every lane runs the row reductions (they shuffle); only valid rows are written
-#pragma unroll
-                    for (int f = 0; f < kNF; ++f) {
-                        if constexpr (kNeox) {
-                            norm_rope_core_split<kF, kLanes, NP>(buf[kCopy + f].w, w(f), cs, p.eps);
-                        } else {
-                            norm_rope_core<kF, kLanes, NP>(buf[kCopy + f].w, w(f), cs, p.eps);
-                        }
-                    }
-                }
-                if (valid) {  // the scatter targets of one launch share their strides (slot 0's)
-                    const int64_t off = int64_t(t) * p.d_t[0] + int64_t(h) * p.d_h[0];
-#pragma unroll
-                    for (int x = 0; x < kSlots; ++x) st_lane(dst[x] + off, x, buf[x]);
-                }
-            };
-            Vec<VW> bufs[kDepth][kSlots];
-#pragma unroll
-            for (int d = 0; d < kDepth; ++d) load(bufs[d], r_beg + d);
+            for (int d = 0; d < kDepth; ++d) load(bufs[d], sp.beg + d, sp.end);
 #pragma unroll 1
-            for (uint32_t R = r_beg; R < r_beg + per; R += kDepth) {
+            for (uint32_t R = sp.beg; R < sp.beg + sp.slots; R += kDepth) {
 #pragma unroll
                 for (int d = 0; d < kDepth; ++d) {
-                    compute_store(bufs[d], R + d);
-                    load(bufs[d], R + d + kDepth);
+                    compute_store(bufs[d], R + d, sp.end);
+                    load(bufs[d], R + d + kDepth, sp.end);
                 }
             }
         }
