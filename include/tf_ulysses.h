@@ -41,8 +41,8 @@
  *    guarded by a mutex.
  *
  * CUDA graphs (flashinfer PR #6332 commit message, "Description", "CUDA graphs":
- * a prepared call allocates nothing; a size first seen inside a capture raises
- * instead of allocating; replays interleave with eager calls).  Every entry
+ * a prepared call allocates nothing; a size first seen inside a capture fails
+ * rather than allocate; replays interleave with eager calls).  Every entry
  * point may be called while `stream` is being captured (cudaStreamBeginCapture,
  * torch.cuda.graph).  Inside a capture the library allocates and frees nothing:
  * a call whose cache entry or RoPE table does not exist yet returns
@@ -74,7 +74,7 @@ extern "C" {
 
 #define TF_ULYSSES_ABI_VERSION 1
 #define TF_ULYSSES_MAX_SHARDS 8      /* largest P */
-#define TF_ULYSSES_CACHE_CAPACITY 12 /* cached target sets (TeleFuser PR #27: "up to 12 cached targets") */
+#define TF_ULYSSES_CACHE_CAPACITY 12 /* cached target sets (the cache bound of TeleFuser PR #27, "Changes Made") */
 #define TF_ULYSSES_MAX_SLOTS 8       /* rotating target sets per cache entry (tf_ulysses_set_slots) */
 
 typedef enum tf_status {
@@ -170,8 +170,9 @@ typedef struct tf_targets {
 /*
  * tf_ulysses_scatter_qkv -- sequence->head scatter of Q, K and V in one grouped
  * launch into cached final-layout targets (TeleFuser PR #27, "Changes Made":
- * direct writes into final-layout targets, up to 12 cached targets keyed by tag,
- * shape, dtype and mode, one grouped completion for tagged Q/K/V).
+ * direct writes into final-layout targets; a bounded cache of at most 12 target
+ * sets keyed on the tag, the shape, the dtype and a mode; one grouped completion
+ * for tagged Q/K/V).
  *
  *  tag        NUL-terminated cache tag (<= 63 bytes); NULL means "".  The cache key is
  *             (tag, mode, tensors present, P, B, S_local, H, D, dtype, device).

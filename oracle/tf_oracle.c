@@ -14,9 +14,9 @@
  *  - same page, "Shared Collective Primitives / Equal-shape gather": shards are
  *    concatenated in rank order (rank-major), which fixes target row = r*S_local + t.
  *  - flashinfer PR #6332 (QkvNormRopeExchangeOverlap) commit message, section
- *    "Assumptions", items "Exchange algorithm" (every rank receives its head band
- *    of all tokens) and "Operator math" (fp32 RMSNorm, eps 1e-6, shared
- *    [head_dim] weight per Q / K; interleaved pairwise RoPE applied in fp32 from a
+ *    "Assumptions", items "Exchange algorithm" (each rank ends up with its own band
+ *    of heads for the whole sequence) and "Operator math" (fp32 RMSNorm, eps 1e-6, shared
+ *    [head_dim] weight per Q / K; RoPE on interleaved element pairs applied in fp32 from a
  *    per-token cos/sin table; order QK-norm -> RoPE; 16-bit operands/outputs);
  *    section "Tests" (RMSNorm with the 16-bit cast before the 16-bit weight scale).
  *
@@ -216,7 +216,7 @@ static void rmsnorm_scale(int fmt, int D, const uint16_t *x, const uint16_t *w, 
 }
 
 /*
- * One head row at a token whose table row is cs, interleaved (pairwise) RoPE:
+ * One head row at a token whose table row is cs, RoPE on interleaved pairs:
  * z = rmsnorm_scale(x), then for i < D/2
  *   o[2i]   = round16(z[2i]*cos - z[2i+1]*sin)
  *   o[2i+1] = round16(z[2i]*sin + z[2i+1]*cos)

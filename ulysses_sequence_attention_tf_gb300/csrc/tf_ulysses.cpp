@@ -3,9 +3,9 @@
 // the resident RoPE tables, the allocator hook and the launches.
 //
 // Sources: TeleFuser PR #27 "Add CUDA IPC Ulysses overlap and lossless LingBot
-// streaming", "Changes Made" (final-layout targets, up to 12 cached targets keyed
-// by tag, shape, dtype, mode and device, one grouped completion for tagged
-// Q/K/V) and "Additional Notes" (no protocol switch once a grouped transfer
+// streaming", "Changes Made" (final-layout targets; a bounded cache of at most 12 target
+// sets, keyed on the tag, the shape, the dtype, a mode and the device; one
+// grouped completion for tagged Q/K/V) and "Additional Notes" (no protocol switch once a grouped transfer
 // started -- here: nothing is launched unless every check passed); TeleFuser PR
 // #22 (RoPE tables kept resident); TeleFuser docs "Communication Architecture",
 // "Cross-Worker Tensor Channel" (slot reuse ordered by an event, no device-wide
@@ -53,7 +53,7 @@ tf_status cuda_fail(cudaError_t e, const char* what) {
 // ---------------------------------------------------------------- stream capture
 // CUDA-graph capture protocol (flashinfer PR #6332 commit message, "Description",
 // "CUDA graphs": a prepared call allocates nothing; a size first seen inside a
-// capture raises instead of allocating; captured calls interleave with eager
+// capture fails rather than allocate; captured calls interleave with eager
 // ones).  Inside a capture the library allocates and frees nothing, records its
 // events as external event nodes (so every replay records them) and waits on
 // events recorded outside the capture as external waits.
