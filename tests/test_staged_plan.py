@@ -39,10 +39,10 @@ int main() {
     if (rb > stage) { if (rpu != 0) ++bad; continue; }
     if (rpu == 0 || uint64_t(rpu) * rb > stage) { ++bad; continue; }
     if (uint64_t(Hl) * rb <= stage && rpu % Hl != 0) { ++bad; continue; }  // whole tokens
-    // the stage choice: the small ring only for bands under 3 KiB on launches over 128 MiB
-    const uint32_t big = staged_stage_bytes(uint64_t(Hl) * rb, rb, uint64_t(200) << 20);
+    // the stage choice: the small ring only for bands under 3 KiB on launches over 288 MiB
+    const uint32_t big = staged_stage_bytes(uint64_t(Hl) * rb, rb, uint64_t(320) << 20);
     if (big != ((uint64_t(Hl) * rb >= 3072 || rb > kStageBytesSmall) ? kStageBytes : kStageBytesSmall)) ++bad;
-    if (staged_stage_bytes(uint64_t(Hl) * rb, rb, uint64_t(64) << 20) != kStageBytes) ++bad;
+    if (staged_stage_bytes(uint64_t(Hl) * rb, rb, uint64_t(288) << 20) != kStageBytes) ++bad;
     const int64_t extent = int64_t(Sl - 1) * st + band;
     for (uint32_t R0 = 0; R0 < rows; R0 += rpu) {
       const uint32_t R1 = R0 + rpu < rows ? R0 + rpu : rows;

@@ -25,7 +25,7 @@ namespace tfu {
 // Two stage rings, chosen per launch by the planner (units of at most the ring's
 // stage size; the kernel takes the ring whose stages fit the planned unit):
 //  * kStageBytes (64 KiB) x 3, one unit loaded ahead: token head bands of 3 KiB
-//    or more, and launches of at most 128 MiB per direction;
+//    or more, and launches of at most 288 MiB per direction;
 //  * kStageBytesSmall (32 KiB) x 6, two units ahead: the rest.
 // Measured on GB300 (fractions of the copy peak): 64 KiB units raise the 72 MB
 // FLUX-like copy scatter to 0.85 (0.77) and 64 MiB single-tensor relayouts to
@@ -76,13 +76,17 @@ __host__ __device__ inline uint32_t tma_rows_per_unit(uint32_t Hl, uint32_t row_
 
 // The stage size the planner uses for a pure relayout whose token head band is
 // `band` bytes, moving `bytes_per_direction` bytes: the large ring for bands of
-// 3 KiB or more, for launches of at most 128 MiB per direction, and for rows
+// 3 KiB or more, for launches of at most 288 MiB per direction, and for rows
 // that do not fit the small stage; the small ring otherwise.
 #ifndef TFU_LARGE_RING_BAND
 #define TFU_LARGE_RING_BAND 3072  // head bands from this many bytes take the large ring
 #endif
 #ifndef TFU_LARGE_RING_MAX_MIB
-#define TFU_LARGE_RING_MAX_MIB 128  // launches up to this many MiB per direction take the large ring
+// launches up to this many MiB per direction take the large ring: 288 measured
+// gathers of 1.5-2 KiB bands at 141 MiB 0.93 / 0.97 of the copy peak against
+// 0.89 / 0.93 at 128, and 2 KiB bands at 256 MiB 0.97-0.98 against 0.95-0.97;
+// the video-DiT gather (2.5 KiB bands, 320 MiB) keeps the small ring
+#define TFU_LARGE_RING_MAX_MIB 288
 #endif
 __host__ __device__ inline uint32_t staged_stage_bytes(uint64_t band, uint32_t row_bytes,
                                                        uint64_t bytes_per_direction) {
