@@ -76,10 +76,12 @@ __host__ __device__ constexpr int block_min_blocks() {
 #endif
 #ifndef TFU_STREAM_MAX_ROUNDS
 // V+Q+K fused launches stream only while the grid walks at most this many rounds
-// of units: streaming measured +7 % at 5 rounds (P=4, S=4096, H=24), +2 % at 20,
-// but -1.3 to -2 % at 40-81 rounds (video DiT, S=32760 at H=48); copy and
-// Q/K-only launches gained at every size (video-DiT copy scatter +2.6 %)
-#define TFU_STREAM_MAX_ROUNDS 24
+// of units.  Streaming measured (P=4, H=24, D=128, read-flushed fractions of the
+// copy peak) +7 % at 5 and 10 rounds, +4 % at 20, +2 % at 25-35 and nothing at
+// 40-60; but -1.3 to -2 % at 40-81 rounds with wider head bands (the video DiT,
+// 67 rounds; S=32760 at H=48).  Copy and Q/K-only launches gained at every size
+// (video-DiT copy scatter +2.6 %).
+#define TFU_STREAM_MAX_ROUNDS 36
 #endif
 
 template <Fused kF, int kLanes, int kCopy, int kNF, bool kNeox, bool kStream>
