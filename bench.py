@@ -16,10 +16,10 @@ inputs are larger than the 129 MB L2).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-``--impl reference`` times the CPU oracle (the reference arm of this build) on
-a bounded token-sample of the same workload.  N>1 (torchrun) runs independent
-replicas, one per GPU ("replicas only": the path has no cross-GPU exchange on
-one box).
+``--impl reference`` times the CPU oracle (the reference arm) on a bounded
+token-sample of the same workload.  N>1 (torchrun) runs independent replicas,
+one per GPU ("replicas only": all P shards of the relayout live in one GPU's
+memory, so the path has no cross-GPU exchange).
 """
 from __future__ import annotations
 
