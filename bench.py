@@ -362,13 +362,15 @@ def run_e2e(args, torch, binding, src, wq, wk, w, stream, dev, world, step_paylo
         torch.cuda.synchronize(dev)
         return c0.elapsed_time(c1)
 
-    # five interleaved repeats of each; the medians are reported (the host link is
-    # shared with the rest of the machine, and a window can catch other traffic)
+    # five interleaved repeats of each (the host link is shared with the rest of
+    # the machine, and a window can catch other traffic): the e2e median, and the
+    # copies' best as the link's ceiling -- their median has come out both above
+    # and below the e2e time on different boxes (2.0x once), so it bounds nothing
     e2e_runs, copy_runs = [], []
     for _ in range(5):
         e2e_runs.append(time_e2e())
         copy_runs.append(time_copies())
-    e2e_ms, copy_ms = statistics.median(e2e_runs), statistics.median(copy_runs)
+    e2e_ms, copy_ms = statistics.median(e2e_runs), min(copy_runs)
     if world > 1:
         e2e_ms = max_over_ranks(torch, dist, e2e_ms, dev)
         copy_ms = max_over_ranks(torch, dist, copy_ms, dev)
@@ -377,12 +379,13 @@ def run_e2e(args, torch, binding, src, wq, wk, w, stream, dev, world, step_paylo
             "steps": args.e2e_steps, "repeats_gbs": [aggregate_gbs(world, step_payload, args.e2e_steps, m)
                                                     for m in e2e_runs],
             "host_link": {"copies_only_ms_per_step": copy_ms / args.e2e_steps,
+                          "copies_only_repeats_ms_per_step": [m / args.e2e_steps for m in copy_runs],
                           "gbs_per_direction": max(h2d, d2h) / (copy_ms / args.e2e_steps / 1e3) / 1e9,
                           "e2e_frac_of_copies_only": copy_ms / e2e_ms},
             "note": "pinned host Q/K/V/attention inputs copied in, all targets and outputs copied out, every "
                     "step; V uploaded contiguous; upload, calls and download of consecutive steps overlap on "
                     "three streams (two buffer sets); median of five repeats of the timed steps, interleaved "
-                    "with five repeats of host_link: the same copies without the calls"}
+                    "with five repeats of host_link: the same copies without the calls (best repeat)"}
 
 
 def main():
