@@ -35,6 +35,10 @@ thread_local std::string g_last_error;
 std::atomic<uint64_t> g_launches{0};
 std::atomic<uint64_t> g_allocs{0};  // device allocations made (cache entries, tables)
 std::mutex g_mu;  // guards the cache, the tables and the allocator
+// The relayout launchers fill per-kernel launch facts (occupancy, the shared-memory
+// opt-in) into function-local statics on first use; calls that launch without
+// g_mu serialise on this one, which is never held while taking g_mu.
+std::mutex g_launch_mu;
 
 tf_status fail(tf_status s, const char* fmt, ...) {
     char buf[512];
@@ -308,13 +312,16 @@ tf_status launch_planned(RelayoutParams& p, const Shape& sh, tfu::Dir dir, tfu::
         const uint32_t passes = TFU_BLOCK_PASSES > 0 ? TFU_BLOCK_PASSES : (p.nx >= 3 ? 1u : 2u);
         const uint32_t unit_rows = uint32_t(tfu::kThreads) / p.vpr * depth * passes;
         if ((s = plan_rows(uint64_t(sh.B) * sh.P * sh.P, unit_rows)) != TF_OK) return s;
+        std::lock_guard<std::mutex> launch_lock(g_launch_mu);
         e = tfu::launch_blocks(p, fused, stream);
     } else if (staged_ok && rpu > 0) {
         if ((s = plan_rows(uint64_t(sh.B) * sh.P * p.nx * sh.P, rpu)) != TF_OK) return s;
+        std::lock_guard<std::mutex> launch_lock(g_launch_mu);
         e = tfu::launch_relayout_staged(p, dir, fused, stream);
     } else {
         p.vec_bytes = fused != tfu::Fused::kNone ? 16 : vec;  // the register kernel's fused rows use 16 bytes
         if ((s = plan_units(p, sh)) != TF_OK) return s;
+        std::lock_guard<std::mutex> launch_lock(g_launch_mu);
         e = tfu::launch_relayout(p, dir, fused, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "launching the relayout kernel");
