@@ -211,6 +211,13 @@ def check_rmsnorm_vs_torch(lib):
             x[0] = 0  # zero row: 0 * 1/sqrt(eps) = 0
             x[1] = 3.0  # constant row
             x[2] *= 1e-3  # tiny row, where eps matters
+            # rows whose squares are fp32 subnormals or vanish, and subnormal inputs:
+            # the mean is negligible next to eps, so y = x / sqrt(eps) rounded
+            x[3] = (torch.randn((D,), generator=gen) * 2.0 ** -70).to(dtype)
+            frac_bits = 7 if dtype == torch.bfloat16 else 10
+            mag = torch.randint(0, 1 << frac_bits, (D,), generator=gen, dtype=torch.int32)
+            sign = torch.randint(0, 2, (D,), generator=gen, dtype=torch.int32) << 15
+            x[4] = (sign | mag).to(torch.int16).view(dtype)  # exponent field 0: zeros and subnormals
             wq, _ = synth.norm_weights(D, dtype, seed=9)
             ones = torch.ones(D, dtype=dtype)
             ident = oracle.rope_table(10000.0, 1, D, lib=lib)[0]  # p = 0: no rotation
@@ -242,6 +249,102 @@ def check_rmsnorm_closed_forms(lib):
         x = torch.randn((D,), generator=gen).to(dtype)
         got = oracle.rmsnorm_rope_row(x, ones, eps, ident, lib=lib).double()
         assert abs(float(got.pow(2).mean().sqrt()) - 1.0) < 2 ** -7
+
+
+def check_rmsnorm_large_magnitudes(lib):
+    """Rows whose squares overflow fp32 (bf16 reaches 3.4e38; any |x| >= 2^64 has
+    a square beyond fp32).  The fused path's RMSNorm is fp32 (flashinfer PR #6332,
+    "Assumptions / Operator math"); its mean of squares is the exact mean rounded
+    once to fp32.  Fixed by the mathematics, independently of that code:
+      * RMSNorm is invariant under x -> 2^k x while the mean stays in fp32's normal
+        range and far above eps (the scaling is exact at every step), so rows of
+        rms ~2^6 scaled by up to 2^57 -- single squares up to ~2^130 -- give the
+        same bits as the unscaled row, whose values torch's rms_norm pins;
+      * a row (c, 0, ..., 0) normalises to sqrt(D) at element 0 whatever c, while
+        c^2/D fits fp32;
+      * once the mean itself exceeds fp32 it is +inf, 1/sqrt(inf) = 0 and the row
+        is all zeros -- what torch's fp32 rms_norm returns for such rows too."""
+    eps, D = 1e-6, 128
+    dtype = torch.bfloat16
+    tab = oracle.rope_table(10000.0, 40, D, lib=lib)
+    wq, _ = synth.norm_weights(D, dtype, seed=31)
+    gen = synth.make_generator(44, "cpu")
+    for trial in range(6):
+        x = (torch.randn((D,), generator=gen) * 64.0).to(dtype)
+        for p in (0, 7, 39):
+            for style in oracle.ROPE_STYLES:
+                base = oracle.rmsnorm_rope_row(x, wq, eps, tab[p], lib=lib, style=style)
+                for k in (1, 20, 40, 56, 57):
+                    xs = x * (2.0 ** k)  # exact: a power of two, no bf16 overflow (|x| < 2^66)
+                    assert torch.equal((xs.float() / 2.0 ** k).to(dtype).view(torch.int16), x.view(torch.int16))
+                    got = oracle.rmsnorm_rope_row(xs, wq, eps, tab[p], lib=lib, style=style)
+                    assert torch.equal(got.view(torch.int16), base.view(torch.int16)), (trial, p, style, k)
+    ones = torch.ones(D, dtype=dtype)
+    ident = tab[0]
+    spike_ref = None
+    for e in (10, 40, 64, 67):  # c^2 / D = 2^(2e - 7) <= 2^127
+        x = torch.zeros(D, dtype=dtype)
+        x[0] = 2.0 ** e
+        got = oracle.rmsnorm_rope_row(x, ones, eps, ident, lib=lib)
+        assert torch.all(got[1:].float() == 0), e
+        assert abs(float(got[0]) - math.sqrt(D)) <= math.sqrt(D) * 2 ** -8, (e, float(got[0]))
+        spike_ref = got if spike_ref is None else spike_ref
+        assert torch.equal(got.view(torch.int16), spike_ref.view(torch.int16)), e
+    # the largest constant whose square fits fp32: mean = c^2, y = c / sqrt(c^2) = 1
+    c = float(torch.tensor(2.0 ** 63 * 255 / 128, dtype=dtype))
+    x = torch.full((D,), c, dtype=dtype)
+    got = oracle.rmsnorm_rope_row(x, ones, eps, ident, lib=lib)
+    assert torch.all(got.float() == 1.0), got[:4]
+    # means beyond fp32: zeros, as torch's fp32 rms_norm gives
+    bf16_max = torch.tensor(0x7F7F, dtype=torch.int16).view(torch.bfloat16).item()
+    rows = [torch.full((D,), v, dtype=dtype) for v in (2.0 ** 64, -(2.0 ** 70), 2.0 ** 100, bf16_max)]
+    spike = torch.zeros(D, dtype=dtype)
+    spike[5] = 2.0 ** 68  # c^2 / D = 2^129
+    rows.append(spike)
+    for x in rows:
+        for w in (ones, wq):
+            got = oracle.rmsnorm_rope_row(x, w, eps, ident, lib=lib)
+            assert torch.all(got.float() == 0), (float(x.abs().max()), got[:4])
+            want = _rms_norm_torch(x.unsqueeze(0), w, eps)[0]
+            assert torch.all(want.float() == 0)
+            for style in oracle.ROPE_STYLES:
+                rot = oracle.rmsnorm_rope_row(x, w, eps, tab[9], lib=lib, style=style)
+                assert torch.all(rot.float() == 0), style
+
+
+def check_rmsnorm_non_finite_rows(lib):
+    """The reading for infinite and NaN inputs, which the pages do not address,
+    taken from IEEE fp32 arithmetic at each step of the fp32 RMSNorm: a NaN makes
+    the mean NaN, so the whole row is NaN; an infinite element (no NaN) makes the
+    mean +inf and 1/sqrt(+inf) = 0, so every finite element normalises to zero
+    and the infinite one to inf * 0 = NaN, which the rotation then also gives to
+    its partner (the pair's other element)."""
+    eps, D, p = 1e-6, 64, 5
+    tab = oracle.rope_table(10000.0, 8, D, lib=lib)
+    gen = synth.make_generator(45, "cpu")
+    for dtype in (torch.bfloat16, torch.float16):
+        w, _ = synth.norm_weights(D, dtype, seed=32)
+        for i in (0, 1, 17, 40, 63):
+            base = torch.randn((D,), generator=gen).to(dtype)
+            x = base.clone()
+            x[i] = float("nan")
+            for style in oracle.ROPE_STYLES:
+                got = oracle.rmsnorm_rope_row(x, w, eps, tab[p], lib=lib, style=style)
+                assert torch.all(torch.isnan(got.float())), (dtype, i, style)
+            for inf in (float("inf"), float("-inf")):
+                x = base.clone()
+                x[i] = inf
+                for style in oracle.ROPE_STYLES:
+                    partner = i ^ 1 if style == "interleaved" else (i + D // 2) % D
+                    got = oracle.rmsnorm_rope_row(x, w, eps, tab[p], lib=lib, style=style).float()
+                    nan = torch.isnan(got)
+                    assert bool(nan[i]) and bool(nan[partner]) and int(nan.sum()) == 2, (dtype, i, style)
+                    rest = torch.ones(D, dtype=torch.bool)
+                    rest[[i, partner]] = False
+                    assert torch.all(got[rest] == 0), (dtype, i, style)
+                x[(i + 3) % D] = float("nan")
+                got = oracle.rmsnorm_rope_row(x, w, eps, tab[p], lib=lib).float()
+                assert torch.all(torch.isnan(got)), (dtype, i)
 
 
 def _rotate_complex(z: torch.Tensor, angles: torch.Tensor) -> torch.Tensor:
@@ -491,6 +594,8 @@ ALL_CHECKS = [
     check_rope_table_textbook,
     check_rmsnorm_vs_torch,
     check_rmsnorm_closed_forms,
+    check_rmsnorm_large_magnitudes,
+    check_rmsnorm_non_finite_rows,
     check_rope_vs_complex,
     check_fused_scatter_composition,
     check_neox_vs_interleaved_reordering,

@@ -66,3 +66,14 @@ def assert_fused_ok(got, want, max_flip_fraction=1e-5):
     assert st["ok"], st
     assert st["n_bit_diff"] <= max(2, int(st["n"] * max_flip_fraction)), st
     return st
+
+
+def assert_fused_ok_nonfinite(got, want, max_flip_fraction=1e-5):
+    """assert_fused_ok for outputs that may hold NaN: every NaN of the oracle must
+    be a NaN in ``got`` and nothing else may be (a NaN's bits are not compared);
+    the other elements follow assert_fused_ok."""
+    got, want = got.cpu(), want.cpu()
+    gn, wn = torch.isnan(got.float()), torch.isnan(want.float())
+    assert torch.equal(gn, wn), ("NaN positions differ", int((gn & ~wn).sum()), int((wn & ~gn).sum()))
+    keep = ~wn
+    return assert_fused_ok(got[keep], want[keep], max_flip_fraction)

@@ -28,7 +28,8 @@ def test_unstreamed_block_kernel_parity(tmp_path):
     lib = build.build(defines=["TFU_BLOCK_STREAM=0"], out=str(tmp_path / "libtf_ulysses.so"))
     env = dict(os.environ, TF_ULYSSES_LIBRARY=lib)
     files = [os.path.join(ROOT, "tests", f)
-             for f in ("test_gpu_fuzz.py", "test_gpu_layouts_neox.py", "test_gpu_parity.py", "test_gpu_chunks.py")]
+             for f in ("test_gpu_fuzz.py", "test_gpu_layouts_neox.py", "test_gpu_parity.py", "test_gpu_chunks.py",
+                       "test_gpu_edge_values.py")]
     cmd = [sys.executable, "-m", "pytest", *files, "-x", "-q", "-m", "gpu", "-p", "no:cacheprovider",
            "-k", "not video_dit and not full_size and not large"]
     r = subprocess.run(cmd, env=env, cwd=ROOT, capture_output=True, text=True, timeout=1200)

@@ -17,6 +17,8 @@ MUTANTS = {
     "gather_token_block_of_group": ("((int64_t)r * Sl + t) * at", "((int64_t)g * Sl + t) * at"),
     "rmsnorm_drops_eps": ("sqrtf(ms + eps)", "sqrtf(ms)"),
     "rmsnorm_sum_not_mean": ("(float)(ss / D)", "(float)(ss)"),
+    "rmsnorm_squares_in_fp32": ("ss += (double)xf[d] * (double)xf[d];", "ss += (double)(xf[d] * xf[d]);"),
+    "rmsnorm_mean_clamped_to_fp32": ("float ms = (float)(ss / D);", "float ms = (float)fmin(ss / D, FLT_MAX);"),
     "rmsnorm_no_cast_before_scale": ("y[d] = round16(fmt, prod);", "y[d] = prod;"),
     "rmsnorm_weight_dropped": ("y[d] * (float)tfo_decode16(fmt, w[d])", "y[d] * 1.0f"),
     "rope_wrong_sign": ("(double)(ac - bs)", "(double)(ac + bs)"),

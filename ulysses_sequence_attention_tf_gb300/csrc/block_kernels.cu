@@ -30,6 +30,8 @@
 //    same code writes the separate [B, S, Hl, D] targets, the fused receive
 //    layout [B, S, Hl, 3*D] (d_h = 3*D*esize, slot offsets 0, D, 2D) and a head
 //    chunk of wider targets (d_t > Hl*d_h; source bands Hg heads apart).
+#include <type_traits>
+
 #include "device_common.cuh"
 #include "relayout.h"
 
@@ -70,14 +72,6 @@ __host__ __device__ constexpr int block_min_blocks() {
     return kNF == 0 ? TFU_COPY_BLOCK_MIN_BLOCKS : (kCopy == 0 ? TFU_QK_MIN_BLOCKS : TFU_FUSED_MIN_BLOCKS);
 }
 
-#ifndef TFU_BLOCK_SMEM_WEIGHTS
-// 1: each fused slot's RMSNorm weights by lane position in 512 bytes of shared
-// memory rather than 16 registers per lane -- the V+Q+K kernel then fits 126
-// registers without spilling (128 with 24 bytes spilled from registers), and
-// measured 6432-6452 GB/s fused (6383), 6336-6340 half-split (6182) on the
-// video-DiT scatter.  0: registers.
-#define TFU_BLOCK_SMEM_WEIGHTS 1
-#endif
 #ifndef TFU_BLOCK_STREAM
 // 1: each row group streams the rows of all its units (next unit's loads during
 // the last pass of the one before); 0: one unit at a time
@@ -138,9 +132,11 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
         st_stream<16>(row, lo);
         st_stream<16>(row + kHalf, hi);
     };
-#if TFU_BLOCK_SMEM_WEIGHTS
     // the weight pairs of each fused slot by lane position, in shared memory
     __shared__ uint32_t w_all[kNF > 0 ? kNF : 1][kLanes][NP];
+    // set when a row's sum of squares was not finite: the fused rows are computed again below
+    __shared__ int redo;
+    if (threadIdx.x == 0) redo = 0;
     if (threadIdx.x < kLanes) {
         const uint32_t lp = threadIdx.x;
 #pragma unroll
@@ -154,18 +150,6 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
     }
     __syncthreads();
     auto w = [&](int f) -> const uint32_t(&)[NP] { return w_all[f][dv]; };
-#else
-    uint32_t w_reg[kNF > 0 ? kNF : 1][NP];  // this lane's weight pairs of each fused slot
-#pragma unroll
-    for (int f = 0; f < kNF; ++f) {
-        const uint8_t* wrow = static_cast<const uint8_t*>(p.weight[kCopy + f]);
-        const uint4 a = *reinterpret_cast<const uint4*>(wrow + (kNeox ? dv * 16 : dv * VW));
-        const uint4 b = *reinterpret_cast<const uint4*>(wrow + (kNeox ? kHalf + dv * 16 : dv * VW + 16));
-        w_reg[f][0] = a.x, w_reg[f][1] = a.y, w_reg[f][2] = a.z, w_reg[f][3] = a.w;
-        w_reg[f][4] = b.x, w_reg[f][5] = b.y, w_reg[f][6] = b.z, w_reg[f][7] = b.w;
-    }
-    auto w = [&](int f) -> const uint32_t(&)[NP] { return w_reg[f]; };
-#endif
     // A group's rows of one unit: plane rows [beg, end) (empty for trailing
     // groups) and the pipeline slots that walk them (a multiple of kDepth)
     struct Span {
@@ -194,6 +178,15 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
 #pragma unroll
     for (int k = 0; k < kCs; ++k) cs[k] = make_float4(1.f, 0.f, 1.f, 0.f);
     uint32_t t_cached = 0xffffffffu;
+    // RMSNorm + weight + RoPE of the lane's part of one row of fused slot f
+    auto fused_row = [&](auto exact, uint32_t(&xw)[NP], int f) {
+        constexpr bool kExact = decltype(exact)::value;
+        if constexpr (kNeox) {
+            norm_rope_core_split<kF, kLanes, NP, kExact>(xw, w(f), cs, p.eps, &redo);
+        } else {
+            norm_rope_core<kF, kLanes, NP, false, kExact>(xw, w(f), cs, p.eps, &redo);
+        }
+    };
     auto set_src = [&]() {
 #pragma unroll
         for (int x = 0; x < kSlots; ++x) {
@@ -236,13 +229,7 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
             }
             // every lane runs the row reductions (they shuffle); only valid rows are written
 #pragma unroll
-            for (int f = 0; f < kNF; ++f) {
-                if constexpr (kNeox) {
-                    norm_rope_core_split<kF, kLanes, NP>(buf[kCopy + f].w, w(f), cs, p.eps);
-                } else {
-                    norm_rope_core<kF, kLanes, NP>(buf[kCopy + f].w, w(f), cs, p.eps);
-                }
-            }
+            for (int f = 0; f < kNF; ++f) fused_row(std::false_type{}, buf[kCopy + f].w, f);
         }
         if (valid) {  // the scatter targets of one launch share their strides (slot 0's)
             const int64_t off = int64_t(t) * p.d_t[0] + int64_t(h) * p.d_h[0];
@@ -305,6 +292,45 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
                 for (int d = 0; d < kDepth; ++d) {
                     compute_store(bufs[d], R + d, sp.end);
                     load(bufs[d], R + d + kDepth, sp.end);
+                }
+            }
+        }
+    }
+    if constexpr (kNF > 0) {
+        // A row whose sum of squares was not finite (an element of magnitude >=
+        // 2^64, an infinite one or a NaN) was stored with the fast mean.  If the
+        // CTA met one, every row group walks its rows of the fused slots once
+        // more, one row at a time, with the complete mean; each row is rewritten
+        // by the lanes that stored it, after their first store.
+        __syncthreads();
+        if (redo) {
+#pragma unroll 1
+            for (uint32_t u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+                const Span sp = locate(u);
+                set_src();
+                set_dst();
+#pragma unroll 1
+                for (uint32_t R = sp.beg; R < sp.beg + sp.slots; ++R) {
+                    const bool valid = R < sp.end;
+                    const uint32_t t = fastdiv(R, p.div_hl);
+                    const uint32_t h = R - t * p.Hl;
+                    if (valid && t != t_cached) {
+                        const float* tab = tab_lane + size_t(t) * kRowFloats;
+#pragma unroll
+                        for (int k = 0; k < kCs; ++k) cs[k] = ld_table(tab + 4 * k);
+                        t_cached = t;
+                    }
+#pragma unroll
+                    for (int f = 0; f < kNF; ++f) {
+                        constexpr int x0 = kCopy;
+                        Vec<VW> v;
+#pragma unroll
+                        for (int k = 0; k < NP; ++k) v.w[k] = 0u;
+                        if (valid) v = ld_lane(src[x0 + f] + int64_t(t) * p.s_t[x0 + f] + int64_t(h) * p.s_h[x0 + f],
+                                               x0 + f);
+                        fused_row(std::true_type{}, v.w, f);
+                        if (valid) st_lane(dst[x0 + f] + int64_t(t) * p.d_t[0] + int64_t(h) * p.d_h[0], x0 + f, v);
+                    }
                 }
             }
         }

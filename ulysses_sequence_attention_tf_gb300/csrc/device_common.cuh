@@ -142,14 +142,6 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
     e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
-// TFU_EXACT_SUMSQ 1: the row's sum of squares is carried as an unevaluated pair
-// hi + lo (TwoSum), so its fp32 rounding is the correctly rounded sum for
-// ordinary inputs and the whole fused path matches a step-by-step evaluation
-// bit for bit.  0: a plain fp32 FMA chain (rare 1-ulp output differences).
-#ifndef TFU_EXACT_SUMSQ
-#define TFU_EXACT_SUMSQ 1
-#endif
-
 // ---- packed fp32 pairs (sm_100+ f32x2 arithmetic: each lane of the pair is an
 // ordinary IEEE round-to-nearest fp32 operation; one instruction issues both) ----
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
@@ -182,6 +174,106 @@ __device__ __forceinline__ void f2_two_sum(uint64_t a, uint64_t b, uint64_t& s, 
     e = f2_add(f2_sub(a, f2_sub(s, bb)), f2_sub(b, bb));
 }
 
+// ---- the row's mean of squares (RMSNorm), fp32 ----
+// The mean is the fp32 rounding of the exact mean of the squares: squares of
+// 16-bit values are exact in fp32, and their sum is carried as an unevaluated
+// float pair hi + lo (TwoSum), so fl(hi + lo) is the correctly rounded sum for
+// ordinary inputs and the mean follows by an exact power-of-two scaling.
+
+// Sum of the squares of the lane's values, reduced over the row's kLanes
+// lanes; every lane of the group ends with the same pair hi + lo.
+template <Fused kF, int kLanes, int NP>
+__device__ __forceinline__ void row_sumsq(const uint32_t (&xw)[NP], float& hi, float& lo) {
+    auto sq = [&](int j) {
+        float a, b;
+        unpack2<kF>(xw[j], a, b);
+        const uint64_t v = f2_pack(a, b);
+        return f2_mul(v, v);
+    };
+    // two interleaved float-pair accumulators (even and odd elements), then one
+    // TwoSum to combine them
+    uint64_t hi2 = sq(0), lo2 = 0;
+#pragma unroll
+    for (int j = 1; j < NP; ++j) {
+        uint64_t s, e;
+        f2_two_sum(hi2, sq(j), s, e);
+        hi2 = s;
+        lo2 = f2_add(lo2, e);
+    }
+    {
+        float he, ho, le, lo_, e;
+        f2_unpack(hi2, he, ho);
+        f2_unpack(lo2, le, lo_);
+        two_sum(he, ho, hi, e);
+        lo = __fadd_rn(__fadd_rn(le, lo_), e);
+    }
+#pragma unroll
+    for (int m = 1; m < kLanes; m <<= 1) {  // both partners compute the same pair
+        const float ohi = __shfl_xor_sync(0xffffffffu, hi, m);
+        const float olo = __shfl_xor_sync(0xffffffffu, lo, m);
+        float s, e;
+        two_sum(hi, ohi, s, e);
+        lo = __fadd_rn(__fadd_rn(lo, olo), e);
+        hi = s;
+    }
+}
+
+constexpr float kFltMax = 3.40282347e38f;
+
+// The fp32 mean of the squares of a head row of D = 2 * kLanes * NP values.
+// A float-pair sum that is not finite means an element of magnitude >= 2^64
+// (its square, or the sum, overflowed fp32), an infinite element or a NaN.
+//  * kExact = false (the pipelined loops): such a row only sets the flag *redo
+//    (in shared memory: nothing held in registers across the loops) -- the mean
+//    returned is then not the row's, and the caller computes the row again with
+//    kExact = true before it is final.
+//  * kExact = true: the lanes of such a row -- the condition is uniform within
+//    the row's lane group, whose lanes all hold the same pair -- sum the squares
+//    of the row scaled by 2^-96 (exact), one scalar pair per lane and shuffles
+//    among the group's lanes only, and scale the mean back up by 2^192 in two
+//    exact steps: the correctly rounded mean, or +inf when the mean itself
+//    exceeds the fp32 range.  An infinite element gives +inf, a NaN NaN.
+template <Fused kF, int kLanes, int NP, bool kExact>
+__device__ __forceinline__ float row_mean_sq(const uint32_t (&xw)[NP], volatile int* redo) {
+    constexpr float kInvD = 1.0f / float(kLanes * NP * 2);  // D is a power of two: exact scaling
+    float hi, lo;
+    row_sumsq<kF, kLanes, NP>(xw, hi, lo);
+    if constexpr (!kExact) {
+        if (!(hi <= kFltMax)) *redo = 1;
+        return __fmul_rn(__fadd_rn(hi, lo), kInvD);
+    } else {
+        if (hi <= kFltMax) return __fmul_rn(__fadd_rn(hi, lo), kInvD);
+        hi = 0.f;
+        lo = 0.f;
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            float v[2], s, e;
+            unpack2<kF>(xw[j], v[0], v[1]);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const float a = __fmul_rn(v[k], 0x1p-96f);
+                two_sum(hi, __fmul_rn(a, a), s, e);
+                lo = __fadd_rn(lo, e);
+                hi = s;
+            }
+        }
+        const uint32_t lane = threadIdx.x & 31u;
+        const uint32_t group =
+            kLanes >= 32 ? 0xffffffffu : ((1u << (kLanes & 31)) - 1u) << (lane & ~uint32_t(kLanes - 1));
+#pragma unroll
+        for (int m = 1; m < kLanes; m <<= 1) {
+            const float ohi = __shfl_xor_sync(group, hi, m);
+            const float olo = __shfl_xor_sync(group, lo, m);
+            float s, e;
+            two_sum(hi, ohi, s, e);
+            lo = __fadd_rn(__fadd_rn(lo, olo), e);
+            hi = s;
+        }
+        if (!(hi <= kFltMax)) return hi;  // +inf (an infinite element) or NaN
+        return __fmul_rn(__fmul_rn(__fmul_rn(__fadd_rn(hi, lo), kInvD), 0x1p96f), 0x1p96f);
+    }
+}
+
 // (cos, sin) float4s one lane reads from a table row: interleaved pairs need one
 // entry per element pair (NP/2 float4s), half-split pairs one per element (NP).
 template <bool kNeox, int NP>
@@ -204,10 +296,11 @@ __device__ __forceinline__ uint32_t cs_lane_offset(uint32_t dv) {
 // matching weight pairs, cs the lane's (cos, sin) entries (cs_lane_offset).
 // RMSNorm, weight scale, then RoPE: interleaved pairs (2i, 2i+1), or with kNeox
 // half-split pairs (i, i + D/2), whose partner values come from lane dv ^ kLanes/2.
-template <Fused kF, int kLanes, int NP, bool kNeox = false>
+// kExact and `redo`: as in row_mean_sq.
+template <Fused kF, int kLanes, int NP, bool kNeox, bool kExact>
 __device__ __forceinline__ void norm_rope_core(uint32_t (&xw)[NP], const uint32_t (&wpk)[NP],
-                                               const float4 (&cs)[cs_vecs<kNeox, NP>()], float eps) {
-    constexpr float kInvD = 1.0f / float(kLanes * NP * 2);  // D is a power of two: exact scaling
+                                               const float4 (&cs)[cs_vecs<kNeox, NP>()], float eps, volatile int* redo) {
+    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(row_mean_sq<kF, kLanes, NP, kExact>(xw, redo), eps)));
     uint64_t x2[NP];  // the lane's values as fp32 pairs
 #pragma unroll
     for (int j = 0; j < NP; ++j) {
@@ -215,47 +308,6 @@ __device__ __forceinline__ void norm_rope_core(uint32_t (&xw)[NP], const uint32_
         unpack2<kF>(xw[j], a, b);
         x2[j] = f2_pack(a, b);
     }
-#if TFU_EXACT_SUMSQ
-    // squares of 16-bit values are exact in fp32; two interleaved float-pair
-    // accumulators (even and odd elements), then one TwoSum to combine them
-    uint64_t hi2 = f2_mul(x2[0], x2[0]), lo2 = 0;
-#pragma unroll
-    for (int j = 1; j < NP; ++j) {
-        uint64_t s2, e2;
-        f2_two_sum(hi2, f2_mul(x2[j], x2[j]), s2, e2);
-        hi2 = s2;
-        lo2 = f2_add(lo2, e2);
-    }
-    float hi, lo;
-    {
-        float he, ho, le, lo_;
-        f2_unpack(hi2, he, ho);
-        f2_unpack(lo2, le, lo_);
-        float e;
-        two_sum(he, ho, hi, e);
-        lo = __fadd_rn(__fadd_rn(le, lo_), e);
-    }
-#pragma unroll
-    for (int m = 1; m < kLanes; m <<= 1) {  // both partners compute the same pair
-        const float ohi = __shfl_xor_sync(0xffffffffu, hi, m);
-        const float olo = __shfl_xor_sync(0xffffffffu, lo, m);
-        float s, e;
-        two_sum(hi, ohi, s, e);
-        lo = __fadd_rn(__fadd_rn(lo, olo), e);
-        hi = s;
-    }
-    const float ss = __fadd_rn(hi, lo);
-#else
-    uint64_t acc2 = 0;
-#pragma unroll
-    for (int j = 0; j < NP; ++j) acc2 = f2_add(acc2, f2_mul(x2[j], x2[j]));
-    float ae, ao;
-    f2_unpack(acc2, ae, ao);
-    float ss = __fadd_rn(ae, ao);
-#pragma unroll
-    for (int m = 1; m < kLanes; m <<= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, m));
-#endif
-    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(ss, kInvD), eps)));
     const uint64_t inv2 = f2_pack(inv, inv);
     if constexpr (!kNeox) {
 #pragma unroll
@@ -301,11 +353,11 @@ __device__ __forceinline__ void norm_rope_core(uint32_t (&xw)[NP], const uint32_
 // the lane's elements of the first half of the row, words [NP/2, NP) their
 // partners D/2 further on; cs[j] holds the (cos, sin) entries of the elements
 // of word j.  RMSNorm and weight scale as in norm_rope_core; the rotation pairs
-// never leave the lane.
-template <Fused kF, int kLanes, int NP>
+// never leave the lane.  kExact and `redo`: as in row_mean_sq.
+template <Fused kF, int kLanes, int NP, bool kExact>
 __device__ __forceinline__ void norm_rope_core_split(uint32_t (&xw)[NP], const uint32_t (&wpk)[NP],
-                                                     const float4 (&cs)[NP / 2], float eps) {
-    constexpr float kInvD = 1.0f / float(kLanes * NP * 2);
+                                                     const float4 (&cs)[NP / 2], float eps, volatile int* redo) {
+    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(row_mean_sq<kF, kLanes, NP, kExact>(xw, redo), eps)));
     uint64_t x2[NP];
 #pragma unroll
     for (int j = 0; j < NP; ++j) {
@@ -313,32 +365,6 @@ __device__ __forceinline__ void norm_rope_core_split(uint32_t (&xw)[NP], const u
         unpack2<kF>(xw[j], a, b);
         x2[j] = f2_pack(a, b);
     }
-    uint64_t hi2 = f2_mul(x2[0], x2[0]), lo2 = 0;
-#pragma unroll
-    for (int j = 1; j < NP; ++j) {
-        uint64_t s2, e2;
-        f2_two_sum(hi2, f2_mul(x2[j], x2[j]), s2, e2);
-        hi2 = s2;
-        lo2 = f2_add(lo2, e2);
-    }
-    float hi, lo;
-    {
-        float he, ho, le, lo_, e;
-        f2_unpack(hi2, he, ho);
-        f2_unpack(lo2, le, lo_);
-        two_sum(he, ho, hi, e);
-        lo = __fadd_rn(__fadd_rn(le, lo_), e);
-    }
-#pragma unroll
-    for (int m = 1; m < kLanes; m <<= 1) {
-        const float ohi = __shfl_xor_sync(0xffffffffu, hi, m);
-        const float olo = __shfl_xor_sync(0xffffffffu, lo, m);
-        float s, e;
-        two_sum(hi, ohi, s, e);
-        lo = __fadd_rn(__fadd_rn(lo, olo), e);
-        hi = s;
-    }
-    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(__fadd_rn(hi, lo), kInvD), eps)));
     const uint64_t inv2 = f2_pack(inv, inv);
     uint32_t z[NP];
 #pragma unroll

@@ -13,11 +13,7 @@ namespace tfu {
 
 constexpr int kGemmBM = 128;  // tile rows (tokens) = TMEM lanes
 constexpr int kGemmBN = 256;  // tile columns (features) = two heads of D = 128
-#ifndef TFU_GEMM_BK
-#define TFU_GEMM_BK 64  // K per stage: 64 (128-byte rows, 128-byte swizzle) or 32 (64-byte rows and swizzle)
-#endif
-constexpr int kGemmBK = TFU_GEMM_BK;
-static_assert(kGemmBK == 64 || kGemmBK == 32, "a stage row is one 128- or 64-byte swizzle span");
+constexpr int kGemmBK = 64;   // K per stage: one 128-byte row, the 128-byte swizzle span
 constexpr int kGemmHeadDim = 128;
 
 struct GemmParams {

@@ -36,6 +36,8 @@
 //  * Every mbarrier wait is bounded; a wait that gives up records a status bit,
 //    raises a shared abort flag, and the CTA drains its copies and MMAs (bounded)
 //    and frees its TMEM before returning.
+#include <atomic>
+
 #include <cudaTypedefs.h>
 
 #include "device_common.cuh"
@@ -49,13 +51,10 @@ namespace {
 
 using namespace dev;
 
-#ifndef TFU_GEMM_STAGES
-#define TFU_GEMM_STAGES (TFU_GEMM_BK == 64 ? 4 : 8)  // stages of 48 KiB (BK 64) or 24 KiB (BK 32)
-#endif
-constexpr int kStagesG = TFU_GEMM_STAGES;
-constexpr uint32_t kRowBytesG = kGemmBK * 2;          // one operand row of a stage: 128 or 64 bytes
-constexpr uint32_t kABytes = kGemmBM * kRowBytesG;     // 16 or 8 KiB
-constexpr uint32_t kBBytes = kGemmBN * kRowBytesG;     // 32 or 16 KiB
+constexpr int kStagesG = 4;                            // stages of 48 KiB (a fifth does not fit)
+constexpr uint32_t kRowBytesG = kGemmBK * 2;          // one operand row of a stage: 128 bytes
+constexpr uint32_t kABytes = kGemmBM * kRowBytesG;     // 16 KiB
+constexpr uint32_t kBBytes = kGemmBN * kRowBytesG;     // 32 KiB
 constexpr uint32_t kStageBytesG = kABytes + kBBytes;
 constexpr int kThreadsG = 192;
 constexpr uint32_t kTmemCols = 256;
@@ -179,14 +178,14 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 }
 
 // Shared-memory matrix descriptor of a K-major operand tile whose rows are
-// kRowBytesG bytes with the swizzle of the same span (128 or 64 bytes), 8-row
-// groups 8 * kRowBytesG bytes apart: start address >> 4 (bits 0-13), leading
-// byte offset (unused by these layouts, 1) at bits 16-29, stride byte offset at
-// bits 32-45, descriptor version 1 at bits 46-47, base offset 0 (tiles are
-// aligned to the swizzle pattern), swizzle mode at bits 61-63 (2 = 128-byte,
-// 4 = 64-byte).  A K step of 16 elements advances the start by 32 bytes.
+// 128 bytes with the 128-byte swizzle, 8-row groups 1024 bytes apart: start
+// address >> 4 (bits 0-13), leading byte offset (unused by this layout, 1) at
+// bits 16-29, stride byte offset at bits 32-45, descriptor version 1 at bits
+// 46-47, base offset 0 (tiles are aligned to the swizzle pattern), swizzle mode
+// 2 (128-byte) at bits 61-63.  A K step of 16 elements advances the start by 32
+// bytes.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
-    constexpr uint64_t kMode = kRowBytesG == 128 ? 2 : 4;
+    constexpr uint64_t kMode = 2;
     return uint64_t((smem_addr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t((8 * kRowBytesG) >> 4) << 32) |
            (uint64_t(1) << 46) | (kMode << 61);
 }
@@ -254,27 +253,48 @@ __device__ __forceinline__ void epilogue_head(uint32_t taddr, bool valid, bool n
         }
         return;
     }
-    float hi = 0.f, lo = 0.f;  // sum of squares of the rounded row: hi + lo exact
+    constexpr float kInvD = 1.0f / kGemmHeadDim;
+    // sum of squares of the rounded row (each value scaled by `scale`, a power of
+    // two): hi + lo exact unless it overflows
+    auto sumsq = [&](float scale, float& hi, float& lo) {
+        hi = 0.f;
+        lo = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-        uint32_t r[32], z[16];
-        tc_ld32(taddr + uint32_t(c * 32), r);
-        tc_wait_ld();
-        round_chunk(r, z);
+        for (int c = 0; c < 4; ++c) {
+            uint32_t r[32], z[16];
+            tc_ld32(taddr + uint32_t(c * 32), r);
+            tc_wait_ld();
+            round_chunk(r, z);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float a, b, s, e;
-            unpack2<Fused::kBF16>(z[i], a, b);
-            two_sum(hi, __fmul_rn(a, a), s, e);  // squares of bf16 values are exact in fp32
-            lo = __fadd_rn(lo, e);
-            hi = s;
-            two_sum(hi, __fmul_rn(b, b), s, e);
-            lo = __fadd_rn(lo, e);
-            hi = s;
+            for (int i = 0; i < 16; ++i) {
+                float a, b, s, e;
+                unpack2<Fused::kBF16>(z[i], a, b);
+                a = __fmul_rn(a, scale);
+                b = __fmul_rn(b, scale);
+                two_sum(hi, __fmul_rn(a, a), s, e);  // squares of bf16 values are exact in fp32
+                lo = __fadd_rn(lo, e);
+                hi = s;
+                two_sum(hi, __fmul_rn(b, b), s, e);
+                lo = __fadd_rn(lo, e);
+                hi = s;
+            }
         }
+    };
+    float hi, lo;
+    sumsq(1.0f, hi, lo);
+    float ms = __fmul_rn(__fadd_rn(hi, lo), kInvD);
+    // A sum that is not finite (an element of magnitude >= 2^64, an infinite one or
+    // a NaN): the row scaled by 2^-96 (exact) gives the mean, scaled back by 2^192
+    // in two exact steps (+inf when the mean exceeds the fp32 range).  TMEM loads
+    // are warp-collective, so the warp rescans when any of its rows needs it.
+    if (__any_sync(0xffffffffu, !(hi <= 3.40282347e38f))) {
+        float hs, ls;
+        sumsq(0x1p-96f, hs, ls);
+        if (!(hi <= 3.40282347e38f))
+            ms = hs <= 3.40282347e38f ? __fmul_rn(__fmul_rn(__fmul_rn(__fadd_rn(hs, ls), kInvD), 0x1p96f), 0x1p96f)
+                                      : hs;
     }
-    const float ss = __fadd_rn(hi, lo);
-    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(ss, 1.0f / kGemmHeadDim), eps)));
+    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
     if constexpr (!kNeox) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {  // pairs 16c .. 16c + 15, table entries likewise
@@ -350,35 +370,12 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// TMA load delivered to the same shared-memory offset (and mbarrier offset) of
-// every CTA in `mask`.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t smem_dst, const CUtensorMap* map, int x, int y, uint32_t bar,
-                                               uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, "
-        "%3}], [%4], %5;" ::"r"(smem_dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
-        : "memory");
-}
-// Arrive on the mbarrier at offset `bar` of every CTA in `mask` once this thread's
-// tcgen05 operations have completed.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
-                     "r"(bar),
-                 "h"(mask)
-                 : "memory");
-}
 
 constexpr uint32_t kAccBufs = 2;  // TMEM accumulators: the epilogue of tile i overlaps the MMAs of tile i+1
 
-// Persistent: cluster c (of kCluster CTAs) takes units c, c + clusters, ...; the
-// shared-memory stage ring and the two TMEM accumulators carry on from unit to
-// unit.  kCluster = 2: the two CTAs compute neighbouring row tiles of the same
-// column tile; each loads one 128-row half of the weight tile and multicasts it
-// to both, so a CTA pulls 32 KB instead of 48 KB per k-block through L2, and a
-// stage is refilled only after the MMAs of both CTAs have read it (their commits
-// arrive on both CTAs' stage barriers).
-template <bool kFusedT, bool kNeox, int kCluster>
+// Persistent: CTA c takes tiles c, c + gridDim.x, ...; the shared-memory stage
+// ring and the two TMEM accumulators carry on from tile to tile.
+template <bool kFusedT, bool kNeox>
 __global__ void __launch_bounds__(kThreadsG, 1) qkv_gemm_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -389,16 +386,14 @@ __global__ void __launch_bounds__(kThreadsG, 1) qkv_gemm_kernel(const __grid_con
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStagesG + 2 * kAccBufs + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const uint32_t rank = kCluster > 1 ? cluster_rank() : 0;
-    const uint32_t cid = blockIdx.x / kCluster, clusters = gridDim.x / kCluster;
-    const uint32_t units = (p.P * p.m_tiles + kCluster - 1) / kCluster * p.n_tiles;
+    const uint32_t cid = blockIdx.x, ctas = gridDim.x;
+    const uint32_t units = p.P * p.m_tiles * p.n_tiles;
     const uint32_t KB = p.K / kGemmBK;
-    constexpr uint16_t kAll = uint16_t((1u << kCluster) - 1u);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStagesG; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, kCluster);  // the MMAs of every CTA that holds the stage release it
+            mbar_init(empty0 + 8 * s, 1);  // the MMAs that read the stage release it
         }
         for (uint32_t a = 0; a < kAccBufs; ++a) {
             mbar_init(acc_full0 + 8 * a, 1);
@@ -415,7 +410,6 @@ __global__ void __launch_bounds__(kThreadsG, 1) qkv_gemm_kernel(const __grid_con
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if constexpr (kCluster > 1) cluster_sync();  // peers signal this CTA's barriers only once they exist
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -423,8 +417,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) qkv_gemm_kernel(const __grid_con
         // ---------------- TMA producer: one continuous stream of k-blocks
         uint32_t q = 0;  // k-blocks issued by this CTA
         bool ok = true;
-        for (uint32_t t = cid; ok && t < units; t += clusters) {
-            const Tile tl = decode_tile<kCluster>(p, t, rank);
+        for (uint32_t t = cid; ok && t < units; t += ctas) {
+            const Tile tl = decode_tile<1>(p, t, 0);
             const CUtensorMap* mx = &p.tmap_x[tl.r];
             for (uint32_t kb = 0; kb < KB; ++kb, ++q) {
                 const uint32_t s = q % kStagesG, use = q / kStagesG;
@@ -435,26 +429,17 @@ __global__ void __launch_bounds__(kThreadsG, 1) qkv_gemm_kernel(const __grid_con
                 const uint32_t a = smem_u32(smem + size_t(s) * kStageBytesG);
                 mbar_expect_tx(full0 + 8 * s, kStageBytesG);
                 tma_load_2d(a, mx, int(kb * kGemmBK), int(tl.m_tile * kGemmBM), full0 + 8 * s);
-                if constexpr (kCluster == 1) {
-                    tma_load_2d(a + kABytes, &p.tmap_w, int(kb * kGemmBK), int(tl.n_tile * kGemmBN), full0 + 8 * s);
-                } else {  // this CTA's half of the weight tile, into both CTAs
-                    const uint32_t half = kBBytes / kCluster;
-                    tma_load_2d_mc(a + kABytes + rank * half, &p.tmap_w_part, int(kb * kGemmBK),
-                                   int(tl.n_tile * kGemmBN + rank * (kGemmBN / kCluster)), full0 + 8 * s, kAll);
-                }
+                tma_load_2d(a + kABytes, &p.tmap_w, int(kb * kGemmBK), int(tl.n_tile * kGemmBN), full0 + 8 * s);
             }
         }
-        // the last load issued into each stage has landed, and (clusters) both CTAs'
-        // MMAs have released every stage, before the CTA exits
-        for (uint32_t k = q > uint32_t(kStagesG) ? q - kStagesG : 0; k < q; ++k) {
+        // the last load issued into each stage has landed before the CTA exits
+        for (uint32_t k = q > uint32_t(kStagesG) ? q - kStagesG : 0; k < q; ++k)
             drain_phase(full0 + 8 * (k % kStagesG), (k / kStagesG) & 1u);
-            if constexpr (kCluster > 1) drain_phase(empty0 + 8 * (k % kStagesG), (k / kStagesG) & 1u);
-        }
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer
         uint32_t q = 0, i = 0;
         bool ok = true;
-        for (uint32_t t = cid; ok && t < units; t += clusters, ++i) {
+        for (uint32_t t = cid; ok && t < units; t += ctas, ++i) {
             const uint32_t a = i % kAccBufs, u = i / kAccBufs;
             if (u > 0 && !wait_phase(acc_empty0 + 8 * a, (u - 1) & 1u, abort_flag)) break;  // epilogue drained it
             tc_fence_after();
@@ -470,12 +455,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) qkv_gemm_kernel(const __grid_con
 #pragma unroll
                 for (uint32_t kk = 0; kk < kGemmBK / 16; ++kk)
                     tc_mma(d, sw128_desc(sa + kk * 32), sw128_desc(sa + kABytes + kk * 32), (kb | kk) != 0);
-                // the stage is free once these MMAs have read it (in every CTA that holds it)
-                if constexpr (kCluster == 1) {
-                    tc_commit(empty0 + 8 * s);
-                } else {
-                    tc_commit_mc(empty0 + 8 * s, kAll);
-                }
+                tc_commit(empty0 + 8 * s);  // the stage is free once these MMAs have read it
             }
             tc_commit(acc_full0 + 8 * a);  // the tile's accumulator is complete (or abandoned)
         }
@@ -486,12 +466,12 @@ __global__ void __launch_bounds__(kThreadsG, 1) qkv_gemm_kernel(const __grid_con
         const uint32_t quarter = warp & 3u;
         const uint32_t HD = p.H * kGemmHeadDim;
         uint32_t i = 0;
-        for (uint32_t t = cid; t < units; t += clusters, ++i) {
+        for (uint32_t t = cid; t < units; t += ctas, ++i) {
             const uint32_t a = i % kAccBufs, u = i / kAccBufs;
             const bool ok = wait_phase(acc_full0 + 8 * a, u & 1u, abort_flag);
             tc_fence_after();
             if (!__all_sync(0xffffffffu, ok && !*abort_flag)) break;  // warp-uniform: TMEM loads are collective
-            const Tile tl = decode_tile<kCluster>(p, t, rank);
+            const Tile tl = decode_tile<1>(p, t, 0);
             const uint32_t m = tl.m_tile * kGemmBM + quarter * 32 + lane;
             const bool valid = tl.m_tile < p.m_tiles && m < p.rows;
             const uint32_t b = valid ? m / p.Sl : 0, tt = valid ? m - b * p.Sl : 0;
@@ -515,12 +495,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) qkv_gemm_kernel(const __grid_con
         }
     }
     // teardown: every MMA has completed (warp 1 waited on mma_done) and every TMEM
-    // read has finished before the columns are freed; a cluster's CTAs leave
-    // together, after every copy and arrival between them has landed
+    // read has finished before the columns are freed
     __syncwarp();  // the single-lane roles rejoin their warps before the CTA barrier
     tc_fence_before();
     __syncthreads();
-    if constexpr (kCluster > 1) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols * kAccBufs);
@@ -779,70 +757,63 @@ __global__ void wait_selftest_kernel(long long budget) {
     if (ok || !abort_flag) atomicOr(&g_gemm_status, 0x80000000u);  // would mean the wait returned wrongly
 }
 
+// The driver's tensor-map encoder, looked up once: the function-local static is
+// initialised by exactly one thread (C++11 magic statics), so concurrent first
+// calls all see the finished lookup.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
         void* ptr = nullptr;
         cudaDriverEntryPointQueryResult q{};
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        return nullptr;
+    }();
     return fn;
 }
 
-template <bool kFusedT, bool kNeox, int kCluster>
+// Per-device "attributes set" flags of a kernel.  Setting an attribute twice is
+// harmless, so racing first calls need only see a torn-free flag.
+using AttrFlags = std::atomic<bool>[64];
+
+template <bool kFusedT, bool kNeox>
 cudaError_t launch_variant(const GemmParams& p, cudaStream_t stream) {
-    static bool attr_done[64] = {};
+    static AttrFlags attr_done = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    auto kernel = qkv_gemm_kernel<kFusedT, kNeox, kCluster>;
-    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    auto kernel = qkv_gemm_kernel<kFusedT, kNeox>;
+    if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemG));
         if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
+        attr_done[dev].store(true);
     }
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const uint64_t units = (uint64_t(p.P) * p.m_tiles + kCluster - 1) / kCluster * p.n_tiles;
-    uint64_t clusters = uint64_t(sms > 0 ? sms : 1) / kCluster;  // one CTA per SM
-    if (clusters < 1) clusters = 1;
-    if (clusters > units) clusters = units;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(unsigned(clusters * kCluster));
-    cfg.blockDim = dim3(kThreadsG);
-    cfg.dynamicSmemBytes = kSmemG;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, p);
+    const uint64_t units = uint64_t(p.P) * p.m_tiles * p.n_tiles;
+    uint64_t ctas = uint64_t(sms > 0 ? sms : 1);  // one CTA per SM
+    if (ctas > units) ctas = units;
+    qkv_gemm_kernel<kFusedT, kNeox><<<unsigned(ctas), kThreadsG, kSmemG, stream>>>(p);
+    return cudaGetLastError();
 }
 
 // The pair form: clusters of two CTAs, as many as can be resident at once (at most
 // one per unit); 0 clusters fit -> cudaErrorNotSupported (the caller falls back).
 template <bool kFusedT, bool kNeox>
 cudaError_t launch_pair_variant(const GemmParams& p, cudaStream_t stream) {
-    static bool attr_done[64] = {};
+    static AttrFlags attr_done = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     auto kernel = qkv_gemm_pair_kernel<kFusedT, kNeox>;
-    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemP));
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
         if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
+        attr_done[dev].store(true);
     }
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -872,16 +843,9 @@ cudaError_t launch_pair_variant(const GemmParams& p, cudaStream_t stream) {
 #ifndef TFU_GEMM_PAIR
 // 1: CTA pairs with the 2-SM MMA (qkv_gemm_pair_kernel; on the video-DiT projection
 // 1666-1692 TFLOP/s fused where the single-CTA kernel gives 1537-1570 on the same
-// GPU, before the 32 MB raster pass and the L2 policy); 0: single CTAs, or the
-// multicast pairs of TFU_GEMM_CLUSTER.
+// GPU, before the 32 MB raster pass and the L2 policy); 0: single CTAs (the
+// fallback, built by the single-CTA parity test).
 #define TFU_GEMM_PAIR 1
-#endif
-
-#ifndef TFU_GEMM_CLUSTER
-// 1: single CTAs.  2: CTA pairs share each weight tile by TMA multicast (a third
-// less L2 traffic per CTA; measured equal on the video-DiT projection, where the
-// stage ring's lookahead, not L2 bandwidth, bounds the tensor pipe).
-#define TFU_GEMM_CLUSTER 1
 #endif
 
 }  // namespace
@@ -895,14 +859,13 @@ bool encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t cols, uin
     const cuuint32_t box[2] = {uint32_t(kGemmBK), box_rows};
     const cuuint32_t estride[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, estride,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, kGemmBK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 cudaError_t launch_qkv_gemm(const GemmParams& p, bool fused, bool neox, cudaStream_t stream) {
     if (uint64_t(p.P) * p.m_tiles * p.n_tiles == 0) return cudaSuccess;
-    constexpr int C = TFU_GEMM_CLUSTER;
     if (TFU_GEMM_PAIR) {
         const cudaError_t e = !fused ? launch_pair_variant<false, false>(p, stream)
                               : neox ? launch_pair_variant<true, true>(p, stream)
@@ -910,8 +873,8 @@ cudaError_t launch_qkv_gemm(const GemmParams& p, bool fused, bool neox, cudaStre
         if (e != cudaErrorNotSupported) return e;
         (void)cudaGetLastError();
     }
-    if (!fused) return launch_variant<false, false, C>(p, stream);
-    return neox ? launch_variant<true, true, C>(p, stream) : launch_variant<true, false, C>(p, stream);
+    if (!fused) return launch_variant<false, false>(p, stream);
+    return neox ? launch_variant<true, true>(p, stream) : launch_variant<true, false>(p, stream);
 }
 
 cudaError_t launch_wait_selftest(long long cycles, cudaStream_t stream) {

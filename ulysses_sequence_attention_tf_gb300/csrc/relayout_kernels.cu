@@ -84,8 +84,12 @@ __device__ __forceinline__ void copy_range(const RelayoutParams& p, const Plane&
 // in flight (software pipeline).  Consecutive rows of a run mostly belong to the
 // same token (Hl heads per token), so a lane reloads its (cos, sin) entries only
 // when the token changes.
-template <Fused kF, int VW, int kLanes, bool kNeox>
-__device__ __forceinline__ void norm_rope_rows(const RelayoutParams& p, const Plane& pl, uint32_t v0, uint32_t v1) {
+// kExact = false: pipelined, the fast mean (a row whose sum of squares is not
+// finite sets *redo); kExact = true: one row at a time with the complete mean
+// (row_mean_sq), same rows per lane group.
+template <Fused kF, int VW, int kLanes, bool kNeox, bool kExact>
+__device__ __forceinline__ void norm_rope_rows(const RelayoutParams& p, const Plane& pl, uint32_t v0, uint32_t v1,
+                                               volatile int* redo) {
     constexpr int NP = VW / 4;                    // element pairs per lane
     constexpr int kRowFloats = kLanes * NP * 2;  // D floats per table row: D/2 (cos, sin) pairs
     constexpr int kCs = cs_vecs<kNeox, NP>();
@@ -129,9 +133,18 @@ __device__ __forceinline__ void norm_rope_rows(const RelayoutParams& p, const Pl
             t_cached = t;
         }
         // every lane runs the row reduction (it shuffles); only valid rows are written
-        norm_rope_core<kF, kLanes, NP, kNeox>(buf.w, wpk, cs, p.eps);
+        norm_rope_core<kF, kLanes, NP, kNeox, kExact>(buf.w, wpk, cs, p.eps, redo);
         if (valid) st_stream<VW>(pl.dst + int64_t(t) * pl.dt + int64_t(h) * pl.dh + int64_t(dv) * VW, buf);
     };
+    if constexpr (kExact) {
+#pragma unroll 1
+        for (uint32_t j = 0; j < per; ++j) {
+            Vec<VW> b;
+            load(b, j);
+            compute_store(b, j);
+        }
+        return;
+    }
     Vec<VW> b0, b1, b2, b3;
     load(b0, 0);
     load(b1, 1);
@@ -176,6 +189,11 @@ __host__ __device__ constexpr int copy_batch() {
 template <Dir kDir, Fused kF, int VW, int kLanes, bool kNeox>
 __global__ void __launch_bounds__(kThreads, min_blocks<kF>()) relayout_kernel(const __grid_constant__ RelayoutParams p) {
     constexpr uint32_t kChunk = uint32_t(chunk_vecs(VW));
+    __shared__ int redo;  // set when a fused row's sum of squares was not finite
+    if constexpr (kF != Fused::kNone) {
+        if (threadIdx.x == 0) redo = 0;
+        __syncthreads();
+    }
 #pragma unroll 1
     for (uint32_t u = blockIdx.x; u < p.n_units; u += gridDim.x) {
         const uint32_t c = fastdiv(u, p.div_planes);
@@ -185,11 +203,28 @@ __global__ void __launch_bounds__(kThreads, min_blocks<kF>()) relayout_kernel(co
         const uint32_t v1 = min(v0 + kChunk, p.nv);
         if constexpr (kF != Fused::kNone) {
             if ((p.fused_mask >> pl.x) & 1u) {
-                norm_rope_rows<kF, VW, kLanes, kNeox>(p, pl, v0, v1);
+                norm_rope_rows<kF, VW, kLanes, kNeox, false>(p, pl, v0, v1, &redo);
                 continue;
             }
         }
         copy_range<kDir, VW, copy_batch<VW>()>(p, pl, v0, v1);
+    }
+    if constexpr (kF != Fused::kNone) {
+        // A fused row whose sum of squares was not finite (an element of magnitude
+        // >= 2^64, an infinite one or a NaN) was stored with the fast mean: if the
+        // CTA met one, its fused rows are computed again with the complete mean,
+        // each row by the lanes that stored it, after their first store.
+        __syncthreads();
+        if (redo) {
+#pragma unroll 1
+            for (uint32_t u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+                const uint32_t c = fastdiv(u, p.div_planes);
+                const Plane pl = decode_plane<kDir>(p, u - c * p.n_planes);
+                if ((p.fused_mask >> pl.x) & 1u)
+                    norm_rope_rows<kF, VW, kLanes, kNeox, true>(p, pl, c * kChunk, min(c * kChunk + kChunk, p.nv),
+                                                                &redo);
+            }
+        }
     }
 }
 

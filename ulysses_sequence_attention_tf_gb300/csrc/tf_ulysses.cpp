@@ -167,11 +167,7 @@ tf_status check_strides(const char* what, const tf_strides& s, int esize, int64_
 
 // 32-byte vectors when every address the kernel forms is 32-byte aligned
 // (bases, strides of dimensions longer than 1, weights, the head row), else 16.
-#ifndef TFU_MAX_VEC_BYTES
-#define TFU_MAX_VEC_BYTES 32
-#endif
 uint32_t pick_vec_bytes(const RelayoutParams& p, const Shape& sh, int64_t src_tokens, int64_t dst_tokens) {
-    if (TFU_MAX_VEC_BYTES < 32) return 16;
     auto ok = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 31u) == 0; };
     auto ok_stride = [](int64_t st, int64_t extent) { return extent <= 1 || st % 32 == 0; };
     if ((int64_t(sh.D) * sh.esize) % 32 != 0) return 16;
@@ -212,15 +208,6 @@ tf_status plan_units(RelayoutParams& p, const Shape& sh) {
     return TF_OK;
 }
 
-#ifndef TFU_USE_STAGED
-#define TFU_USE_STAGED 1  // staged kernel for pure relayouts (copy scatters, gathers)
-#endif
-#ifndef TFU_FUSED_BLOCKS
-#define TFU_FUSED_BLOCKS 1  // fused scatter with 32-byte vectors: one pass over token blocks of all slots
-#endif
-#ifndef TFU_COPY_BLOCKS
-#define TFU_COPY_BLOCKS 0  // the same single pass for copy scatters (else the staged kernel)
-#endif
 #ifndef TFU_SMALL_BAND
 // Token head bands (Hl * D * esize bytes) up to this size take the register paths
 // for pure relayouts: the block kernel for copy scatters, the register kernel for
@@ -244,10 +231,9 @@ constexpr uint64_t kBlockCopyBandBytes = TFU_BLOCK_COPY_BAND;
 
 // Plan and launch one relayout:
 //  * scatters with 32-byte vectors and D * esize in {64, 128, 256, 512} bytes
-//    (fused always; copies into the fused receive layout, copies whose token head
-//    band is at most 1 KiB -- or 2.5 KiB for head rows of 256 bytes or more --, or
-//    all copies when TFU_COPY_BLOCKS): the block kernel, all slots of a token
-//    block in one pass;
+//    (fused always; copies into the fused receive layout, and copies whose token
+//    head band is at most 1 KiB -- or 2.5 KiB for head rows of 256 bytes or
+//    more): the block kernel, all slots of a token block in one pass;
 //  * other pure relayouts whose head row fits a stage, except gathers of small
 //    bands or 128-byte rows: the shared-memory-staged (bulk-copy) kernel;
 //  * the rest: the register kernel with 32- or 16-byte vectors.
@@ -291,10 +277,8 @@ tf_status launch_planned(RelayoutParams& p, const Shape& sh, tfu::Dir dir, tfu::
     // faster through the registers than through the bulk-copy engine
     const bool mid_band = rb >= 256 && uint64_t(sh.Hl) * rb <= kBlockCopyBandBytes;
     const bool block_ok = dir == tfu::Dir::kScatter && dst_shared && (rb == 64 || rb == 128 || rb == 256 || rb == 512) &&
-                          (fused != tfu::Fused::kNone ? TFU_FUSED_BLOCKS
-                                                      : (TFU_COPY_BLOCKS || !dst_rows_packed || small_band || mid_band));
-    const bool staged_ok = TFU_USE_STAGED && fused == tfu::Fused::kNone &&
-                           !(dir == tfu::Dir::kGather && (small_band || rb <= 128));
+                          (fused != tfu::Fused::kNone || !dst_rows_packed || small_band || mid_band);
+    const bool staged_ok = fused == tfu::Fused::kNone && !(dir == tfu::Dir::kGather && (small_band || rb <= 128));
     const uint32_t vec = pick_vec_bytes(p, sh, src_tokens, dst_tokens);
     // staged units: the stage ring by head band and launch size (tma_plan.h)
     const uint64_t band = uint64_t(sh.Hl) * rb;

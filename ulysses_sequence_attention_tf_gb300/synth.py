@@ -151,6 +151,69 @@ def unique_id_shards(P, B, S_local, H, D, *, device="cpu"):
     return [ids[r * n:(r + 1) * n].to(torch.int16).view(B, S_local, H, D).clone() for r in range(P)]
 
 
+# Head rows with extreme or non-finite values, for the fused path's edge cases.
+# bf16 reaches 3.4e38, so squares overflow fp32 from |x| = 2^64 on; fp16 tops out
+# at 65504 (no overflow), so its cases are the non-finite and the tiny ones.
+EDGE_KINDS = {
+    torch.bfloat16: ("const_2^63", "const_2^64", "const_2^100", "normal_2^60", "normal_2^62", "spike_2^64",
+                     "spike_2^100", "inf", "-inf", "nan", "subnormal", "zero", "tiny"),
+    torch.float16: ("max", "inf", "-inf", "nan", "subnormal", "zero", "tiny"),
+}
+
+
+def edge_row(kind, D, dtype, gen):
+    """One head row [D] of the edge kind ``kind`` (CPU): constant rows, N(0, 1)
+    rows scaled by a power of two, a single large element in an N(0, 1) row, one
+    +-inf or NaN element in an N(0, 1) row, random subnormals, zeros, or N(0, 1)
+    scaled to 2^-70 (bf16) / 2^-20 (fp16)."""
+    base = torch.randn((D,), generator=gen)
+    at = int(torch.randint(D, (1,), generator=gen))
+    name, _, arg = kind.partition("_")
+    if name == "const":
+        return torch.full((D,), 2.0 ** int(arg[2:]), dtype=dtype)
+    if name == "normal":
+        return (base * 2.0 ** int(arg[2:])).to(dtype)
+    if name in ("spike", "inf", "-inf", "nan"):
+        row = base.to(dtype)
+        row[at] = {"spike": 2.0 ** int(arg[2:] or 0), "inf": float("inf"), "-inf": float("-inf"),
+                   "nan": float("nan")}[name]
+        return row
+    if name == "max":
+        return torch.full((D,), torch.finfo(dtype).max, dtype=dtype) * torch.sign(base).to(dtype)
+    if name == "subnormal":
+        frac_bits = 7 if dtype == torch.bfloat16 else 10
+        mag = torch.randint(1, 1 << frac_bits, (D,), generator=gen, dtype=torch.int32)
+        sign = torch.randint(0, 2, (D,), generator=gen, dtype=torch.int32) << 15
+        return (sign | mag).to(torch.int16).view(dtype)
+    if name == "zero":
+        return torch.zeros((D,), dtype=dtype)
+    if name == "tiny":
+        return (base * 2.0 ** (-70 if dtype == torch.bfloat16 else -20)).to(dtype)
+    raise ValueError(f"unknown edge kind {kind!r}")
+
+
+def plant_edge_rows(shards, *, seed=0, every=7):
+    """Overwrite head rows of P shard tensors [B, S_local, H, D] (CPU, in place)
+    with edge rows: every ``every``-th row in shard-major order cycles through the
+    kinds of the element type, and shard 0's first token gets one kind on all its
+    heads.  Returns the number of rows planted."""
+    dtype = shards[0].dtype
+    kinds = EDGE_KINDS[dtype]
+    gen = make_generator(seed + 1299709, "cpu")
+    B, Sl, H, D = shards[0].shape
+    n = 0
+    for r, x in enumerate(shards):
+        for b in range(B):
+            for t in range(Sl):
+                for h in range(H):
+                    i = ((r * B + b) * Sl + t) * H + h
+                    if i % every == 0 or (r == 0 and b == 0 and t == 0):
+                        kind = kinds[(i // every + (0 if t else h)) % len(kinds)]
+                        x[b, t, h] = edge_row(kind, D, dtype, gen)
+                        n += 1
+    return n
+
+
 def move(d, device):
     """Copy a ``qkv_shards`` result to ``device`` keeping every view's strides
     (views into a fused projection stay views into the copied projection)."""
