@@ -250,6 +250,42 @@ def measure_projection(torch, binding, synth, w, stream, dev, wq, wk, iters=10):
             "iters": iters}
 
 
+def measure_noalloc(torch, binding, w, sets, wq, wk, stream, dev, rounds=5, calls=10):
+    """The allocation-free scatter (its cos/sin table in the library's fixed
+    scratch) against scatter_qkv_into on the same caller-owned targets: rounds of
+    `calls` calls each, the two interleaved, CUDA events on the stream; inputs
+    rotate over the input sets (larger than L2)."""
+    P, B, S, H, D = w["P"], w["B"], w["S"], w["H"], w["D"]
+    outs = [[torch.empty((B, S, H // P, D), dtype=torch.bfloat16, device=dev) for _ in range(P)] for _ in "qkv"]
+    kw = dict(norm_rope=True, q_weight=wq, k_weight=wk, eps=w["eps"], theta=w["theta"], stream=stream)
+    fns = {"noalloc": binding.scatter_qkv_noalloc, "into": binding.scatter_qkv_into}
+
+    def run(name, n):
+        for j in range(n):
+            g = sets[j % len(sets)]
+            fns[name](g["q"], g["k"], g["v"], *outs, **kw)
+
+    for name in fns:
+        run(name, 3)
+    torch.cuda.synchronize(dev)
+    ms = {name: [] for name in fns}
+    for _ in range(rounds):
+        for name in fns:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run(name, calls)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms[name].append(e0.elapsed_time(e1) / calls)
+    med = {name: statistics.median(v) for name, v in ms.items()}
+    sp, sx, _ = step_bytes(w)
+    return {"ms_per_call": med["noalloc"], "GB/s": (sp + sx) / (med["noalloc"] / 1e3) / 1e9,
+            "into_ms_per_call": med["into"], "ratio_to_into": med["noalloc"] / med["into"],
+            "repeats_ms": ms,
+            "note": "tf_ulysses_scatter_qkv_noalloc, fused Q/K/V scatter into caller-owned targets, table in the "
+                    "fixed scratch (built by the first call, reused after); medians of interleaved rounds"}
+
+
 def measured_tensor_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -282,14 +318,20 @@ def run_e2e(args, torch, binding, src, wq, wk, w, stream, dev, world, step_paylo
     events order each buffer's reuse."""
     import torch.distributed as dist
     nbuf = 2
-    h_in = {key: [x.contiguous().cpu().pin_memory() for x in src[key]] for key in ("q", "k", "v", "attn")}
+    H, D = w["H"], w["D"]
+    # Q/K contiguous; V uploaded as the fused projection buffer [B, Sl, 3*H*D] it is a
+    # view of, and passed as that strided view: the same call as the device-timed steps
+    h_in = {key: [x.contiguous().cpu().pin_memory() for x in src[key]] for key in ("q", "k", "attn")}
+    h_in["vbuf"] = [b.cpu().pin_memory() for b in src["backing"]]
     d_in = [{key: [torch.empty_like(x, device=dev) for x in h_in[key]] for key in h_in} for _ in range(nbuf)]
+    d_v = [[b[..., 2 * H * D:].unflatten(-1, (H, D)) for b in d_in[i]["vbuf"]] for i in range(nbuf)]
+    assert d_v[0][0].stride() == src["v"][0].stride()
     s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     s_cmp = stream
     results = []
 
     def calls(i):
-        tq, tk, tv, _ = binding.scatter_qkv(f"bench_e2e{i}", d_in[i]["q"], d_in[i]["k"], d_in[i]["v"],
+        tq, tk, tv, _ = binding.scatter_qkv(f"bench_e2e{i}", d_in[i]["q"], d_in[i]["k"], d_v[i],
                                             norm_rope=True, q_weight=wq, k_weight=wk, eps=w["eps"],
                                             theta=w["theta"], stream=s_cmp)
         o, _ = binding.gather_out(f"bench_e2e{i}", d_in[i]["attn"], stream=s_cmp)
@@ -382,8 +424,9 @@ def run_e2e(args, torch, binding, src, wq, wk, w, stream, dev, world, step_paylo
                           "copies_only_repeats_ms_per_step": [m / args.e2e_steps for m in copy_runs],
                           "gbs_per_direction": max(h2d, d2h) / (copy_ms / args.e2e_steps / 1e3) / 1e9,
                           "e2e_frac_of_copies_only": copy_ms / e2e_ms},
-            "note": "pinned host Q/K/V/attention inputs copied in, all targets and outputs copied out, every "
-                    "step; V uploaded contiguous; upload, calls and download of consecutive steps overlap on "
+            "note": "pinned host Q/K/attention inputs and V's fused projection buffer [B, Sl, 3*H*D] copied "
+                    "in (V passed as its strided view, as in the device-timed steps), all targets and outputs "
+                    "copied out, every step; upload, calls and download of consecutive steps overlap on "
                     "three streams (two buffer sets); median of five repeats of the timed steps, interleaved "
                     "with five repeats of host_link: the same copies without the calls (best repeat)"}
 
@@ -477,6 +520,8 @@ def main():
     if args.e2e_steps > 0:
         e2e = run_e2e(args, torch, binding, sets[0], wq, wk, w, stream, dev, world, sp + gp)
 
+    noalloc = measure_noalloc(torch, binding, w, sets, wq, wk, stream, dev)
+
     projection = None
     if not args.no_projection:
         projection = measure_projection(torch, binding, synth, w, stream, dev, wq, wk)
@@ -505,8 +550,10 @@ def main():
             "pct_of_hbm_measured": 100.0 * value / world / peak,
             "pct_of_hbm_nominal_8000": 100.0 * value / world / NOMINAL_HBM_GBS,
             "kernels": {
-                "scatter_fused": {"ms": scat_avg, "GB/s": achieved, "bytes": sp + sx},
-                "gather": {"ms": gath_avg, "GB/s": gp / (gath_avg / 1e3) / 1e9, "bytes": gp},
+                "scatter_fused": {"ms": scat_avg, "GB/s": achieved, "bytes": sp + sx,
+                                  "kcycles_at_median_sm_clock": scat_avg * (clocks["sm_mhz"] or 0)},
+                "gather": {"ms": gath_avg, "GB/s": gp / (gath_avg / 1e3) / 1e9, "bytes": gp,
+                           "kcycles_at_median_sm_clock": gath_avg * (clocks["sm_mhz"] or 0)},
             },
             "tolerance": {"relayout": "bit-exact", "fused_qk": "max-abs 1e-2 (bf16) / 2e-3 (fp16); an element "
                           "above that must differ by exactly 1 ulp (checked by the -m gpu tests)"},
@@ -515,6 +562,7 @@ def main():
                          "kernel": FUSED_KERNEL},
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "noalloc_fused": noalloc,
             "qkv_projection": projection,
             "clocks": clocks,
             "gpu_launches": launches,

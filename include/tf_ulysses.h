@@ -233,16 +233,23 @@ TF_API tf_status tf_ulysses_scatter_qkv_into(const void *const *q, const void *c
  *
  * Arguments, layouts and errors are those of tf_ulysses_scatter_qkv_into; the
  * caller passes the inputs and the targets.  When mode is
- * TF_MODE_SCATTER_NORM_ROPE and nr->cos_sin is NULL, the cos/sin table is built
- * on `stream`, on every call, into a fixed 16 MiB device array that is part of
- * the library (file-scope, held by every GPU that loads the library until
- * exit), so P * S_local * D must not exceed 4,194,304 (4 Mi floats); larger
- * sizes return TF_ERR_UNSUPPORTED before any launch.  Nothing is allocated: no
+ * TF_MODE_SCATTER_NORM_ROPE and nr->cos_sin is NULL, the cos/sin table comes
+ * from a fixed 16 MiB device array that is part of the library (file-scope,
+ * held by every GPU that loads the library until exit), so P * S_local * D must
+ * not exceed 4,194,304 (4 Mi floats); larger sizes return TF_ERR_UNSUPPORTED
+ * before any launch.  The array keeps the last table built into it: a call
+ * whose (theta, P * S_local rows, D) it already holds (or a longer table of the
+ * same theta and D) uses it as it is, after the end of that build in stream
+ * order; any other call rebuilds it on `stream` first.  Nothing is allocated: no
  * cudaMalloc, cudaFree or allocating library routine is called.
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  All calls share the one array: calls whose work
- * overlaps on the GPU (e.g. on two streams without ordering) race on it.
+ * The first call on a device sets the device up with that device current: it
+ * looks up the array's device address (cudaGetSymbolAddress) and creates the
+ * event that marks the end of each build; make that first call before any
+ * stream capture.  The address is kept for the life of the process, so a
+ * device must not be reset (cudaDeviceReset) while the library is loaded.  All
+ * calls share the one array: a rebuild whose work overlaps on the GPU with
+ * another call's scatter (e.g. calls of different theta, rows or D on two
+ * streams without ordering) races with it.
  */
 TF_API tf_status tf_ulysses_scatter_qkv_noalloc(const void *const *q, const void *const *k, const void *const *v,
                                                 const tf_strides *strides,

@@ -303,9 +303,10 @@ def scatter_qkv_into(q, k, v, q_out, k_out=None, v_out=None, *, norm_rope=False,
 def scatter_qkv_noalloc(q, k, v, q_out, k_out=None, v_out=None, *, norm_rope=False, q_weight=None, k_weight=None,
                         eps=1e-6, theta=10000.0, cos_sin=None, rope="interleaved", layout="bshd", stream=None):
     """``scatter_qkv_into`` for callers that cannot allocate device memory: the
-    library allocates nothing; a needed cos/sin table is rebuilt on every call
-    in the library's fixed 16 MiB device scratch (P*S_local*D <= 4 Mi floats).
-    Calls that overlap on the GPU race on that scratch."""
+    library allocates nothing; a needed cos/sin table lives in the library's
+    fixed 16 MiB device scratch (P*S_local*D <= 4 Mi floats), rebuilt only when
+    it does not already hold this (theta, rows, D).  A rebuild whose work
+    overlaps on the GPU with another call's scatter races with it."""
     P, B, Sl, H, D, strides = _scatter_args(q, k, v)
     _check_targets((q_out, k_out, v_out), layout)
     mode = _mode(norm_rope, rope, layout)

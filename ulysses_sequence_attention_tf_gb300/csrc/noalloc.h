@@ -11,9 +11,15 @@ namespace tfu {
 // (16 MiB), enough for S = 32760 tokens at D = 128.
 constexpr size_t kNoAllocTableFloats = size_t(4) << 20;
 
-// Device address of the fixed scratch on the current device.  The first call on
-// a device looks it up (cudaGetSymbolAddress) and caches it; later calls only
-// read the cache.
-cudaError_t noalloc_table_address(float** out);
+// The fixed scratch of the current device holding the (cos, sin) table of
+// (theta, >= S rows, D) in stream order on `stream`; *out receives its device
+// address.  The first call on a device sets the device up (looks up the array's
+// address with cudaGetSymbolAddress and creates the event that marks the end of
+// each build).  The table is rebuilt on `stream` only when the array does not
+// already hold (theta, >= S rows, D) (*built = true); otherwise `stream` waits on
+// the end of the last build (*built = false).  capturing: `stream` is capturing
+// a graph (the event is then recorded and waited on as an external node).
+// S * D must not exceed kNoAllocTableFloats.
+cudaError_t noalloc_table(float theta, int S, int D, cudaStream_t stream, bool capturing, float** out, bool* built);
 
 }  // namespace tfu

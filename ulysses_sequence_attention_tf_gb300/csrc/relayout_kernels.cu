@@ -240,9 +240,9 @@ __global__ void __launch_bounds__(256) rope_table_kernel(const __grid_constant__
         const int64_t pos = idx / p.half;
         const int i = int(idx - pos * p.half);
         const double angle = double(pos) * p.inv_freq[i];
-        const float c = __double2float_rn(cos(angle));
-        const float s = __double2float_rn(sin(angle));
-        reinterpret_cast<float2*>(p.out)[idx] = make_float2(c, s);
+        double s, c;
+        sincos(angle, &s, &c);  // one argument reduction for both
+        reinterpret_cast<float2*>(p.out)[idx] = make_float2(__double2float_rn(c), __double2float_rn(s));
     }
 }
 

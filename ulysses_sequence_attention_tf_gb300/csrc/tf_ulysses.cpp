@@ -715,8 +715,9 @@ TF_API tf_status tf_ulysses_scatter_qkv_into(const void* const* q, const void* c
     return launch_scatter(pl, nr, device, st, cap, &used);
 }
 
-// Allocation-free scatter: the library-built cos/sin table goes to the fixed
-// scratch of noalloc.cu, rebuilt on every call in stream order.
+// Allocation-free scatter: the library-built cos/sin table lives in the fixed
+// scratch of noalloc.cu, rebuilt in stream order only when it does not already
+// hold the table of this (theta, rows, D).
 TF_API tf_status tf_ulysses_scatter_qkv_noalloc(const void* const* q, const void* const* k, const void* const* v,
                                                 const tf_strides* strides, int P, int B, int S_local, int H, int D,
                                                 tf_dtype dtype, tf_mode mode, const tf_norm_rope* nr,
@@ -738,14 +739,13 @@ TF_API tf_status tf_ulysses_scatter_qkv_noalloc(const void* const* q, const void
     if (pl.empty) return TF_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (own_table) {
+        bool cap = false;
+        if ((s = capture_state(st, &cap)) != TF_OK) return s;
         float* table = nullptr;
-        cudaError_t e = tfu::noalloc_table_address(&table);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(cos/sin scratch)");
-        double inv_freq[128];  // D <= 256 in the fused mode
-        for (int i = 0; i < D / 2; ++i) inv_freq[i] = std::pow(double(nr->theta), -2.0 * i / D);
-        e = tfu::launch_rope_table(table, inv_freq, P * S_local, D, st);
-        if (e != cudaSuccess) return cuda_fail(e, "building the cos/sin table in the fixed scratch");
-        g_launches.fetch_add(1);
+        bool built = false;
+        cudaError_t e = tfu::noalloc_table(nr->theta, P * S_local, D, st, cap, &table, &built);
+        if (e != cudaSuccess) return cuda_fail(e, "preparing the cos/sin table in the fixed scratch");
+        if (built) g_launches.fetch_add(1);
         pl.p.table = table;
     }
     return launch_planned(pl.p, pl.sh, tfu::Dir::kScatter, pl.fused, pl.sh.Sl, int64_t(P) * S_local, st);
