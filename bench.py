@@ -57,6 +57,7 @@ def parse_args():
     ap.add_argument("--sets", type=int, default=2, help="rotating input sets (each ~2 GB)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-projection", action="store_true", help="skip the fused QKV projection measurement")
+    ap.add_argument("--no-noalloc", action="store_true", help="skip the allocation-free scatter measurement")
     ap.add_argument("--cpu-tokens", type=int, default=4096, help="tokens per shard in the CPU-baseline sample")
     return ap.parse_args()
 
@@ -520,7 +521,7 @@ def main():
     if args.e2e_steps > 0:
         e2e = run_e2e(args, torch, binding, sets[0], wq, wk, w, stream, dev, world, sp + gp)
 
-    noalloc = measure_noalloc(torch, binding, w, sets, wq, wk, stream, dev)
+    noalloc = None if args.no_noalloc else measure_noalloc(torch, binding, w, sets, wq, wk, stream, dev)
 
     projection = None
     if not args.no_projection:

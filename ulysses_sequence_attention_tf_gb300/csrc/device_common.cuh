@@ -182,14 +182,9 @@ __device__ __forceinline__ void f2_two_sum(uint64_t a, uint64_t b, uint64_t& s, 
 
 // Sum of the squares of the lane's values, reduced over the row's kLanes
 // lanes; every lane of the group ends with the same pair hi + lo.
-template <Fused kF, int kLanes, int NP>
-__device__ __forceinline__ void row_sumsq(const uint32_t (&xw)[NP], float& hi, float& lo) {
-    auto sq = [&](int j) {
-        float a, b;
-        unpack2<kF>(xw[j], a, b);
-        const uint64_t v = f2_pack(a, b);
-        return f2_mul(v, v);
-    };
+template <int kLanes, int NP>
+__device__ __forceinline__ void row_sumsq(const uint64_t (&x2)[NP], float& hi, float& lo) {
+    auto sq = [&](int j) { return f2_mul(x2[j], x2[j]); };
     // two interleaved float-pair accumulators (even and odd elements), then one
     // TwoSum to combine them
     uint64_t hi2 = sq(0), lo2 = 0;
@@ -233,11 +228,11 @@ constexpr float kFltMax = 3.40282347e38f;
 //    among the group's lanes only, and scale the mean back up by 2^192 in two
 //    exact steps: the correctly rounded mean, or +inf when the mean itself
 //    exceeds the fp32 range.  An infinite element gives +inf, a NaN NaN.
-template <Fused kF, int kLanes, int NP, bool kExact>
-__device__ __forceinline__ float row_mean_sq(const uint32_t (&xw)[NP], volatile int* redo) {
+template <int kLanes, int NP, bool kExact>
+__device__ __forceinline__ float row_mean_sq(const uint64_t (&x2)[NP], volatile int* redo) {
     constexpr float kInvD = 1.0f / float(kLanes * NP * 2);  // D is a power of two: exact scaling
     float hi, lo;
-    row_sumsq<kF, kLanes, NP>(xw, hi, lo);
+    row_sumsq<kLanes, NP>(x2, hi, lo);
     if constexpr (!kExact) {
         if (!(hi <= kFltMax)) *redo = 1;
         return __fmul_rn(__fadd_rn(hi, lo), kInvD);
@@ -248,7 +243,7 @@ __device__ __forceinline__ float row_mean_sq(const uint32_t (&xw)[NP], volatile 
 #pragma unroll
         for (int j = 0; j < NP; ++j) {
             float v[2], s, e;
-            unpack2<kF>(xw[j], v[0], v[1]);
+            f2_unpack(x2[j], v[0], v[1]);
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const float a = __fmul_rn(v[k], 0x1p-96f);
@@ -300,7 +295,6 @@ __device__ __forceinline__ uint32_t cs_lane_offset(uint32_t dv) {
 template <Fused kF, int kLanes, int NP, bool kNeox, bool kExact>
 __device__ __forceinline__ void norm_rope_core(uint32_t (&xw)[NP], const uint32_t (&wpk)[NP],
                                                const float4 (&cs)[cs_vecs<kNeox, NP>()], float eps, volatile int* redo) {
-    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(row_mean_sq<kF, kLanes, NP, kExact>(xw, redo), eps)));
     uint64_t x2[NP];  // the lane's values as fp32 pairs
 #pragma unroll
     for (int j = 0; j < NP; ++j) {
@@ -308,6 +302,7 @@ __device__ __forceinline__ void norm_rope_core(uint32_t (&xw)[NP], const uint32_
         unpack2<kF>(xw[j], a, b);
         x2[j] = f2_pack(a, b);
     }
+    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(row_mean_sq<kLanes, NP, kExact>(x2, redo), eps)));
     const uint64_t inv2 = f2_pack(inv, inv);
     if constexpr (!kNeox) {
 #pragma unroll
@@ -357,7 +352,6 @@ __device__ __forceinline__ void norm_rope_core(uint32_t (&xw)[NP], const uint32_
 template <Fused kF, int kLanes, int NP, bool kExact>
 __device__ __forceinline__ void norm_rope_core_split(uint32_t (&xw)[NP], const uint32_t (&wpk)[NP],
                                                      const float4 (&cs)[NP / 2], float eps, volatile int* redo) {
-    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(row_mean_sq<kF, kLanes, NP, kExact>(xw, redo), eps)));
     uint64_t x2[NP];
 #pragma unroll
     for (int j = 0; j < NP; ++j) {
@@ -365,6 +359,7 @@ __device__ __forceinline__ void norm_rope_core_split(uint32_t (&xw)[NP], const u
         unpack2<kF>(xw[j], a, b);
         x2[j] = f2_pack(a, b);
     }
+    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(row_mean_sq<kLanes, NP, kExact>(x2, redo), eps)));
     const uint64_t inv2 = f2_pack(inv, inv);
     uint32_t z[NP];
 #pragma unroll
