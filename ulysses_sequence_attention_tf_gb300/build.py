@@ -1,6 +1,6 @@
 """Build ``libtf_ulysses.so`` (in-tree) with nvcc for sm_103a.
 
-The two translation units (kernels, host ABI) compile in parallel into
+The translation units (kernels, host ABI) compile in parallel into
 ``_build/`` and link into ``ulysses_sequence_attention_tf_gb300/libtf_ulysses.so``.
 cudart is linked statically, so the library depends only on the driver.
 """
@@ -21,9 +21,9 @@ LIB = os.path.join(PKG, "libtf_ulysses.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               f"-I{INCLUDE}", f"-I{CSRC}"]
-SOURCES = ["gemm_kernels.cu", "block_kernels.cu", "relayout_kernels.cu", "staged_kernels.cu", "tf_ulysses.cpp",
-           "noalloc.cu"]
-DEPS = SOURCES + ["relayout.h", "noalloc.h", "device_common.cuh", "tma_plan.h", "gemm.h"]
+SOURCES = ["block_kernels.cu", "block_kernels_v16.cu", "gemm_kernels.cu", "relayout_kernels.cu", "staged_kernels.cu",
+           "tf_ulysses.cpp", "noalloc.cu"]
+DEPS = SOURCES + ["relayout.h", "noalloc.h", "device_common.cuh", "block_kernel.cuh", "tma_plan.h", "gemm.h"]
 
 
 def nvcc() -> str:

@@ -1,414 +1,28 @@
-// block_kernels.cu -- the scatter over token blocks of all tensors together
-// (sm_103a), used for every fused scatter with 32-byte vectors.
-//
-// What is computed (TeleFuser docs, "Communication Architecture", section
-// "Sequence Parallel Communication / Ulysses"; head bands and rank order as in
-// flashinfer PR #6332 commit message, "Assumptions / Exchange algorithm"):
-//   T^x_g[b, r*Sl + t, h, :] = f_x(S^x_r[b, t, g*Hl + h, :], p = r*Sl + t)
-// with f_x the bit copy for V (and every tensor of a plain scatter) and, for Q/K
-// of a fused scatter, RMSNorm + weight + RoPE (flashinfer PR #6332,
-// "Assumptions / Operator math"; interleaved pairs, or half-split pairs).
-// TeleFuser PR #27 overlaps V's transfer with the Q/K norm/RoPE ("Changes
-// Made"); on one GPU both are SM work, so here they share every warp: a unit
-// carries V's rows and Q/K's rows of the same token block.
-//
-// Design:
-//  * A unit is the row range [c*rpu, (c+1)*rpu) of one (batch b, shard r, head
-//    group g) block, for every slot: kCopy copied slots (V first) and kNF fused
-//    ones (Q, then K).  A persistent grid walks the units, chunk-major with g
-//    innermost, so CTAs running together read whole source token rows and
-//    write all P head groups of a token block.
-//  * Each lane group of kLanes = D*2/32 lanes takes a contiguous run of the
-//    unit's rows and keeps kDepth rows (of every slot) loaded ahead of the one it
-//    computes, across unit boundaries too: the last pass over a unit's rows
-//    already loads the group's rows of its next unit (V+Q+K launches of many
-//    rounds of units keep to one unit at a time, which measured faster there).
-//    One 32-byte vector per lane per row and slot; loads bypass L1, stores are
-//    evict-first.
-//  * The (cos, sin) entries are loaded once per token and reused across its
-//    heads and by Q and K.  Destination row (t, h) sits at t*d_t + h*d_h, so the
-//    same code writes the separate [B, S, Hl, D] targets, the fused receive
-//    layout [B, S, Hl, 3*D] (d_h = 3*D*esize, slot offsets 0, D, 2D) and a head
-//    chunk of wider targets (d_t > Hl*d_h; source bands Hg heads apart).
-#include <type_traits>
-
-#include "device_common.cuh"
-#include "relayout.h"
-
-#ifndef TFU_FUSED_MIN_BLOCKS
-#define TFU_FUSED_MIN_BLOCKS 2  // resident 256-thread CTAs per SM the fused register budget is sized for
-#endif
-#ifndef TFU_COPY_BLOCK_MIN_BLOCKS
-#define TFU_COPY_BLOCK_MIN_BLOCKS 2  // resident CTAs per SM the copy block kernel's registers allow
-#endif
+// block_kernels.cu -- the block kernel (block_kernel.cuh) for rows whose every
+// address is 32-byte aligned: fused scatters and the copy scatters the planner
+// gives it.  Fused scatters of rows only 16-byte aligned go to
+// block_kernels_v16.cu (a separate translation unit, so the two sets of
+// instantiations compile in parallel).
+#include "block_kernel.cuh"
 
 namespace tfu {
-namespace {
-
-using namespace dev;
-
-// 16 bytes of a half-split head row, read-only, allocating in L1
-__device__ __forceinline__ Vec<16> ld_half(const uint8_t* p) {
-    Vec<16> v;
-    asm("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
-        : "l"(p));
-    return v;
-}
-
-int block_device_sms() {
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    return sms > 0 ? sms : 1;
-}
-
-#ifndef TFU_QK_MIN_BLOCKS
-#define TFU_QK_MIN_BLOCKS TFU_FUSED_MIN_BLOCKS  // resident CTAs per SM for fused launches without a copied slot
-#endif
-
-template <int kCopy, int kNF>
-__host__ __device__ constexpr int block_min_blocks() {
-    return kNF == 0 ? TFU_COPY_BLOCK_MIN_BLOCKS : (kCopy == 0 ? TFU_QK_MIN_BLOCKS : TFU_FUSED_MIN_BLOCKS);
-}
-
-#ifndef TFU_BLOCK_STREAM
-// 1: each row group streams the rows of all its units (next unit's loads during
-// the last pass of the one before); 0: one unit at a time
-#define TFU_BLOCK_STREAM 1
-#endif
-#ifndef TFU_STREAM_MAX_ROUNDS
-// V+Q+K fused launches stream only while the grid walks at most this many rounds
-// of units.  Streaming measured (P=4, H=24, D=128, read-flushed fractions of the
-// copy peak) +7 % at 5 and 10 rounds, +4 % at 20, +2 % at 25-35 and nothing at
-// 40-60; but -1.3 to -2 % at 40-81 rounds with wider head bands (the video DiT,
-// 67 rounds; S=32760 at H=48).  Copy and Q/K-only launches gained at every size
-// (video-DiT copy scatter +2.6 %).
-#define TFU_STREAM_MAX_ROUNDS 36
-#endif
-
-template <Fused kF, int kLanes, int kCopy, int kNF, bool kNeox, bool kStream>
-__global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
-    block_kernel(const __grid_constant__ RelayoutParams p) {
-    constexpr int VW = 32, NP = 8;                // 32 bytes = 8 element pairs per lane
-    constexpr int kSlots = kCopy + kNF;
-    constexpr int kDepth = kNF == 0 ? kCopyBlockDepth : (kCopy == 0 ? kQkBlockDepth : kBlockDepth);
-    constexpr int kRowFloats = kLanes * NP * 2;  // D floats per table row
-    constexpr int kCs = NP / 2;                   // (cos, sin) float4s of the lane's element pairs
-    constexpr uint32_t kGroups = kThreads / kLanes;
-    constexpr uint32_t kHalf = kLanes * 16;       // bytes in half a head row
-    static_assert(kSlots >= 1 && kSlots <= kMaxSlots && (kNF == 0) == (kF == Fused::kNone), "slot pattern");
-    const uint32_t g_row = threadIdx.x / kLanes, dv = threadIdx.x % kLanes;
-    // Lane dv's bytes of a head row: one 32-byte vector at dv*32 -- or, for the
-    // fused slots of half-split RoPE, 16 bytes at dv*16 of each half, so that
-    // both elements of every rotation pair sit in the same lane.
-    auto is_split = [](int x) { return kNeox && x >= kCopy; };
-    const uint32_t lane_off[2] = {dv * VW, dv * 16};  // whole-vector slots, split slots
-    // `row` already holds the lane's offset (lane_off)
-    auto ld_lane = [&](const uint8_t* row, int x) {
-        if (!is_split(x)) return ld_stream<VW>(row);
-        // the two 16-byte halves go through L1: the video-DiT half-split scatter
-        // measured 6389 GB/s against 6314 with L1::no_allocate on these loads
-        const Vec<16> lo = ld_half(row), hi = ld_half(row + kHalf);
-        Vec<VW> v;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            v.w[k] = lo.w[k];
-            v.w[4 + k] = hi.w[k];
-        }
-        return v;
-    };
-    auto st_lane = [&](uint8_t* row, int x, const Vec<VW>& v) {
-        if (!is_split(x)) {
-            st_stream<VW>(row, v);
-            return;
-        }
-        Vec<16> lo, hi;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            lo.w[k] = v.w[k];
-            hi.w[k] = v.w[4 + k];
-        }
-        st_stream<16>(row, lo);
-        st_stream<16>(row + kHalf, hi);
-    };
-    // the weight pairs of each fused slot by lane position, in shared memory
-    __shared__ uint32_t w_all[kNF > 0 ? kNF : 1][kLanes][NP];
-    // set when a row's sum of squares was not finite: the fused rows are computed again below
-    __shared__ int redo;
-    if (threadIdx.x == 0) redo = 0;
-    if (threadIdx.x < kLanes) {
-        const uint32_t lp = threadIdx.x;
-#pragma unroll
-        for (int f = 0; f < kNF; ++f) {
-            const uint8_t* wrow = static_cast<const uint8_t*>(p.weight[kCopy + f]);
-            const uint4 a = *reinterpret_cast<const uint4*>(wrow + (kNeox ? lp * 16 : lp * VW));
-            const uint4 b = *reinterpret_cast<const uint4*>(wrow + (kNeox ? kHalf + lp * 16 : lp * VW + 16));
-            w_all[f][lp][0] = a.x, w_all[f][lp][1] = a.y, w_all[f][lp][2] = a.z, w_all[f][lp][3] = a.w;
-            w_all[f][lp][4] = b.x, w_all[f][lp][5] = b.y, w_all[f][lp][6] = b.z, w_all[f][lp][7] = b.w;
-        }
-    }
-    __syncthreads();
-    auto w = [&](int f) -> const uint32_t(&)[NP] { return w_all[f][dv]; };
-    // A group's rows of one unit: plane rows [beg, end) (empty for trailing
-    // groups) and the pipeline slots that walk them (a multiple of kDepth)
-    struct Span {
-        uint32_t beg, end, slots;
-    };
-    auto span_of = [&](uint32_t c) -> Span {
-        const uint32_t R0 = c * p.rpu;
-        const uint32_t n_rows = min(R0 + p.rpu, p.plane_rows) - R0;
-        const uint32_t per = (n_rows + kGroups - 1) / kGroups;  // rows per group, the same for every lane
-        const uint32_t beg = R0 + g_row * per;
-        return Span{beg, min(beg + per, R0 + n_rows), (per + kDepth - 1) / kDepth * kDepth};
-    };
-    uint32_t g, r, b;  // the (head group, shard, batch) of the unit located last
-    auto locate = [&](uint32_t u) -> Span {
-        const uint32_t c = fastdiv(u, p.div_planes);
-        const uint32_t q = u - c * p.n_planes;  // q = (b * P + r) * P + g
-        g = q % p.P;
-        r = (q / p.P) % p.P;
-        b = q / (p.P * p.P);
-        return span_of(c);
-    };
-    const uint8_t* src[kSlots];  // each slot's source block of the unit being loaded
-    uint8_t* dst[kSlots];        // each slot's target block of the unit being stored
-    const float* tab_lane = nullptr;
-    float4 cs[kCs];              // the lane's (cos, sin) entries of token t_cached
-#pragma unroll
-    for (int k = 0; k < kCs; ++k) cs[k] = make_float4(1.f, 0.f, 1.f, 0.f);
-    uint32_t t_cached = 0xffffffffu;
-    // RMSNorm + weight + RoPE of the lane's part of one row of fused slot f
-    auto fused_row = [&](auto exact, uint32_t(&xw)[NP], int f) {
-        constexpr bool kExact = decltype(exact)::value;
-        if constexpr (kNeox) {
-            norm_rope_core_split<kF, kLanes, NP, kExact>(xw, w(f), cs, p.eps, &redo);
-        } else {
-            norm_rope_core<kF, kLanes, NP, false, kExact>(xw, w(f), cs, p.eps, &redo);
-        }
-    };
-    auto set_src = [&]() {
-#pragma unroll
-        for (int x = 0; x < kSlots; ++x) {
-            const uint32_t lo = lane_off[is_split(x) ? 1 : 0];
-            src[x] = p.src[x][r] + int64_t(b) * p.s_b[x] + int64_t(g) * p.Hg * p.s_h[x] + lo;
-        }
-    };
-    auto set_dst = [&]() {
-#pragma unroll
-        for (int x = 0; x < kSlots; ++x) {
-            const uint32_t lo = lane_off[is_split(x) ? 1 : 0];
-            dst[x] = p.dst[x][g] + int64_t(b) * p.d_b[x] + int64_t(r) * p.Sl * p.d_t[x] + lo;
-        }
-        // the lane's element pairs use table entries [dv*NP, dv*NP + NP) in both mappings
-        if constexpr (kNF > 0) tab_lane = p.table + size_t(r) * p.Sl * kRowFloats + dv * (2 * NP);
-        t_cached = 0xffffffffu;  // a new shard r: another table block
-    };
-    auto load = [&](Vec<VW>(&buf)[kSlots], uint32_t R, uint32_t end) {
-        const uint32_t t = fastdiv(R, p.div_hl);
-        const uint32_t h = R - t * p.Hl;
-#pragma unroll
-        for (int x = 0; x < kSlots; ++x) {
-            if constexpr (kNF > 0) {  // masked rows still go through the row reduction
-#pragma unroll
-                for (int k = 0; k < NP; ++k) buf[x].w[k] = 0u;
-            }
-            if (R < end) buf[x] = ld_lane(src[x] + int64_t(t) * p.s_t[x] + int64_t(h) * p.s_h[x], x);
-        }
-    };
-    auto compute_store = [&](Vec<VW>(&buf)[kSlots], uint32_t R, uint32_t end) {
-        const bool valid = R < end;
-        const uint32_t t = fastdiv(R, p.div_hl);
-        const uint32_t h = R - t * p.Hl;
-        if constexpr (kNF > 0) {
-            if (valid && t != t_cached) {
-                const float* tab = tab_lane + size_t(t) * kRowFloats;
-#pragma unroll
-                for (int k = 0; k < kCs; ++k) cs[k] = ld_table(tab + 4 * k);
-                t_cached = t;
-            }
-            // every lane runs the row reductions (they shuffle); only valid rows are written
-#pragma unroll
-            for (int f = 0; f < kNF; ++f) fused_row(std::false_type{}, buf[kCopy + f].w, f);
-        }
-        if (valid) {  // the scatter targets of one launch share their strides (slot 0's)
-            const int64_t off = int64_t(t) * p.d_t[0] + int64_t(h) * p.d_h[0];
-#pragma unroll
-            for (int x = 0; x < kSlots; ++x) st_lane(dst[x] + off, x, buf[x]);
-        }
-    };
-    Vec<VW> bufs[kDepth][kSlots];
-    if constexpr (kStream) {
-        // Each row group walks the rows of all its units as one stream: during the
-        // last pipeline pass of a unit its loads already fetch the first rows of the
-        // group's next unit, so the loads of a new unit overlap the arithmetic of the
-        // one before.  (g, r, b) and src then hold the unit being loaded, dst the
-        // unit being stored.
-        uint32_t u = blockIdx.x;  // the grid never exceeds the unit count
-        Span ld = locate(u), st = ld;
-        set_src();
-        set_dst();
-#pragma unroll
-        for (int d = 0; d < kDepth; ++d) load(bufs[d], ld.beg + d, ld.end);
-#pragma unroll 1
-        for (;;) {
-#pragma unroll 1
-            for (uint32_t j = 0; j < st.slots; j += kDepth) {
-                uint32_t ld_row = ld.beg + j + kDepth;
-                if (j + kDepth >= st.slots) {  // last pass: load the next unit's first rows
-                    const uint32_t un = u + gridDim.x;
-                    if (un < p.n_units) {
-                        ld = locate(un);
-                        set_src();
-                    } else {
-                        ld.beg = ld.end = 0;  // nothing left: the loads below are masked
-                    }
-                    ld_row = ld.beg;
-                }
-#pragma unroll
-                for (int d = 0; d < kDepth; ++d) {
-                    compute_store(bufs[d], st.beg + j + d, st.end);
-                    load(bufs[d], ld_row + d, ld.end);
-                }
-            }
-            u += gridDim.x;
-            if (u >= p.n_units) break;
-            st = ld;
-            set_dst();
-        }
-    } else {
-        // one unit at a time: its rows are loaded, computed and stored before the
-        // next unit's first loads
-#pragma unroll 1
-        for (uint32_t u = blockIdx.x; u < p.n_units; u += gridDim.x) {
-            const Span sp = locate(u);
-            set_src();
-            set_dst();
-#pragma unroll
-            for (int d = 0; d < kDepth; ++d) load(bufs[d], sp.beg + d, sp.end);
-#pragma unroll 1
-            for (uint32_t R = sp.beg; R < sp.beg + sp.slots; R += kDepth) {
-#pragma unroll
-                for (int d = 0; d < kDepth; ++d) {
-                    compute_store(bufs[d], R + d, sp.end);
-                    load(bufs[d], R + d + kDepth, sp.end);
-                }
-            }
-        }
-    }
-    if constexpr (kNF > 0) {
-        // A row whose sum of squares was not finite (an element of magnitude >=
-        // 2^64, an infinite one or a NaN) was stored with the fast mean.  If the
-        // CTA met one, every row group walks its rows of the fused slots once
-        // more, one row at a time, with the complete mean; each row is rewritten
-        // by the lanes that stored it, after their first store.
-        __syncthreads();
-        if (redo) {
-#pragma unroll 1
-            for (uint32_t u = blockIdx.x; u < p.n_units; u += gridDim.x) {
-                const Span sp = locate(u);
-                set_src();
-                set_dst();
-#pragma unroll 1
-                for (uint32_t R = sp.beg; R < sp.beg + sp.slots; ++R) {
-                    const bool valid = R < sp.end;
-                    const uint32_t t = fastdiv(R, p.div_hl);
-                    const uint32_t h = R - t * p.Hl;
-                    if (valid && t != t_cached) {
-                        const float* tab = tab_lane + size_t(t) * kRowFloats;
-#pragma unroll
-                        for (int k = 0; k < kCs; ++k) cs[k] = ld_table(tab + 4 * k);
-                        t_cached = t;
-                    }
-#pragma unroll
-                    for (int f = 0; f < kNF; ++f) {
-                        constexpr int x0 = kCopy;
-                        Vec<VW> v;
-#pragma unroll
-                        for (int k = 0; k < NP; ++k) v.w[k] = 0u;
-                        if (valid) v = ld_lane(src[x0 + f] + int64_t(t) * p.s_t[x0 + f] + int64_t(h) * p.s_h[x0 + f],
-                                               x0 + f);
-                        fused_row(std::true_type{}, v.w, f);
-                        if (valid) st_lane(dst[x0 + f] + int64_t(t) * p.d_t[0] + int64_t(h) * p.d_h[0], x0 + f, v);
-                    }
-                }
-            }
-        }
-    }
-}
-
-template <Fused kF, int kLanes, int kCopy, int kNF, bool kNeox, bool kStream>
-cudaError_t launch_block_as(const RelayoutParams& p, cudaStream_t stream) {
-    static int blocks_per_sm = 0;  // same for every device of one architecture
-    if (blocks_per_sm == 0) {
-        int bps = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &bps, block_kernel<kF, kLanes, kCopy, kNF, kNeox, kStream>, kThreads, 0);
-        if (e != cudaSuccess) return e;
-        blocks_per_sm = bps > 0 ? bps : 1;
-    }
-    const int64_t want = int64_t(block_device_sms()) * blocks_per_sm;
-    const unsigned grid = unsigned(want < int64_t(p.n_units) ? want : int64_t(p.n_units));
-    block_kernel<kF, kLanes, kCopy, kNF, kNeox, kStream><<<grid, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
-}
-
-template <Fused kF, int kLanes, int kCopy, int kNF, bool kNeox>
-cudaError_t launch_block(const RelayoutParams& p, cudaStream_t stream) {
-    if constexpr (kCopy == 1 && kNF == 2 && TFU_BLOCK_STREAM) {
-        // rounds of units = units / resident CTAs
-        const uint64_t resident = uint64_t(block_device_sms()) * block_min_blocks<kCopy, kNF>();
-        if (p.n_units > uint64_t(TFU_STREAM_MAX_ROUNDS) * resident)
-            return launch_block_as<kF, kLanes, kCopy, kNF, kNeox, false>(p, stream);
-    }
-    // Q/K-only half-split rows keep one unit at a time: streamed, they spill registers
-    constexpr bool kStreamed = TFU_BLOCK_STREAM != 0 && !(kCopy == 0 && kNF > 0 && kNeox);
-    return launch_block_as<kF, kLanes, kCopy, kNF, kNeox, kStreamed>(p, stream);
-}
-
-template <Fused kF, int kCopy, int kNF, bool kNeox>
-cudaError_t launch_block_lanes(const RelayoutParams& p, cudaStream_t stream) {
-    switch (p.vpr) {  // lanes per head row = D * esize / 32
-        case 2: return launch_block<kF, 2, kCopy, kNF, kNeox>(p, stream);
-        case 4: return launch_block<kF, 4, kCopy, kNF, kNeox>(p, stream);
-        case 8: return launch_block<kF, 8, kCopy, kNF, kNeox>(p, stream);
-        case 16: return launch_block<kF, 16, kCopy, kNF, kNeox>(p, stream);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
-template <Fused kF, bool kNeox>
-cudaError_t launch_block_fused(const RelayoutParams& p, cudaStream_t stream) {
-    const uint32_t n_copy = (p.fused_mask & 1u) ? 0u : 1u;  // V (unfused) can only be slot 0
-    const uint32_t nf = p.nx - n_copy;
-    if (nf < 1 || nf > 2 || p.fused_mask != ((1u << nf) - 1u) << n_copy) return cudaErrorInvalidValue;
-    if (n_copy)
-        return nf == 2 ? launch_block_lanes<kF, 1, 2, kNeox>(p, stream) : launch_block_lanes<kF, 1, 1, kNeox>(p, stream);
-    return nf == 2 ? launch_block_lanes<kF, 0, 2, kNeox>(p, stream) : launch_block_lanes<kF, 0, 1, kNeox>(p, stream);
-}
-
-template <Fused kF>
-cudaError_t launch_block_style(const RelayoutParams& p, cudaStream_t stream) {
-    if (!p.table) return cudaErrorInvalidValue;
-    return p.rope_neox ? launch_block_fused<kF, true>(p, stream) : launch_block_fused<kF, false>(p, stream);
-}
-
-}  // namespace
 
 cudaError_t launch_blocks(const RelayoutParams& p, Fused fused, cudaStream_t stream) {
     if (p.n_units == 0) return cudaSuccess;
-    if (p.vec_bytes != 32 || p.rpu == 0) return cudaErrorInvalidValue;
+    if (p.rpu == 0) return cudaErrorInvalidValue;
+    if (p.vec_bytes == 16) return fused == Fused::kNone ? cudaErrorInvalidValue : launch_blocks_v16(p, fused, stream);
+    if (p.vec_bytes != 32) return cudaErrorInvalidValue;
     switch (fused) {
         case Fused::kNone:
             if (p.fused_mask != 0) return cudaErrorInvalidValue;
             switch (p.nx) {
-                case 1: return launch_block_lanes<Fused::kNone, 1, 0, false>(p, stream);
-                case 2: return launch_block_lanes<Fused::kNone, 2, 0, false>(p, stream);
-                case 3: return launch_block_lanes<Fused::kNone, 3, 0, false>(p, stream);
+                case 1: return launch_block_lanes<Fused::kNone, 1, 0, false, false>(p, stream);
+                case 2: return launch_block_lanes<Fused::kNone, 2, 0, false, false>(p, stream);
+                case 3: return launch_block_lanes<Fused::kNone, 3, 0, false, false>(p, stream);
                 default: return cudaErrorInvalidValue;
             }
-        case Fused::kBF16: return launch_block_style<Fused::kBF16>(p, stream);
-        case Fused::kFP16: return launch_block_style<Fused::kFP16>(p, stream);
+        case Fused::kBF16: return launch_block_style<Fused::kBF16, false>(p, stream);
+        case Fused::kFP16: return launch_block_style<Fused::kFP16, false>(p, stream);
     }
     return cudaErrorInvalidValue;
 }

@@ -2,7 +2,7 @@
 // loads/stores, plane decoding, 16-bit conversions and the per-lane fused
 // RMSNorm + RoPE of a head row (flashinfer PR #6332 commit message,
 // "Assumptions / Operator math", interleaved pairs; the half-split pairing as a
-// variant; formulas in tf_ulysses.h).
+// variant, its pairs held within a lane; formulas in tf_ulysses.h).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -269,32 +269,14 @@ __device__ __forceinline__ float row_mean_sq(const uint64_t (&x2)[NP], volatile 
     }
 }
 
-// (cos, sin) float4s one lane reads from a table row: interleaved pairs need one
-// entry per element pair (NP/2 float4s), half-split pairs one per element (NP).
-template <bool kNeox, int NP>
-__host__ __device__ constexpr int cs_vecs() {
-    return kNeox ? NP : NP / 2;
-}
-
-// Float offset of lane dv's first (cos, sin) entry in a table row [D/2][2] when a
-// head row is spread over kLanes lanes of 2*NP elements each.  Interleaved: lane
-// dv holds pairs [dv*NP, dv*NP + NP).  Half-split: lane dv holds elements
-// [dv*2NP, dv*2NP + 2NP), whose table entries are those of element index
-// modulo D/2 (the lower and the upper half of a row share them).
-template <bool kNeox, int kLanes, int NP>
-__device__ __forceinline__ uint32_t cs_lane_offset(uint32_t dv) {
-    return kNeox ? (dv % (kLanes / 2)) * (4 * NP) : dv * (2 * NP);
-}
-
 // The arithmetic of one lane: xw holds NP element pairs (2*NP consecutive
 // elements) of one head row spread over kLanes consecutive lanes, wpk the
-// matching weight pairs, cs the lane's (cos, sin) entries (cs_lane_offset).
-// RMSNorm, weight scale, then RoPE: interleaved pairs (2i, 2i+1), or with kNeox
-// half-split pairs (i, i + D/2), whose partner values come from lane dv ^ kLanes/2.
+// matching weight pairs, cs the (cos, sin) entries of the lane's pairs, two per
+// float4.  RMSNorm, weight scale, then RoPE on interleaved pairs (2i, 2i+1).
 // kExact and `redo`: as in row_mean_sq.
-template <Fused kF, int kLanes, int NP, bool kNeox, bool kExact>
+template <Fused kF, int kLanes, int NP, bool kExact>
 __device__ __forceinline__ void norm_rope_core(uint32_t (&xw)[NP], const uint32_t (&wpk)[NP],
-                                               const float4 (&cs)[cs_vecs<kNeox, NP>()], float eps, volatile int* redo) {
+                                               const float4 (&cs)[NP / 2], float eps, volatile int* redo) {
     uint64_t x2[NP];  // the lane's values as fp32 pairs
 #pragma unroll
     for (int j = 0; j < NP; ++j) {
@@ -304,43 +286,16 @@ __device__ __forceinline__ void norm_rope_core(uint32_t (&xw)[NP], const uint32_
     }
     const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(row_mean_sq<kLanes, NP, kExact>(x2, redo), eps)));
     const uint64_t inv2 = f2_pack(inv, inv);
-    if constexpr (!kNeox) {
 #pragma unroll
-        for (int j = 0; j < NP; ++j) {
-            float a, b;
-            f2_unpack(f2_mul(x2[j], inv2), a, b);
-            const uint32_t y = pack2<kF>(a, b);  // normalised value rounded before the weight scale
-            unpack2<kF>(mul2<kF>(y, wpk[j]), a, b);
-            const float4 c4 = cs[j / 2];
-            const float c = (j & 1) ? c4.z : c4.x;
-            const float s = (j & 1) ? c4.w : c4.y;
-            xw[j] = pack2<kF>(__fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s)),
-                              __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c)));
-        }
-    } else {
-        static_assert(kLanes >= 2, "a half-split row needs its halves on different lanes");
-        uint32_t z[NP];
-#pragma unroll
-        for (int j = 0; j < NP; ++j) {
-            float a, b;
-            f2_unpack(f2_mul(x2[j], inv2), a, b);
-            z[j] = mul2<kF>(pack2<kF>(a, b), wpk[j]);
-        }
-        // lower-half lanes: o = z*c - z'*s; upper: o = z*c + z'*s (z' = the partner
-        // element of the other half).  The lower lanes take -z' (a sign flip of both
-        // 16-bit halves, exact), so both evaluate z*c + z'*s with the same roundings.
-        const bool upper = (threadIdx.x & uint32_t(kLanes / 2)) != 0;
-        const uint32_t flip = upper ? 0u : 0x80008000u;
-#pragma unroll
-        for (int j = 0; j < NP; ++j) {
-            const uint32_t pz = __shfl_xor_sync(0xffffffffu, z[j], kLanes / 2) ^ flip;
-            float a, b, pa, pb;
-            unpack2<kF>(z[j], a, b);
-            unpack2<kF>(pz, pa, pb);
-            const float4 c4 = cs[j];  // entries of elements 2j and 2j + 1
-            xw[j] = pack2<kF>(__fadd_rn(__fmul_rn(a, c4.x), __fmul_rn(pa, c4.y)),
-                              __fadd_rn(__fmul_rn(b, c4.z), __fmul_rn(pb, c4.w)));
-        }
+    for (int j = 0; j < NP; ++j) {
+        float a, b;
+        f2_unpack(f2_mul(x2[j], inv2), a, b);
+        const uint32_t y = pack2<kF>(a, b);  // normalised value rounded before the weight scale
+        unpack2<kF>(mul2<kF>(y, wpk[j]), a, b);
+        const float4 c4 = cs[j / 2];
+        const float c = (j & 1) ? c4.z : c4.x;
+        const float s = (j & 1) ? c4.w : c4.y;
+        xw[j] = pack2<kF>(__fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s)), __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c)));
     }
 }
 

@@ -104,10 +104,9 @@ struct RelayoutParams {
 // bulk copies on the video-DiT shape.  New fields go at the end.
 
 // Launch the relayout of every plane in `p` with the register kernel (vector
-// width p.vec_bytes).  Fused scatters need vec_bytes == 16 (p.vpr = D / 8 lanes
-// per head row, D in {32, 64, 128, 256}).  Scatter destination rows of a plane
-// are d_h bytes apart.
-cudaError_t launch_relayout(const RelayoutParams& p, Dir dir, Fused fused, cudaStream_t stream);
+// width p.vec_bytes); pure relayouts only (fused scatters take the block
+// kernel).  Scatter destination rows of a plane are d_h bytes apart.
+cudaError_t launch_relayout(const RelayoutParams& p, Dir dir, cudaStream_t stream);
 
 // Launch the shared-memory-staged (bulk-copy) relayout of a pure relayout
 // (no fused rows).  Requires rpu > 0; units are counted in rows
@@ -116,10 +115,14 @@ cudaError_t launch_relayout_staged(const RelayoutParams& p, Dir dir, Fused fused
 
 // Launch the scatter over token blocks of all slots together (copied slots
 // first, then the fused ones, normalised and rotated in the same pass).
-// Requires vec_bytes == 32, vpr in {2, 4, 8, 16}, and units counted in rows of
-// one (b, r, g) block: n_planes = B * P * P, rpu = rows per unit,
-// n_chunks = ceil(plane_rows / rpu).  Destination rows are d_h bytes apart.
+// Requires vpr = D * esize / 32 in {2, 4, 8, 16} (lanes per head row, 32 bytes
+// each), vec_bytes == 32 -- or 16 for a fused scatter whose rows are only
+// 16-byte aligned -- and units counted in rows of one (b, r, g) block:
+// n_planes = B * P * P, rpu = rows per unit, n_chunks = ceil(plane_rows / rpu).
+// Destination rows are d_h bytes apart.
 cudaError_t launch_blocks(const RelayoutParams& p, Fused fused, cudaStream_t stream);
+// The fused scatters of launch_blocks with vec_bytes == 16.
+cudaError_t launch_blocks_v16(const RelayoutParams& p, Fused fused, cudaStream_t stream);
 
 // Device status word of the staged kernel: 0, or 1 when a bounded wait for a
 // bulk load gave up.  read_staged_status optionally clears it.

@@ -230,10 +230,12 @@ constexpr uint64_t kBlockCopyBandBytes = TFU_BLOCK_COPY_BAND;
 #endif
 
 // Plan and launch one relayout:
-//  * scatters with 32-byte vectors and D * esize in {64, 128, 256, 512} bytes
-//    (fused always; copies into the fused receive layout, and copies whose token
-//    head band is at most 1 KiB -- or 2.5 KiB for head rows of 256 bytes or
-//    more): the block kernel, all slots of a token block in one pass;
+//  * scatters with D * esize in {64, 128, 256, 512} bytes: every fused scatter
+//    (32-byte vectors, or two 16-byte halves per lane when the rows are only
+//    16-byte aligned), and with 32-byte vectors the copies into the fused
+//    receive layout and the copies whose token head band is at most 1 KiB -- or
+//    2.5 KiB for head rows of 256 bytes or more: the block kernel, all slots of a
+//    token block in one pass;
 //  * other pure relayouts whose head row fits a stage, except gathers of small
 //    bands or 128-byte rows: the shared-memory-staged (bulk-copy) kernel;
 //  * the rest: the register kernel with 32- or 16-byte vectors.
@@ -285,8 +287,8 @@ tf_status launch_planned(RelayoutParams& p, const Shape& sh, tfu::Dir dir, tfu::
     const uint64_t bytes_per_direction = uint64_t(sh.B) * sh.P * p.nx * sh.P * rows * rb;
     const uint32_t rpu = tfu::tma_rows_per_unit(uint32_t(sh.Hl), rb,
                                                 tfu::staged_stage_bytes(band, rb, bytes_per_direction));
-    if (block_ok && vec == 32) {
-        p.vec_bytes = 32;
+    if (block_ok && (vec == 32 || fused != tfu::Fused::kNone)) {
+        p.vec_bytes = vec;  // 16: the fused rows are moved as two 16-byte halves per lane
         p.vpr = rb / 32;
         // a unit gives every row group of the CTA whole pipeline passes (kThreads / vpr
         // groups, depth rows each): one pass when three slots share the rows, else two
@@ -303,10 +305,11 @@ tf_status launch_planned(RelayoutParams& p, const Shape& sh, tfu::Dir dir, tfu::
         std::lock_guard<std::mutex> launch_lock(g_launch_mu);
         e = tfu::launch_relayout_staged(p, dir, fused, stream);
     } else {
-        p.vec_bytes = fused != tfu::Fused::kNone ? 16 : vec;  // the register kernel's fused rows use 16 bytes
+        if (fused != tfu::Fused::kNone) return fail(TF_ERR_UNSUPPORTED, "this fused scatter has no kernel");
+        p.vec_bytes = vec;
         if ((s = plan_units(p, sh)) != TF_OK) return s;
         std::lock_guard<std::mutex> launch_lock(g_launch_mu);
-        e = tfu::launch_relayout(p, dir, fused, stream);
+        e = tfu::launch_relayout(p, dir, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "launching the relayout kernel");
     g_launches.fetch_add(1);
