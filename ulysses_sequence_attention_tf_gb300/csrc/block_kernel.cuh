@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
     // set when a row's sum of squares was not finite: the fused rows are computed again below
     __shared__ int redo;
     if (threadIdx.x == 0) redo = 0;
+    grid_dependency_wait();  // nothing global is touched before this
     if (threadIdx.x < kLanes) {
         const uint32_t lp = threadIdx.x;
 #pragma unroll
@@ -366,8 +367,7 @@ cudaError_t launch_block_as(const RelayoutParams& p, cudaStream_t stream) {
     }
     const int64_t want = int64_t(block_device_sms()) * blocks_per_sm;
     const unsigned grid = unsigned(want < int64_t(p.n_units) ? want : int64_t(p.n_units));
-    block_kernel<kF, kLanes, kCopy, kNF, kNeox, kStream, kV16><<<grid, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_overlapped(block_kernel<kF, kLanes, kCopy, kNF, kNeox, kStream, kV16>, grid, kThreads, 0, stream, p);
 }
 
 template <Fused kF, int kLanes, int kCopy, int kNF, bool kNeox, bool kV16>

@@ -60,6 +60,17 @@ __device__ __forceinline__ float4 ld_table(const float* p) {
     return v;
 }
 
+// ---------------------------------------------------------------- launch overlap
+// Programmatic dependent launch (launch_overlapped in relayout.h): wait until the
+// grid before this one in the stream has completed and its writes are visible
+// -- called before a kernel's first global memory access -- and then let the
+// grid after this one be scheduled as this one's CTAs retire.  Both are no-ops
+// for a launch without the attribute.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- planes
 struct Plane {
     const uint8_t* src;

@@ -103,6 +103,27 @@ struct RelayoutParams {
 // before `nx` (shifting every later field by 4 bytes) measured ~1.3 % slower
 // bulk copies on the video-DiT shape.  New fields go at the end.
 
+// Launch `kernel` allowed to overlap the kernel before it in the stream
+// (programmatic dependent launch): its CTAs may be scheduled while that kernel's
+// last CTAs drain, and wait at grid_dependency_wait() (device_common.cuh) until
+// it has completed and its writes are visible, so stream order is kept.  Before
+// an operation that is not such a kernel the launch is an ordinary one.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_overlapped(void (*kernel)(Params...), unsigned grid, unsigned block, size_t smem,
+                                     cudaStream_t stream, const Args&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Launch the relayout of every plane in `p` with the register kernel (vector
 // width p.vec_bytes); pure relayouts only (fused scatters take the block
 // kernel).  Scatter destination rows of a plane are d_h bytes apart.

@@ -89,6 +89,7 @@ __host__ __device__ constexpr int copy_batch() {
 template <Dir kDir, int VW>
 __global__ void __launch_bounds__(kThreads, TFU_COPY_MIN_BLOCKS) relayout_kernel(const __grid_constant__ RelayoutParams p) {
     constexpr uint32_t kChunk = uint32_t(chunk_vecs(VW));
+    grid_dependency_wait();
 #pragma unroll 1
     for (uint32_t u = blockIdx.x; u < p.n_units; u += gridDim.x) {
         const uint32_t c = fastdiv(u, p.div_planes);
@@ -106,6 +107,7 @@ struct RopeTableParams {
 };
 
 __global__ void __launch_bounds__(256) rope_table_kernel(const __grid_constant__ RopeTableParams p) {
+    grid_dependency_wait();
     const int64_t n = int64_t(p.S) * p.half;
     for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < n; idx += int64_t(gridDim.x) * blockDim.x) {
         const int64_t pos = idx / p.half;
@@ -129,8 +131,7 @@ cudaError_t launch_one(const RelayoutParams& p, cudaStream_t stream) {
     }
     const int64_t want = int64_t(device_sms()) * blocks_per_sm;
     const unsigned grid = unsigned(want < int64_t(p.n_units) ? want : int64_t(p.n_units));
-    relayout_kernel<kDir, VW><<<grid, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_overlapped(relayout_kernel<kDir, VW>, grid, kThreads, 0, stream, p);
 }
 
 template <int VW>
@@ -160,8 +161,7 @@ cudaError_t launch_rope_table(float* table, const double* inv_freq_host, int S, 
     if (n == 0) return cudaSuccess;
     const int64_t blocks = (n + 255) / 256;
     const unsigned grid = unsigned(blocks < int64_t(device_sms()) * 8 ? blocks : int64_t(device_sms()) * 8);
-    rope_table_kernel<<<grid, 256, 0, stream>>>(rp);
-    return cudaGetLastError();
+    return launch_overlapped(rope_table_kernel, grid, 256, 0, stream, rp);
 }
 
 }  // namespace tfu

@@ -18,6 +18,8 @@
 //  * Every wait is bounded (clock64 budget).  A wait that gives up sets a bit in
 //    a device status word and a shared abort flag; the kernel then drains the
 //    copies it issued (bounded as well) and returns.  No trap, no endless loop.
+#include <atomic>
+
 #include "device_common.cuh"
 #include "relayout.h"
 #include "tma_plan.h"
@@ -242,6 +244,7 @@ __global__ void __launch_bounds__(32, 1) copy_staged_kernel(const __grid_constan
         split_st = split_st || unit_split_runs(p.rpu, p.Hl, p.d_t[x], p.d_h[x], p.row_bytes) >= kStoreSplitRuns;
     }
     const uint32_t n_my = blockIdx.x < p.n_units ? (p.n_units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    grid_dependency_wait();  // the barriers above are shared memory; nothing global is touched before this
     if (!split_ld && !split_st) {
         if (lane == 0) copy_dma_loop<kDir, false, R>(p, smem, full, abort_flag, n_my, 0, false);
         return;
@@ -252,20 +255,19 @@ __global__ void __launch_bounds__(32, 1) copy_staged_kernel(const __grid_constan
 
 template <Dir kDir, class R>
 cudaError_t launch_copy(const RelayoutParams& p, cudaStream_t stream) {
-    static bool attr_done[64] = {};  // per device: the shared-memory opt-in
+    static std::atomic<bool> attr_done[64] = {};  // per device: the shared-memory opt-in (setting it twice is harmless)
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 1;
-    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
         cudaError_t e = cudaFuncSetAttribute(copy_staged_kernel<kDir, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(R::kSmem));
         if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
+        attr_done[dev].store(true);
     }
     const unsigned grid = unsigned(p.n_units < uint32_t(sms) ? p.n_units : uint32_t(sms));
-    copy_staged_kernel<kDir, R><<<grid, 32, R::kSmem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_overlapped(copy_staged_kernel<kDir, R>, grid, 32, R::kSmem, stream, p);
 }
 
 // The ring whose stages fit the planned units: the small one when a unit fits
