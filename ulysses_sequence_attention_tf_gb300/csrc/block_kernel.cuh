@@ -246,8 +246,16 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
                 t_cached = t;
             }
             // every lane runs the row reductions (they shuffle); only valid rows are written
+            // Q and K sharing the cross-lane work (norm_rope_pair) measured faster where
+            // V+Q+K launches walk one unit at a time (video DiT: 311.5 against 316.1 us)
+            // and slower on streamed units (Q/K only 266.5 against 254.2 us; the
+            // FLUX-like scatter 29.9-31.0 against 29.6 us)
+            if constexpr (kNF == 2 && kCopy == 1 && !kStream) {
+                norm_rope_pair<kF, kLanes, NP, kNeox>(buf[kCopy].w, buf[kCopy + 1].w, w(0), w(1), cs, p.eps, &redo);
+            } else {
 #pragma unroll
-            for (int f = 0; f < kNF; ++f) fused_row(std::false_type{}, buf[kCopy + f].w, f);
+                for (int f = 0; f < kNF; ++f) fused_row(std::false_type{}, buf[kCopy + f].w, f);
+            }
         }
         if (valid) {  // the scatter targets of one launch share their strides (slot 0's)
             const int64_t off = int64_t(t) * p.d_t[0] + int64_t(h) * p.d_h[0];

@@ -191,28 +191,30 @@ __device__ __forceinline__ void f2_two_sum(uint64_t a, uint64_t b, uint64_t& s, 
 // float pair hi + lo (TwoSum), so fl(hi + lo) is the correctly rounded sum for
 // ordinary inputs and the mean follows by an exact power-of-two scaling.
 
+// Lane-local part of row_sumsq: the float pair hi + lo of the squares of the
+// lane's values (exact).
+template <int NP>
+__device__ __forceinline__ void lane_sumsq(const uint64_t (&x2)[NP], float& hi, float& lo) {
+    uint64_t hi2 = f2_mul(x2[0], x2[0]), lo2 = 0;
+#pragma unroll
+    for (int j = 1; j < NP; ++j) {
+        uint64_t s, e;
+        f2_two_sum(hi2, f2_mul(x2[j], x2[j]), s, e);
+        hi2 = s;
+        lo2 = f2_add(lo2, e);
+    }
+    float he, ho, le, lo_, e;
+    f2_unpack(hi2, he, ho);
+    f2_unpack(lo2, le, lo_);
+    two_sum(he, ho, hi, e);
+    lo = __fadd_rn(__fadd_rn(le, lo_), e);
+}
+
 // Sum of the squares of the lane's values, reduced over the row's kLanes
 // lanes; every lane of the group ends with the same pair hi + lo.
 template <int kLanes, int NP>
 __device__ __forceinline__ void row_sumsq(const uint64_t (&x2)[NP], float& hi, float& lo) {
-    auto sq = [&](int j) { return f2_mul(x2[j], x2[j]); };
-    // two interleaved float-pair accumulators (even and odd elements), then one
-    // TwoSum to combine them
-    uint64_t hi2 = sq(0), lo2 = 0;
-#pragma unroll
-    for (int j = 1; j < NP; ++j) {
-        uint64_t s, e;
-        f2_two_sum(hi2, sq(j), s, e);
-        hi2 = s;
-        lo2 = f2_add(lo2, e);
-    }
-    {
-        float he, ho, le, lo_, e;
-        f2_unpack(hi2, he, ho);
-        f2_unpack(lo2, le, lo_);
-        two_sum(he, ho, hi, e);
-        lo = __fadd_rn(__fadd_rn(le, lo_), e);
-    }
+    lane_sumsq<NP>(x2, hi, lo);
 #pragma unroll
     for (int m = 1; m < kLanes; m <<= 1) {  // both partners compute the same pair
         const float ohi = __shfl_xor_sync(0xffffffffu, hi, m);
@@ -280,22 +282,11 @@ __device__ __forceinline__ float row_mean_sq(const uint64_t (&x2)[NP], volatile 
     }
 }
 
-// The arithmetic of one lane: xw holds NP element pairs (2*NP consecutive
-// elements) of one head row spread over kLanes consecutive lanes, wpk the
-// matching weight pairs, cs the (cos, sin) entries of the lane's pairs, two per
-// float4.  RMSNorm, weight scale, then RoPE on interleaved pairs (2i, 2i+1).
-// kExact and `redo`: as in row_mean_sq.
-template <Fused kF, int kLanes, int NP, bool kExact>
-__device__ __forceinline__ void norm_rope_core(uint32_t (&xw)[NP], const uint32_t (&wpk)[NP],
-                                               const float4 (&cs)[NP / 2], float eps, volatile int* redo) {
-    uint64_t x2[NP];  // the lane's values as fp32 pairs
-#pragma unroll
-    for (int j = 0; j < NP; ++j) {
-        float a, b;
-        unpack2<kF>(xw[j], a, b);
-        x2[j] = f2_pack(a, b);
-    }
-    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(row_mean_sq<kLanes, NP, kExact>(x2, redo), eps)));
+// The second half of norm_rope_core for one row: y = round(x * inv),
+// z = round(y * w), interleaved RoPE, into xw.
+template <Fused kF, int NP>
+__device__ __forceinline__ void scale_rotate(uint32_t (&xw)[NP], const uint64_t (&x2)[NP], const uint32_t (&wpk)[NP],
+                                             const float4 (&cs)[NP / 2], float inv) {
     const uint64_t inv2 = f2_pack(inv, inv);
 #pragma unroll
     for (int j = 0; j < NP; ++j) {
@@ -310,22 +301,12 @@ __device__ __forceinline__ void norm_rope_core(uint32_t (&xw)[NP], const uint32_
     }
 }
 
-// Half-split RoPE on a row whose lanes hold matching halves: words [0, NP/2) are
-// the lane's elements of the first half of the row, words [NP/2, NP) their
-// partners D/2 further on; cs[j] holds the (cos, sin) entries of the elements
-// of word j.  RMSNorm and weight scale as in norm_rope_core; the rotation pairs
-// never leave the lane.  kExact and `redo`: as in row_mean_sq.
-template <Fused kF, int kLanes, int NP, bool kExact>
-__device__ __forceinline__ void norm_rope_core_split(uint32_t (&xw)[NP], const uint32_t (&wpk)[NP],
-                                                     const float4 (&cs)[NP / 2], float eps, volatile int* redo) {
-    uint64_t x2[NP];
-#pragma unroll
-    for (int j = 0; j < NP; ++j) {
-        float a, b;
-        unpack2<kF>(xw[j], a, b);
-        x2[j] = f2_pack(a, b);
-    }
-    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(row_mean_sq<kLanes, NP, kExact>(x2, redo), eps)));
+// The second half of norm_rope_core_split for one row: words [0, NP/2) hold the
+// lane's elements of the first half of the row, words [NP/2, NP) their partners
+// D/2 further on, cs[j] the (cos, sin) entries of word j's elements.
+template <Fused kF, int NP>
+__device__ __forceinline__ void scale_rotate_split(uint32_t (&xw)[NP], const uint64_t (&x2)[NP],
+                                                   const uint32_t (&wpk)[NP], const float4 (&cs)[NP / 2], float inv) {
     const uint64_t inv2 = f2_pack(inv, inv);
     uint32_t z[NP];
 #pragma unroll
@@ -345,6 +326,102 @@ __device__ __forceinline__ void norm_rope_core_split(uint32_t (&xw)[NP], const u
         xw[j + NP / 2] = pack2<kF>(__fadd_rn(__fmul_rn(a0, c4.y), __fmul_rn(b0, c4.x)),
                                    __fadd_rn(__fmul_rn(a1, c4.w), __fmul_rn(b1, c4.z)));
     }
+}
+
+// The arithmetic of one lane: xw holds NP element pairs (2*NP consecutive
+// elements) of one head row spread over kLanes consecutive lanes, wpk the
+// matching weight pairs, cs the (cos, sin) entries of the lane's pairs, two per
+// float4.  RMSNorm, weight scale, then RoPE on interleaved pairs (2i, 2i+1).
+// kExact and `redo`: as in row_mean_sq.
+template <Fused kF, int kLanes, int NP, bool kExact>
+__device__ __forceinline__ void norm_rope_core(uint32_t (&xw)[NP], const uint32_t (&wpk)[NP],
+                                               const float4 (&cs)[NP / 2], float eps, volatile int* redo) {
+    uint64_t x2[NP];  // the lane's values as fp32 pairs
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        float a, b;
+        unpack2<kF>(xw[j], a, b);
+        x2[j] = f2_pack(a, b);
+    }
+    scale_rotate<kF, NP>(xw, x2, wpk, cs, __frcp_rn(__fsqrt_rn(__fadd_rn(row_mean_sq<kLanes, NP, kExact>(x2, redo), eps))));
+}
+
+// norm_rope_core (fast mean; norm_rope_core_split's rows with kSplit) for two
+// rows at once -- the Q and K rows of one position, spread over the same kLanes
+// lanes -- sharing the cross-lane work:
+// the lower half of the row's lanes reduces the first row's float-pair sums and
+// the upper half the second row's (each half receives the other half's partial
+// sums of the row it keeps with one exchange, then reduces among itself), each
+// half computes one 1/sqrt(mean + eps), and one more exchange gives every lane
+// both.  Every lane of a half holds the same pair, so a row's mean is the same
+// correctly rounded value as in row_mean_sq; a sum that is not finite sets *redo.
+template <Fused kF, int kLanes, int NP, bool kSplit>
+__device__ __forceinline__ void norm_rope_pair(uint32_t (&xa)[NP], uint32_t (&xb)[NP], const uint32_t (&wa)[NP],
+                                               const uint32_t (&wb)[NP], const float4 (&cs)[NP / 2], float eps,
+                                               volatile int* redo) {
+    static_assert(kLanes >= 2, "two rows share the cross-lane work of at least two lanes");
+    constexpr float kInvD = 1.0f / float(kLanes * NP * 2);
+    constexpr int kHalf = kLanes / 2;
+    uint64_t x2a[NP], x2b[NP];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        float a, b;
+        unpack2<kF>(xa[j], a, b);
+        x2a[j] = f2_pack(a, b);
+        unpack2<kF>(xb[j], a, b);
+        x2b[j] = f2_pack(a, b);
+    }
+    float ha, la, hb, lb;
+    lane_sumsq<NP>(x2a, ha, la);
+    lane_sumsq<NP>(x2b, hb, lb);
+    const bool upper = (threadIdx.x & uint32_t(kHalf)) != 0;
+    float hi = upper ? hb : ha, lo = upper ? lb : la;  // the row this lane keeps
+    {
+        const float ohi = __shfl_xor_sync(0xffffffffu, upper ? ha : hb, kHalf);
+        const float olo = __shfl_xor_sync(0xffffffffu, upper ? la : lb, kHalf);
+        float s, e;
+        two_sum(hi, ohi, s, e);
+        lo = __fadd_rn(__fadd_rn(lo, olo), e);
+        hi = s;
+    }
+#pragma unroll
+    for (int m = 1; m < kHalf; m <<= 1) {
+        const float ohi = __shfl_xor_sync(0xffffffffu, hi, m);
+        const float olo = __shfl_xor_sync(0xffffffffu, lo, m);
+        float s, e;
+        two_sum(hi, ohi, s, e);
+        lo = __fadd_rn(__fadd_rn(lo, olo), e);
+        hi = s;
+    }
+    if (!(hi <= kFltMax)) *redo = 1;
+    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(__fadd_rn(hi, lo), kInvD), eps)));
+    const float oinv = __shfl_xor_sync(0xffffffffu, inv, kHalf);
+    if constexpr (kSplit) {
+        scale_rotate_split<kF, NP>(xa, x2a, wa, cs, upper ? oinv : inv);
+        scale_rotate_split<kF, NP>(xb, x2b, wb, cs, upper ? inv : oinv);
+    } else {
+        scale_rotate<kF, NP>(xa, x2a, wa, cs, upper ? oinv : inv);
+        scale_rotate<kF, NP>(xb, x2b, wb, cs, upper ? inv : oinv);
+    }
+}
+
+// Half-split RoPE on a row whose lanes hold matching halves: words [0, NP/2) are
+// the lane's elements of the first half of the row, words [NP/2, NP) their
+// partners D/2 further on; cs[j] holds the (cos, sin) entries of the elements
+// of word j.  RMSNorm and weight scale as in norm_rope_core; the rotation pairs
+// never leave the lane.  kExact and `redo`: as in row_mean_sq.
+template <Fused kF, int kLanes, int NP, bool kExact>
+__device__ __forceinline__ void norm_rope_core_split(uint32_t (&xw)[NP], const uint32_t (&wpk)[NP],
+                                                     const float4 (&cs)[NP / 2], float eps, volatile int* redo) {
+    uint64_t x2[NP];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        float a, b;
+        unpack2<kF>(xw[j], a, b);
+        x2[j] = f2_pack(a, b);
+    }
+    scale_rotate_split<kF, NP>(xw, x2, wpk, cs,
+                               __frcp_rn(__fsqrt_rn(__fadd_rn(row_mean_sq<kLanes, NP, kExact>(x2, redo), eps))));
 }
 
 }  // namespace dev
