@@ -41,9 +41,9 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 WORKLOAD = dict(name="video_dit_p4_s32760", P=4, B=1, S=32760, H=40, D=128, eps=1e-6, theta=10000.0)
 PROFILE = os.path.join(ROOT, "profiles", "fused_scatter_video_dit_p4_s32760.txt")
-# the fused scatter's kernel: its source, the shared device helpers and the parameter block
+# the fused scatter's kernel: its template and instantiation, the shared device helpers and the parameter block
 KERNEL_SOURCES = [os.path.join(ROOT, "ulysses_sequence_attention_tf_gb300", "csrc", f)
-                  for f in ("block_kernels.cu", "device_common.cuh", "relayout.h")]
+                  for f in ("block_kernel.cuh", "block_kernels.cu", "device_common.cuh", "relayout.h")]
 FUSED_KERNEL = "block_kernel<bf16, D=128 (8 lanes/row), V copied + Q/K fused, interleaved> (one launch per step)"
 
 
