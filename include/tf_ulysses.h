@@ -43,7 +43,8 @@
  * CUDA graphs (flashinfer PR #6332 commit message, "Description", "CUDA graphs":
  * a prepared call allocates nothing; a size first seen inside a capture fails
  * rather than allocate; replays interleave with eager calls).  Every entry
- * point may be called while `stream` is being captured (cudaStreamBeginCapture,
+ * point except tf_ulysses_scatter_qkv_noalloc (below; no claim is made for it)
+ * may be called while `stream` is being captured (cudaStreamBeginCapture,
  * torch.cuda.graph).  Inside a capture the library allocates and frees nothing:
  * a call whose cache entry or RoPE table does not exist yet returns
  * TF_ERR_UNSUPPORTED before enqueuing anything -- make one eager call with the
@@ -53,8 +54,12 @@
  * rotating slot, see tf_ulysses_set_slots) current at capture time, and every
  * replay rewrites those; ordering replays against eager calls that read or
  * write the same targets is the caller's, as for two eager calls on different
- * streams.  tf_ulysses_scatter_qkv_noalloc additionally needs one eager call on
- * the device before capturing (it looks up its scratch address).
+ * streams.
+ *
+ * Kernel launches (every relayout kernel; not the projection): each launch may
+ * start while the kernel before it in the stream drains (programmatic dependent
+ * launch) and waits, before it touches memory, until that kernel has completed
+ * and its writes are visible, so the results are those of plain stream order.
  */
 #ifndef TF_ULYSSES_H
 #define TF_ULYSSES_H
