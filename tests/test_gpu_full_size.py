@@ -105,6 +105,28 @@ def test_video_dit_whole_step_vs_oracle(tf, pool):
     assert tf.device_status(clear=False) == 0
 
 
+def test_back_to_back_launches_keep_stream_order(tf):
+    """Relayout kernels are launched to overlap the kernel before them in the
+    stream, and wait for it before touching memory.  A chain where each launch
+    reads what the previous one wrote -- V scattered at full size, the targets
+    gathered straight back, the result scattered again, all enqueued without a
+    synchronisation -- must give back V and its scatter bit for bit."""
+    P, B, S, H, D = 4, 1, 32760, 40, 128
+    Sl = S // P
+    dtype = torch.bfloat16
+    d = synth.qkv_shards(P, B, Sl, H, D, dtype, seed=74, layout="v_strided", device="cuda")
+    v = d["v"]
+    for _ in range(3):
+        tv, _, _, _ = tf.scatter_qkv("b2b_scatter", v)
+        back, _ = tf.gather_out("b2b_gather", tv)
+        tv2, _, _, _ = tf.scatter_qkv("b2b_rescatter", back)
+        torch.cuda.synchronize()
+        for r in range(P):
+            assert bits_equal(back[r], v[r].contiguous()), r
+        for g in range(P):
+            assert bits_equal(tv2[g], tv[g]), g
+
+
 @pytest.mark.parametrize("D", [64, 128])
 def test_fused_portfolio_p8_whole_output_vs_oracle(tf, pool, D):
     P, B, S, H = 8, 1, 32760, 48

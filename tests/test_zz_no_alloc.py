@@ -10,7 +10,8 @@ next call of the same (theta, rows, D).
 Checked here through the C ABI, call after call: the first call on its shape
 builds the table in the fixed array; the next one with new data reuses it; a
 call of another shape and RoPE base rebuilds it; a shorter sequence with the
-first base reuses the longer table built before it.  Every call's targets equal
+first base reuses the longer table built before it.  A table built on one
+stream is waited for by a reuse on another.  Every call's targets equal
 those of the existing caller-owned-target entry point bit for bit (both read
 the same table bits through the same kernels) and the oracle's under the fused
 rule; no allocation callback fires and the library's allocation count does not
@@ -120,3 +121,30 @@ def test_noalloc_rejects_sizes_beyond_the_fixed_scratch(tf):
     tf.scatter_qkv_into(g["q"], None, None, ref, norm_rope=True, q_weight=wq, k_weight=wk, cos_sin=table)
     for gi in range(P):
         assert bits_equal(out[gi], ref[gi])
+
+
+def test_noalloc_reuse_on_another_stream_waits_for_the_build(tf):
+    """A call that rebuilds the fixed table on one stream, then a call of the same
+    (theta, rows, D) on a second stream with no synchronisation between them: the
+    second waits on the end of the build (the event recorded after it), so both
+    give the targets of scatter_qkv_into bit for bit."""
+    P, B, S, H, D = 4, 1, 8192, 16, 128
+    Sl, Hl = S // P, H // P
+    dtype = torch.bfloat16
+    theta = 31337.0  # a base no other call of this file uses: the first call rebuilds
+    d = synth.qkv_shards(P, B, Sl, H, D, dtype, seed=60, layout="v_strided", device="cuda")
+    wq, wk = synth.norm_weights(D, dtype, seed=60, device="cuda")
+    kw = dict(norm_rope=True, q_weight=wq, k_weight=wk, eps=1e-6, theta=theta)
+    ref = [_targets(P, B, S, Hl, D, dtype, 0.0) for _ in range(3)]
+    tf.scatter_qkv_into(d["q"], d["k"], d["v"], *ref, **kw)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = [[_targets(P, B, S, Hl, D, dtype, 9.0) for _ in range(3)] for _ in range(2)]
+    torch.cuda.synchronize()
+    tf.scatter_qkv_noalloc(d["q"], d["k"], d["v"], *outs[0], stream=s1, **kw)
+    tf.scatter_qkv_noalloc(d["q"], d["k"], d["v"], *outs[1], stream=s2, **kw)
+    torch.cuda.synchronize()
+    for o in outs:
+        for x in range(3):
+            for gi in range(P):
+                assert bits_equal(o[x][gi], ref[x][gi]), (x, gi)
