@@ -244,6 +244,12 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
 #pragma unroll
                 for (int k = 0; k < kCs; ++k) cs[k] = ld_table(tab + 4 * k);
                 t_cached = t;
+                // One unit at a time: the entries of the group's next token go into
+                // L1 now, so that its first row finds them there (video-DiT V+Q+K
+                // 307.4 against 311.5 us; streamed launches gained nothing).
+                if constexpr (!kStream) {
+                    if (t + 1 < p.Sl) asm volatile("prefetch.global.L1 [%0];" ::"l"(tab + kRowFloats));
+                }
             }
             // every lane runs the row reductions (they shuffle); only valid rows are written
             // Q and K sharing the cross-lane work (norm_rope_pair) measured faster where
