@@ -44,6 +44,7 @@ PROFILE = os.path.join(ROOT, "profiles", "fused_scatter_video_dit_p4_s32760.txt"
 # the fused scatter's kernel: its template and instantiation, the shared device helpers and the parameter block
 KERNEL_SOURCES = [os.path.join(ROOT, "ulysses_sequence_attention_tf_gb300", "csrc", f)
                   for f in ("block_kernel.cuh", "block_kernels.cu", "device_common.cuh", "relayout.h")]
+E2E_REPEATS = 9  # interleaved repeats of the e2e steps and of the copies alone
 FUSED_KERNEL = "block_kernel<bf16, D=128 (8 lanes/row), V copied + Q/K fused, interleaved> (one launch per step)"
 
 
@@ -405,12 +406,13 @@ def run_e2e(args, torch, binding, src, wq, wk, w, stream, dev, world, step_paylo
         torch.cuda.synchronize(dev)
         return c0.elapsed_time(c1)
 
-    # five interleaved repeats of each (the host link is shared with the rest of
-    # the machine, and a window can catch other traffic): the e2e median, and the
-    # copies' best as the link's ceiling -- their median has come out both above
-    # and below the e2e time on different boxes (2.0x once), so it bounds nothing
+    # nine interleaved repeats of each (the host link is shared with the rest of
+    # the machine, and a window can catch other traffic: three of five repeats at
+    # half speed once): the e2e median, and the copies' best as the link's
+    # ceiling -- their median has come out both above and below the e2e time on
+    # different boxes (2.0x once), so it bounds nothing
     e2e_runs, copy_runs = [], []
-    for _ in range(5):
+    for _ in range(E2E_REPEATS):
         e2e_runs.append(time_e2e())
         copy_runs.append(time_copies())
     e2e_ms, copy_ms = statistics.median(e2e_runs), min(copy_runs)
@@ -428,8 +430,8 @@ def run_e2e(args, torch, binding, src, wq, wk, w, stream, dev, world, step_paylo
             "note": "pinned host Q/K/attention inputs and V's fused projection buffer [B, Sl, 3*H*D] copied "
                     "in (V passed as its strided view, as in the device-timed steps), all targets and outputs "
                     "copied out, every step; upload, calls and download of consecutive steps overlap on "
-                    "three streams (two buffer sets); median of five repeats of the timed steps, interleaved "
-                    "with five repeats of host_link: the same copies without the calls (best repeat)"}
+                    "three streams (two buffer sets); median of nine repeats of the timed steps, interleaved "
+                    "with nine repeats of host_link: the same copies without the calls (best repeat)"}
 
 
 def main():

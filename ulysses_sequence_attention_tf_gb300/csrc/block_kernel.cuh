@@ -28,12 +28,16 @@
 //    sources or targets are only 16-byte aligned (kV16), as two 16-byte ones
 //    (the lane layout is the same); loads bypass L1, stores are evict-first.
 //  * The (cos, sin) entries are loaded once per token and reused across its
-//    heads and by Q and K.  Destination row (t, h) sits at t*d_t + h*d_h, so the
+//    heads and by Q and K; launches without a copied slot bring them into a
+//    per-thread shared-memory ring with the row loads, so that the arithmetic
+//    never waits on them.  Q/K-only launches compute the Q and K rows of a
+//    position together (norm_rope_qk).  Destination row (t, h) sits at t*d_t + h*d_h, so the
 //    same code writes the separate [B, S, Hl, D] targets, the fused receive
 //    layout [B, S, Hl, 3*D] (d_h = 3*D*esize, slot offsets 0, D, 2D) and a head
 //    chunk of wider targets (d_t > Hl*d_h; source bands Hg heads apart).
 #pragma once
 
+#include <atomic>
 #include <type_traits>
 
 #include "device_common.cuh"
@@ -58,6 +62,40 @@ __device__ __forceinline__ Vec<16> ld_half(const uint8_t* p) {
         : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
         : "l"(p));
     return v;
+}
+
+// The (cos, sin) ring of launches without a copied slot (block_tab_ring): each
+// thread's own entries, 16 bytes per cp.async, read back by the same thread after
+// its copies have landed (cp.async.wait_group), so no barrier is involved.
+__device__ __forceinline__ void tab_cp16(uint32_t saddr, const float* g) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(g) : "memory");
+}
+__device__ __forceinline__ void tab_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void tab_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ float4 tab_lds(uint32_t saddr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(saddr)
+                 : "memory");
+    return v;
+}
+// Table rows in flight per thread: at most one per row loaded ahead, and one more
+// so that a slot is rewritten only a full row after it was read.
+constexpr int kTabSlots = 4;
+// Q/K-only video DiT: 248 against 254 us with the ring (DRAM waits 1.33 against
+// 2.29 stalls per issue); V+Q+K launches measured slower with it (311.0 against
+// 307.4 us, the FLUX-like scatter 31.5 against 29.6 us) and load the entries
+// directly.
+template <int kCopy, int kNF>
+__host__ __device__ constexpr bool block_tab_ring() {
+    return kCopy == 0 && kNF > 0;
+}
+// dynamic shared memory: kTabSlots slots x 4 float4s x kThreads threads
+template <int kCopy, int kNF>
+__host__ __device__ constexpr size_t block_tab_smem() {
+    return block_tab_ring<kCopy, kNF>() ? size_t(kTabSlots) * 4 * kThreads * 16 : 0;
 }
 
 inline int block_device_sms() {
@@ -166,6 +204,17 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
             w_all[f][lp][4] = b.x, w_all[f][lp][5] = b.y, w_all[f][lp][6] = b.z, w_all[f][lp][7] = b.w;
         }
     }
+    // Q/K only: the (Q, K) weight pairs of each of the lane's elements (norm_rope_qk)
+    __shared__ uint32_t wqk_all[kLanes][kNF == 2 ? 2 * NP : 1];
+    if constexpr (kNF == 2 && kCopy == 0) {
+        __syncthreads();
+        if (threadIdx.x < kLanes * NP) {
+            const uint32_t lp = threadIdx.x / NP, j = threadIdx.x % NP;
+            const uint32_t wq = w_all[0][lp][j], wk = w_all[1][lp][j];
+            wqk_all[lp][2 * j] = __byte_perm(wq, wk, 0x5410);
+            wqk_all[lp][2 * j + 1] = __byte_perm(wq, wk, 0x7632);
+        }
+    }
     __syncthreads();
     auto w = [&](int f) -> const uint32_t(&)[NP] { return w_all[f][dv]; };
     // A group's rows of one unit: plane rows [beg, end) (empty for trailing
@@ -196,6 +245,14 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
 #pragma unroll
     for (int k = 0; k < kCs; ++k) cs[k] = make_float4(1.f, 0.f, 1.f, 0.f);
     uint32_t t_cached = 0xffffffffu;
+    // Each thread's (cos, sin) entries travel through its own slots of a small
+    // shared-memory ring: copied (cp.async) when a row of a new token is loaded,
+    // read back when that row is computed.  Slot s, float4 k of thread i at
+    // ((s * kCs + k) * kThreads + i) * 16.
+    extern __shared__ __align__(16) uint8_t tab_ring[];
+    const uint32_t ring0 = uint32_t(__cvta_generic_to_shared(tab_ring)) + threadIdx.x * 16u;
+    auto ring_at = [&](uint32_t slot, int k) { return ring0 + (slot * kCs + uint32_t(k)) * kThreads * 16u; };
+    uint32_t t_loaded = 0xffffffffu, n_loaded = 0, n_read = 0;
     // RMSNorm + weight + RoPE of the lane's part of one row of fused slot f
     auto fused_row = [&](auto exact, uint32_t(&xw)[NP], int f) {
         constexpr bool kExact = decltype(exact)::value;
@@ -211,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
             const uint32_t lo = lane_off[is_split(x) ? 1 : 0];
             src[x] = p.src[x][r] + int64_t(b) * p.s_b[x] + int64_t(g) * p.Hg * p.s_h[x] + lo;
         }
+        t_loaded = 0xffffffffu;  // a new unit on the load side
     };
     auto set_dst = [&]() {
 #pragma unroll
@@ -225,6 +283,17 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
     auto load = [&](Vec<VW>(&buf)[kSlots], uint32_t R, uint32_t end) {
         const uint32_t t = fastdiv(R, p.div_hl);
         const uint32_t h = R - t * p.Hl;
+        if constexpr (block_tab_ring<kCopy, kNF>()) {
+            if (R < end && t != t_loaded) {  // the compute side sees the same tokens in the same order
+                const float* tab = p.table + (size_t(r) * p.Sl + t) * kRowFloats + dv * (2 * NP);
+                const uint32_t slot = n_loaded % kTabSlots;
+#pragma unroll
+                for (int k = 0; k < kCs; ++k) tab_cp16(ring_at(slot, k), tab + 4 * k);
+                t_loaded = t;
+                ++n_loaded;
+            }
+            tab_commit();  // one group per load call, possibly empty
+        }
 #pragma unroll
         for (int x = 0; x < kSlots; ++x) {
             if constexpr (kNF > 0) {  // masked rows still go through the row reduction
@@ -240,23 +309,30 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
         const uint32_t h = R - t * p.Hl;
         if constexpr (kNF > 0) {
             if (valid && t != t_cached) {
-                const float* tab = tab_lane + size_t(t) * kRowFloats;
+                if constexpr (block_tab_ring<kCopy, kNF>()) {
+                    tab_wait<kDepth - 1>();  // this row's load call was kDepth calls ago
+                    const uint32_t slot = n_read % kTabSlots;
 #pragma unroll
-                for (int k = 0; k < kCs; ++k) cs[k] = ld_table(tab + 4 * k);
-                t_cached = t;
-                // One unit at a time: the entries of the group's next token go into
-                // L1 now, so that its first row finds them there (video-DiT V+Q+K
-                // 307.4 against 311.5 us; streamed launches gained nothing).
-                if constexpr (!kStream) {
-                    if (t + 1 < p.Sl) asm volatile("prefetch.global.L1 [%0];" ::"l"(tab + kRowFloats));
+                    for (int k = 0; k < kCs; ++k) cs[k] = tab_lds(ring_at(slot, k));
+                    ++n_read;
+                } else {
+                    const float* tab = tab_lane + size_t(t) * kRowFloats;
+#pragma unroll
+                    for (int k = 0; k < kCs; ++k) cs[k] = ld_table(tab + 4 * k);
+                    if constexpr (!kStream) {
+                        if (t + 1 < p.Sl) asm volatile("prefetch.global.L1 [%0];" ::"l"(tab + kRowFloats));
+                    }
                 }
+                t_cached = t;
             }
-            // every lane runs the row reductions (they shuffle); only valid rows are written
-            // Q and K sharing the cross-lane work (norm_rope_pair) measured faster where
-            // V+Q+K launches walk one unit at a time (video DiT: 311.5 against 316.1 us)
-            // and slower on streamed units (Q/K only 266.5 against 254.2 us; the
-            // FLUX-like scatter 29.9-31.0 against 29.6 us)
-            if constexpr (kNF == 2 && kCopy == 1 && !kStream) {
+            // every lane runs the row reductions (they shuffle); only valid rows are written.
+            // Q/K only: both rows as fp32 pairs (video DiT 231.7 against 247.7 us with
+            // the ring alone).  V+Q+K one unit at a time: Q and K share the cross-lane
+            // work (311.5 against 316.1 us); streamed V+Q+K launches keep the per-row
+            // form (the FLUX-like scatter 29.9-31.0 us with the shared form, 29.6 without)
+            if constexpr (kNF == 2 && kCopy == 0) {
+                norm_rope_qk<kF, kLanes, NP, kNeox>(buf[0].w, buf[1].w, wqk_all[dv], cs, p.eps, &redo);
+            } else if constexpr (kNF == 2 && kCopy == 1 && !kStream) {
                 norm_rope_pair<kF, kLanes, NP, kNeox>(buf[kCopy].w, buf[kCopy + 1].w, w(0), w(1), cs, p.eps, &redo);
             } else {
 #pragma unroll
@@ -329,6 +405,7 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
         }
     }
     if constexpr (kNF > 0) {
+        if constexpr (block_tab_ring<kCopy, kNF>()) tab_wait<0>();
         // A row whose sum of squares was not finite (an element of magnitude >=
         // 2^64, an infinite one or a NaN) was stored with the fast mean.  If the
         // CTA met one, every row group walks its rows of the fused slots once
@@ -371,17 +448,30 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
 
 template <Fused kF, int kLanes, int kCopy, int kNF, bool kNeox, bool kStream, bool kV16>
 cudaError_t launch_block_as(const RelayoutParams& p, cudaStream_t stream) {
-    static int blocks_per_sm = 0;  // same for every device of one architecture
-    if (blocks_per_sm == 0) {
-        int bps = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &bps, block_kernel<kF, kLanes, kCopy, kNF, kNeox, kStream, kV16>, kThreads, 0);
-        if (e != cudaSuccess) return e;
-        blocks_per_sm = bps > 0 ? bps : 1;
+    auto* kernel = block_kernel<kF, kLanes, kCopy, kNF, kNeox, kStream, kV16>;
+    constexpr size_t kSmem = block_tab_smem<kCopy, kNF>();
+    if constexpr (kSmem > 0) {
+        // per device: the opt-in to more than 48 KiB of dynamic shared memory
+        // (setting it twice is harmless)
+        static std::atomic<bool> attr_done[64] = {};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev < 0 || dev >= 64 || !attr_done[dev].load()) {
+            const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem));
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < 64) attr_done[dev].store(true);
+        }
     }
-    const int64_t want = int64_t(block_device_sms()) * blocks_per_sm;
+    static std::atomic<int> blocks_per_sm{0};  // same for every device of one architecture
+    if (blocks_per_sm.load() == 0) {
+        int bps = 0;
+        const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kernel, kThreads, kSmem);
+        if (e != cudaSuccess) return e;
+        blocks_per_sm.store(bps > 0 ? bps : 1);
+    }
+    const int64_t want = int64_t(block_device_sms()) * blocks_per_sm.load();
     const unsigned grid = unsigned(want < int64_t(p.n_units) ? want : int64_t(p.n_units));
-    return launch_overlapped(block_kernel<kF, kLanes, kCopy, kNF, kNeox, kStream, kV16>, grid, kThreads, 0, stream, p);
+    return launch_overlapped(kernel, grid, kThreads, kSmem, stream, p);
 }
 
 template <Fused kF, int kLanes, int kCopy, int kNF, bool kNeox, bool kV16>
@@ -392,8 +482,7 @@ cudaError_t launch_block(const RelayoutParams& p, cudaStream_t stream) {
         if (p.n_units > uint64_t(TFU_STREAM_MAX_ROUNDS) * resident)
             return launch_block_as<kF, kLanes, kCopy, kNF, kNeox, false, kV16>(p, stream);
     }
-    // Q/K-only half-split rows keep one unit at a time: streamed, they spill registers
-    constexpr bool kStreamed = TFU_BLOCK_STREAM != 0 && !(kCopy == 0 && kNF > 0 && kNeox);
+    constexpr bool kStreamed = TFU_BLOCK_STREAM != 0;
     return launch_block_as<kF, kLanes, kCopy, kNF, kNeox, kStreamed, kV16>(p, stream);
 }
 

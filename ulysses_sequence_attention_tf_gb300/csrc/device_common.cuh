@@ -178,6 +178,11 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
 // TwoSum on both lanes of a pair
 __device__ __forceinline__ void f2_two_sum(uint64_t a, uint64_t b, uint64_t& s, uint64_t& e) {
     s = f2_add(a, b);
@@ -422,6 +427,121 @@ __device__ __forceinline__ void norm_rope_core_split(uint32_t (&xw)[NP], const u
     }
     scale_rotate_split<kF, NP>(xw, x2, wpk, cs,
                                __frcp_rn(__fsqrt_rn(__fadd_rn(row_mean_sq<kLanes, NP, kExact>(x2, redo), eps))));
+}
+
+// The Q and K rows of one position, spread over the same kLanes lanes, computed
+// together: element j of both rows forms one fp32 pair (q_j, k_j), so that every
+// packed operation serves both rows -- the sums of squares, the cross-lane
+// reduction (one 64-bit pair of float pairs per level), the inverse-RMS scale and
+// the rotation, whose (cos, sin) entries Q and K share.  The lane's squares are
+// summed in two independent float-pair chains (first and second elements of its
+// words) merged once, so every row's mean is the same correctly rounded value as
+// in row_mean_sq; the lower half of the row's lanes then computes Q's
+// 1/sqrt(mean + eps) and the upper half K's, and one exchange gives every lane
+// both.  Each rotation product is a packed fma with the addend -0, which rounds
+// exactly as the product alone and cannot be contracted into the sum that
+// follows; the addend comes from eps (finite and >= 0) so that the compiler
+// cannot fold it.  wqk[2j] and wqk[2j+1] hold the (Q, K) weight pairs of word j's
+// first and second element.  kSplit: half-split pairs as in norm_rope_core_split.
+// A sum that is not finite sets *redo (row_mean_sq).
+template <Fused kF, int kLanes, int NP, bool kSplit>
+__device__ __forceinline__ void norm_rope_qk(uint32_t (&xq)[NP], uint32_t (&xk)[NP], const uint32_t (&wqk)[2 * NP],
+                                             const float4 (&cs)[NP / 2], float eps, volatile int* redo) {
+    constexpr float kInvD = 1.0f / float(kLanes * NP * 2);  // D is a power of two: exact scaling
+    uint64_t e2[NP], o2[NP];  // (q, k) of each word's first and of its second element
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        float qa, qb, ka, kb;
+        unpack2<kF>(xq[j], qa, qb);
+        unpack2<kF>(xk[j], ka, kb);
+        e2[j] = f2_pack(qa, ka);
+        o2[j] = f2_pack(qb, kb);
+    }
+    uint64_t hi2 = f2_mul(e2[0], e2[0]), lo2 = 0, hb2 = f2_mul(o2[0], o2[0]), lb2 = 0;
+#pragma unroll
+    for (int j = 1; j < NP; ++j) {
+        uint64_t s, e;
+        f2_two_sum(hi2, f2_mul(e2[j], e2[j]), s, e);
+        hi2 = s;
+        lo2 = f2_add(lo2, e);
+        f2_two_sum(hb2, f2_mul(o2[j], o2[j]), s, e);
+        hb2 = s;
+        lb2 = f2_add(lb2, e);
+    }
+    {
+        uint64_t s, e;
+        f2_two_sum(hi2, hb2, s, e);
+        hi2 = s;
+        lo2 = f2_add(f2_add(lo2, lb2), e);
+    }
+#pragma unroll
+    for (int m = 1; m < kLanes; m <<= 1) {  // both partners compute the same pairs
+        const uint64_t ohi = __shfl_xor_sync(0xffffffffu, hi2, m);
+        const uint64_t olo = __shfl_xor_sync(0xffffffffu, lo2, m);
+        uint64_t s, e;
+        f2_two_sum(hi2, ohi, s, e);
+        lo2 = f2_add(f2_add(lo2, olo), e);
+        hi2 = s;
+    }
+    float hq, hk, lq, lk;
+    f2_unpack(hi2, hq, hk);
+    f2_unpack(lo2, lq, lk);
+    if (!(hq <= kFltMax) || !(hk <= kFltMax)) *redo = 1;
+    // the lower half of the row's lanes computes Q's 1/sqrt(mean + eps), the upper half K's
+    static_assert(kLanes >= 2, "the two halves of a row's lanes");
+    const bool upper = (threadIdx.x & uint32_t(kLanes / 2)) != 0;
+    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(__fadd_rn(upper ? hk : hq, upper ? lk : lq), kInvD), eps)));
+    const float oinv = __shfl_xor_sync(0xffffffffu, inv, kLanes / 2);
+    const uint64_t inv2 = f2_pack(upper ? oinv : inv, upper ? inv : oinv);
+    // normalised values rounded to 16 bits, times the weights (rounded to 16 bits)
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        float a, b;
+        f2_unpack(f2_mul(e2[j], inv2), a, b);
+        unpack2<kF>(mul2<kF>(pack2<kF>(a, b), wqk[2 * j]), a, b);
+        e2[j] = f2_pack(a, b);
+        f2_unpack(f2_mul(o2[j], inv2), a, b);
+        unpack2<kF>(mul2<kF>(pack2<kF>(a, b), wqk[2 * j + 1]), a, b);
+        o2[j] = f2_pack(a, b);
+    }
+    const float nz = __fmul_rn(-0.0f, eps);
+    const uint64_t z2 = f2_pack(nz, nz);
+    // (u, v) rotated by (c, s): u*c - v*s and u*s + v*c, every product rounded
+    auto rot = [&](uint64_t u, uint64_t v, float c, float s, uint64_t& ou, uint64_t& ov) {
+        const uint64_t c2 = f2_pack(c, c), s2 = f2_pack(s, s);
+        ou = f2_sub(f2_fma(u, c2, z2), f2_fma(v, s2, z2));
+        ov = f2_add(f2_fma(u, s2, z2), f2_fma(v, c2, z2));
+    };
+    if constexpr (!kSplit) {
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            const float4 c4 = cs[j / 2];
+            uint64_t ou, ov;
+            rot(e2[j], o2[j], (j & 1) ? c4.z : c4.x, (j & 1) ? c4.w : c4.y, ou, ov);
+            float uq, uk, vq, vk;
+            f2_unpack(ou, uq, uk);
+            f2_unpack(ov, vq, vk);
+            xq[j] = pack2<kF>(uq, vq);
+            xk[j] = pack2<kF>(uk, vk);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < NP / 2; ++j) {
+            const float4 c4 = cs[j];
+            uint64_t a0, b0, a1, b1;
+            rot(e2[j], e2[j + NP / 2], c4.x, c4.y, a0, b0);
+            rot(o2[j], o2[j + NP / 2], c4.z, c4.w, a1, b1);
+            float a0q, a0k, a1q, a1k, b0q, b0k, b1q, b1k;
+            f2_unpack(a0, a0q, a0k);
+            f2_unpack(a1, a1q, a1k);
+            f2_unpack(b0, b0q, b0k);
+            f2_unpack(b1, b1q, b1k);
+            xq[j] = pack2<kF>(a0q, a1q);
+            xk[j] = pack2<kF>(a0k, a1k);
+            xq[j + NP / 2] = pack2<kF>(b0q, b1q);
+            xk[j + NP / 2] = pack2<kF>(b0k, b1k);
+        }
+    }
 }
 
 }  // namespace dev
