@@ -127,6 +127,29 @@ def test_back_to_back_launches_keep_stream_order(tf):
             assert bits_equal(tv2[g], tv[g]), g
 
 
+@pytest.mark.parametrize("rope", ["interleaved", "neox"])
+def test_video_dit_qk_only_whole_output_vs_oracle(tf, pool, rope):
+    """The Q/K-only launch (V moved by another path) at the video-DiT shape, both
+    RoPE styles: the (cos, sin) ring and the paired Q/K rows over ~26 rounds of
+    units, every element against the oracle."""
+    P, B, S, H, D = 4, 1, 32760, 40, 128
+    Sl, Hl = S // P, H // P
+    dtype = torch.bfloat16
+    d = synth.qkv_shards(P, B, Sl, H, D, dtype, seed=91, layout="v_strided", with_v=False)
+    wq, wk = synth.norm_weights(D, dtype, seed=91)
+    g = synth.move(d, "cuda")
+    outs = [[torch.empty((B, S, Hl, D), dtype=dtype, device="cuda") for _ in range(P)] for _ in "qk"]
+    tf.scatter_qkv_into(g["q"], g["k"], None, outs[0], outs[1], None, norm_rope=True, q_weight=wq.cuda(),
+                        k_weight=wk.cuda(), eps=EPS, theta=THETA, rope=rope)
+    torch.cuda.synchronize()
+    got = [[t.cpu() for t in o] for o in outs]
+    del g, outs
+    table = oracle.rope_table(THETA, S, D)
+    flips = _check_fused(got[0], fused_oracle(pool, d["q"], P, wq, table, style=rope))
+    flips += _check_fused(got[1], fused_oracle(pool, d["k"], P, wk, table, style=rope))
+    assert flips <= 8, flips
+
+
 @pytest.mark.parametrize("D", [64, 128])
 def test_fused_portfolio_p8_whole_output_vs_oracle(tf, pool, D):
     P, B, S, H = 8, 1, 32760, 48

@@ -99,6 +99,27 @@ def test_flux_fused_projection_norm_rope(tf, dtype):
         assert bits_equal(tv[i].cpu(), want_v[i])
 
 
+# Q/K only (V moved by another path): P=4, S=8192, H=24 -- 1024 units of 192 rows,
+# about 3.4 per CTA, so every CTA streams its loads (and its lanes' (cos, sin)
+# ring) from one unit into the next; six rows per lane group and unit cross
+# token boundaries (Hl = 6).
+@pytest.mark.parametrize("dtype,rope", [(torch.bfloat16, "interleaved"), (torch.float16, "interleaved"),
+                                        (torch.bfloat16, "neox"), (torch.float16, "neox")])
+def test_qk_only_several_units_per_cta(tf, dtype, rope):
+    P, B, S, H, D = 4, 1, 8192, 24, 128
+    d = synth.qkv_shards(P, B, S // P, H, D, dtype, seed=5, layout="fused", with_v=False)
+    wq, wk = synth.norm_weights(D, dtype, seed=5)
+    g = to_device_like(d)
+    tq, tk, tv, _ = tf.scatter_qkv(f"qk_units_{rope}", g["q"], g["k"], None, norm_rope=True, q_weight=wq.cuda(),
+                                   k_weight=wk.cuda(), eps=EPS, theta=THETA, rope=rope)
+    assert tv is None
+    table = oracle.rope_table(THETA, S, D)
+    for key, tg, w in (("q", tq, wq), ("k", tk, wk)):
+        want = oracle.scatter_norm_rope(d[key], P, w, EPS, table, style=rope)
+        for i in range(P):
+            assert_fused_ok(tg[i], want[i])
+
+
 def test_rope_table_matches_oracle(tf):
     for S, D in ((4096, 128), (777, 64), (32760, 128)):
         lib_tab = tf.rope_table(THETA, S, D).cpu()

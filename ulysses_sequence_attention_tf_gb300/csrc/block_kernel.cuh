@@ -140,6 +140,8 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
     constexpr uint32_t kGroups = kThreads / kLanes;
     constexpr uint32_t kHalf = kLanes * 16;       // bytes in half a head row
     static_assert(kSlots >= 1 && kSlots <= kMaxSlots && (kNF == 0) == (kF == Fused::kNone), "slot pattern");
+    static_assert(!block_tab_ring<kCopy, kNF>() || kTabSlots >= kDepth + 1,
+                  "the table ring holds a slot for every row in flight and one more");
     const uint32_t g_row = threadIdx.x / kLanes, dv = threadIdx.x % kLanes;
     // Lane dv's bytes of a head row: one 32-byte vector at dv*32 -- or, for the
     // fused slots of half-split RoPE, 16 bytes at dv*16 of each half, so that
