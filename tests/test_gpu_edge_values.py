@@ -86,6 +86,12 @@ CASES = [
     (4, 1, 96, 16, 128, torch.bfloat16, "pad16", True, "neox"),
     (2, 1, 64, 4, 256, torch.bfloat16, "pad16", True, "interleaved"),
     (4, 1, 96, 16, 64, torch.float16, "pad16", True, "neox"),
+    # Q/K only at every lane count and with 16-byte-aligned rows (the (cos, sin)
+    # ring and the paired rows, then the recompute pass)
+    (2, 2, 70, 8, 64, torch.float16, "v_strided", False, "interleaved"),
+    (3, 1, 50, 6, 32, torch.bfloat16, "v_strided", False, "neox"),
+    (4, 1, 96, 16, 128, torch.bfloat16, "pad16", False, "interleaved"),
+    (2, 1, 64, 4, 256, torch.float16, "pad16", False, "neox"),
 ]
 
 
