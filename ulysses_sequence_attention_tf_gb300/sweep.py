@@ -13,6 +13,7 @@ Configurations (seeded synthetic inputs from ``synth``):
   F   the fused scatter across shapes: P in {2,4,8} x D in {64,128} x {bf16, fp16},
       H=48, B=1, S=32760 padded to a multiple of P, V a view into a fused projection,
       RMSNorm + interleaved RoPE on Q/K
+  FQK the same shapes with Q and K only (V moved by another path)
 
 Every point prints one JSON line:
   * GB/s over algorithmic bytes (each payload element read once and written once;
@@ -275,18 +276,19 @@ def point_relayout(name, timer, peak, cudart, P, B, S, H, D, dtype, ntensors, di
     return rec
 
 
-def point_fused(name, timer, peak, P, B, S, H, D, dtype, layout, seed=0):
+def point_fused(name, timer, peak, P, B, S, H, D, dtype, layout, seed=0, with_v=True):
     Sl, Hl = S // P, H // P
     dev = torch.device("cuda")
-    g = synth.qkv_shards(P, B, Sl, H, D, dtype, seed=seed, device=dev, layout=layout)
+    g = synth.qkv_shards(P, B, Sl, H, D, dtype, seed=seed, device=dev, layout=layout, with_v=with_v)
     wq, wk = synth.norm_weights(D, dtype, seed=seed, device=dev)
     esize = torch.empty((), dtype=dtype).element_size()
-    nbytes = 2 * 3 * B * S * H * D * esize + S * D * 4 + 2 * D * esize
+    tensors = 3 if with_v else 2
+    nbytes = 2 * tensors * B * S * H * D * esize + S * D * 4 + 2 * D * esize
 
     def ours():
         binding.scatter_qkv(f"sweep_{name}", g["q"], g["k"], g["v"], norm_rope=True, q_weight=wq, k_weight=wk)
     rec = {"sweep": name, "direction": "scatter_norm_rope", "P": P, "B": B, "S": S, "H": H, "D": D,
-           "dtype": str(dtype).replace("torch.", ""), "tensors": 3, "layout": layout, "bytes": nbytes,
+           "dtype": str(dtype).replace("torch.", ""), "tensors": tensors, "layout": layout, "bytes": nbytes,
            "bytes_per_direction": nbytes // 2}
     rec.update(_stats(timer, ours, nbytes, peak))
     rec["contiguous_copy_gbs_median_flushed"], rec["contiguous_copy_gbs_median_read_flushed"] = \
@@ -315,7 +317,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--only", default=None, help="comma-separated subset of C1..C5, F")
+    ap.add_argument("--only", default=None, help="comma-separated subset of C1..C5, F, FQK")
     ap.add_argument("--no-baselines", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3 or args.iters < 20:
@@ -328,7 +330,7 @@ def main(argv=None):
     peak, peak_src = measured_peak()
     timer = Timer(args.iters, args.warmup, torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda"))
     cudart = None if args.no_baselines else _cudart()
-    only = set(args.only.split(",")) if args.only else {"C1", "C2", "C3", "C4", "C5", "F"}
+    only = set(args.only.split(",")) if args.only else {"C1", "C2", "C3", "C4", "C5", "F", "FQK"}
     base = not args.no_baselines
     recs = []
     bf16, fp16 = torch.bfloat16, torch.float16
@@ -360,6 +362,12 @@ def main(argv=None):
             for D in (64, 128):
                 for dt in (bf16, fp16):
                     recs.append(point_fused("F", timer, peak, P, 1, synth.padded_seq(32760, P), 48, D, dt, "v_strided"))
+    if "FQK" in only:
+        for P in (2, 4, 8):
+            for D in (64, 128):
+                for dt in (bf16, fp16):
+                    recs.append(point_fused("FQK", timer, peak, P, 1, synth.padded_seq(32760, P), 48, D, dt,
+                                            "v_strided", with_v=False))
     gated = [r for r in recs if r["pass"] is not None]
     emit({"summary": {"points": len(recs), "gated_points": len(gated), "gated_pass": sum(r["pass"] for r in gated),
                       "gated_pass_write_flushed": sum(r["pass_write_flushed"] for r in gated),
