@@ -40,6 +40,7 @@ def main(argv=None):
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--rope", choices=["interleaved", "neox"], default="interleaved")
     ap.add_argument("--layout", choices=["v_strided", "fused", "contiguous", "pad16"], default="v_strided")
+    ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16", help="element type of the scatters")
     args = ap.parse_args(argv)
     P, H, D, B = args.P, args.H, args.D, args.B
     S = args.S or (8192 if args.case == "projection" else 32760)
@@ -48,7 +49,8 @@ def main(argv=None):
     binding.lib()
     binding.use_torch_allocator(True)
     dev = torch.device("cuda", 0)
-    wq, wk = synth.norm_weights(D, torch.bfloat16, seed=0, device=dev)
+    dt = torch.float16 if args.dtype == "fp16" and args.case != "projection" else torch.bfloat16
+    wq, wk = synth.norm_weights(D, dt, seed=0, device=dev)
     if args.case == "projection":
         xs, w = synth.projection_inputs(P, B, Sl, H * D, H, D, torch.bfloat16, seed=1, device=dev)
         outs = {k: [torch.empty((B, S, Hl, D), dtype=torch.bfloat16, device=dev) for _ in range(P)] for k in "qkv"}
@@ -64,11 +66,11 @@ def main(argv=None):
     elif args.case in ("scatter", "scatter_fused", "scatter_fused_qk"):
         if args.layout == "pad16":
             pad = 16 // 2
-            g = {key: [synth.qkv_shards(1, B, Sl, H, D + pad, torch.bfloat16, seed=10 * r + i, device=dev,
+            g = {key: [synth.qkv_shards(1, B, Sl, H, D + pad, dt, seed=10 * r + i, device=dev,
                                         with_k=False, with_v=False)["q"][0][..., :D] for r in range(P)]
                  for i, key in enumerate("qkv")}
         else:
-            g = synth.qkv_shards(P, B, Sl, H, D, torch.bfloat16, seed=0, layout=args.layout, device=dev)
+            g = synth.qkv_shards(P, B, Sl, H, D, dt, seed=0, layout=args.layout, device=dev)
         v = None if args.case == "scatter_fused_qk" else g["v"]  # Q/K only: V moves elsewhere
         fused = args.case != "scatter"
 
