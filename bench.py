@@ -59,6 +59,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-projection", action="store_true", help="skip the fused QKV projection measurement")
     ap.add_argument("--no-noalloc", action="store_true", help="skip the allocation-free scatter measurement")
+    ap.add_argument("--no-qk-only", action="store_true", help="skip the Q/K-only fused scatter measurement")
     ap.add_argument("--cpu-tokens", type=int, default=4096, help="tokens per shard in the CPU-baseline sample")
     return ap.parse_args()
 
@@ -286,6 +287,43 @@ def measure_noalloc(torch, binding, w, sets, wq, wk, stream, dev, rounds=5, call
             "repeats_ms": ms,
             "note": "tf_ulysses_scatter_qkv_noalloc, fused Q/K/V scatter into caller-owned targets, table in the "
                     "fixed scratch (built by the first call, reused after); medians of interleaved rounds"}
+
+
+def measure_qk_only(torch, binding, w, sets, wq, wk, stream, dev, peak, rounds=5, calls=10):
+    """The fused scatter of Q and K alone (V moved by another path) at the same
+    shape, interleaved and half-split RoPE: rounds of `calls` calls into
+    caller-owned targets, CUDA events on the stream, inputs rotating over the
+    input sets (each launch reads 671 MB, more than L2)."""
+    P, B, S, H, D = w["P"], w["B"], w["S"], w["H"], w["D"]
+    outs = [[torch.empty((B, S, H // P, D), dtype=torch.bfloat16, device=dev) for _ in range(P)] for _ in "qk"]
+    sp, sx, _ = step_bytes(w)
+    nbytes = sp * 2 // 3 + sx  # Q and K read and written, the table and the weights
+    res = {}
+    for name, rope in (("interleaved", "interleaved"), ("half_split", "neox")):
+        kw = dict(norm_rope=True, q_weight=wq, k_weight=wk, eps=w["eps"], theta=w["theta"], rope=rope, stream=stream)
+
+        def run(n):
+            for j in range(n):
+                g = sets[j % len(sets)]
+                binding.scatter_qkv_into(g["q"], g["k"], None, outs[0], outs[1], None, **kw)
+
+        run(3)
+        torch.cuda.synchronize(dev)
+        ms = []
+        for _ in range(rounds):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run(calls)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms.append(e0.elapsed_time(e1) / calls)
+        med = statistics.median(ms)
+        gbs = nbytes / (med / 1e3) / 1e9
+        res[name] = {"ms_per_call": med, "GB/s": gbs, "frac": gbs / peak, "repeats_ms": ms}
+    res["bytes"] = nbytes
+    res["note"] = ("tf_ulysses_scatter_qkv_into with Q and K only, RMSNorm + RoPE, into caller-owned targets; "
+                   "back-to-back calls, medians of rounds")
+    return res
 
 
 def measured_tensor_peak():
@@ -531,6 +569,7 @@ def main():
         e2e = run_e2e(args, torch, binding, sets[0], wq, wk, w, stream, dev, world, sp + gp)
 
     noalloc = None if args.no_noalloc else measure_noalloc(torch, binding, w, sets, wq, wk, stream, dev)
+    qk_only = None if args.no_qk_only else measure_qk_only(torch, binding, w, sets, wq, wk, stream, dev, peak)
 
     projection = None
     if not args.no_projection:
@@ -575,6 +614,7 @@ def main():
             "cpu_baseline": cpu,
             "e2e": e2e,
             "noalloc_fused": noalloc,
+            "qk_only_fused": qk_only,
             "qkv_projection": projection,
             "clocks": clocks,
             "gpu_launches": launches,
