@@ -379,8 +379,10 @@ TF_API void tf_ulysses_set_allocator(tf_alloc_fn alloc, tf_free_fn release, void
  * Device status of the current device's kernels that wait in-kernel: 0 when
  * every wait completed; bit 0 is set when a bounded wait of the staged
  * (bulk-copy) kernel gave up, bit 1 when one of the projection kernel did --
- * that kernel then stopped early and its outputs are incomplete.  Synchronises
- * with the device.  clear != 0 resets the words after reading them.
+ * that kernel then stopped early and its outputs are incomplete.  Bit 2 exists
+ * in checked builds of the library (compiled with TFU_CHECKED=1) only: a block
+ * kernel access fell outside the buffer the plan allows and was skipped.
+ * Synchronises with the device.  clear != 0 resets the words after reading them.
  */
 TF_API tf_status tf_ulysses_device_status(int clear, unsigned *status);
 

@@ -487,6 +487,7 @@ def test_fused_16_byte_aligned_sources(tf):
 
 
 def test_device_status_clean_after_all_launches(tf):
-    """No bounded in-kernel wait gave up during any launch of this module."""
+    """No bounded in-kernel wait gave up during any launch of this process so far,
+    and (checked builds) no block-kernel access fell outside its planned buffer."""
     torch.cuda.synchronize()
     assert tf.device_status(clear=False) == 0

@@ -98,6 +98,40 @@ __host__ __device__ constexpr size_t block_tab_smem() {
     return block_tab_ring<kCopy, kNF>() ? size_t(kTabSlots) * 4 * kThreads * 16 : 0;
 }
 
+#if TFU_CHECKED
+// checked builds: nonzero once an access fell outside its planned buffer
+__device__ unsigned g_block_status;
+#endif
+
+// Whether [ptr, ptr + bytes) lies in [lo, end).  Checked builds test it and
+// record a failure in g_block_status (the caller then skips the access); other
+// builds compile it to `true`.
+__device__ __forceinline__ bool access_ok(const void* ptr, uint32_t bytes, const void* lo, const void* end) {
+#if TFU_CHECKED
+    const uintptr_t a = reinterpret_cast<uintptr_t>(ptr);
+    if (lo && a >= reinterpret_cast<uintptr_t>(lo) && a + bytes <= reinterpret_cast<uintptr_t>(end)) return true;
+    atomicOr(&g_block_status, 1u);
+    return false;
+#else
+    (void)ptr, (void)bytes, (void)lo, (void)end;
+    return true;
+#endif
+}
+
+// g_block_status of this translation unit (always 0 in unchecked builds)
+inline cudaError_t read_this_block_status(unsigned* out, bool clear) {
+#if TFU_CHECKED
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_block_status, sizeof(unsigned));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_block_status, &zero, sizeof(unsigned));
+#else
+    (void)clear;
+    *out = 0;
+    return cudaSuccess;
+#endif
+}
+
 inline int block_device_sms() {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
@@ -148,6 +182,34 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
     // both elements of every rotation pair sit in the same lane.
     auto is_split = [](int x) { return kNeox && x >= kCopy; };
     const uint32_t lane_off[2] = {dv * VW, dv * 16};  // whole-vector slots, split slots
+    // checked builds: a lane's row (holding its lane offset) of slot x against
+    // the planned bounds of shard/head-group i's buffer; the whole head row is tested
+    constexpr uint32_t kRowBytes = kLanes * VW;
+    auto src_ok = [&](const uint8_t* row, int x, uint32_t i) {
+#if TFU_CHECKED
+        return access_ok(row - lane_off[is_split(x) ? 1 : 0], kRowBytes, p.src[x][i], p.src_end[x][i]);
+#else
+        (void)row, (void)x, (void)i;
+        return true;
+#endif
+    };
+    auto dst_ok = [&](const uint8_t* row, int x, uint32_t i) {
+#if TFU_CHECKED
+        return access_ok(row - lane_off[is_split(x) ? 1 : 0], kRowBytes, p.dst[x][i], p.dst_end[x][i]);
+#else
+        (void)row, (void)x, (void)i;
+        return true;
+#endif
+    };
+    // a lane's (cos, sin) entries of one token: 2 * NP floats
+    auto tab_ok = [&](const float* t) {
+#if TFU_CHECKED
+        return access_ok(t, 2 * NP * sizeof(float), p.table, p.table_end);
+#else
+        (void)t;
+        return true;
+#endif
+    };
     // `row` already holds the lane's offset (lane_off)
     auto ld_lane = [&](const uint8_t* row, int x) {
         if (!is_split(x)) {
@@ -232,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
         return Span{beg, min(beg + per, R0 + n_rows), (per + kDepth - 1) / kDepth * kDepth};
     };
     uint32_t g, r, b;  // the (head group, shard, batch) of the unit located last
+    uint32_t g_st = 0;  // the head group of the unit being stored (set_dst)
     auto locate = [&](uint32_t u) -> Span {
         const uint32_t c = fastdiv(u, p.div_planes);
         const uint32_t q = u - c * p.n_planes;  // q = (b * P + r) * P + g
@@ -278,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
             const uint32_t lo = lane_off[is_split(x) ? 1 : 0];
             dst[x] = p.dst[x][g] + int64_t(b) * p.d_b[x] + int64_t(r) * p.Sl * p.d_t[x] + lo;
         }
+        g_st = g;
         // the lane's element pairs use table entries [dv*NP, dv*NP + NP) in both mappings
         if constexpr (kNF > 0) tab_lane = p.table + size_t(r) * p.Sl * kRowFloats + dv * (2 * NP);
         t_cached = 0xffffffffu;  // a new shard r: another table block
@@ -289,8 +353,10 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
             if (R < end && t != t_loaded) {  // the compute side sees the same tokens in the same order
                 const float* tab = p.table + (size_t(r) * p.Sl + t) * kRowFloats + dv * (2 * NP);
                 const uint32_t slot = n_loaded % kTabSlots;
+                if (tab_ok(tab)) {
 #pragma unroll
-                for (int k = 0; k < kCs; ++k) tab_cp16(ring_at(slot, k), tab + 4 * k);
+                    for (int k = 0; k < kCs; ++k) tab_cp16(ring_at(slot, k), tab + 4 * k);
+                }
                 t_loaded = t;
                 ++n_loaded;
             }
@@ -302,7 +368,10 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
 #pragma unroll
                 for (int k = 0; k < NP; ++k) buf[x].w[k] = 0u;
             }
-            if (R < end) buf[x] = ld_lane(src[x] + int64_t(t) * p.s_t[x] + int64_t(h) * p.s_h[x], x);
+            if (R < end) {
+                const uint8_t* row = src[x] + int64_t(t) * p.s_t[x] + int64_t(h) * p.s_h[x];
+                if (src_ok(row, x, r)) buf[x] = ld_lane(row, x);
+            }
         }
     };
     auto compute_store = [&](Vec<VW>(&buf)[kSlots], uint32_t R, uint32_t end) {
@@ -319,8 +388,10 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
                     ++n_read;
                 } else {
                     const float* tab = tab_lane + size_t(t) * kRowFloats;
+                    if (tab_ok(tab)) {
 #pragma unroll
-                    for (int k = 0; k < kCs; ++k) cs[k] = ld_table(tab + 4 * k);
+                        for (int k = 0; k < kCs; ++k) cs[k] = ld_table(tab + 4 * k);
+                    }
                     if constexpr (!kStream) {
                         if (t + 1 < p.Sl) asm volatile("prefetch.global.L1 [%0];" ::"l"(tab + kRowFloats));
                     }
@@ -344,7 +415,8 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
         if (valid) {  // the scatter targets of one launch share their strides (slot 0's)
             const int64_t off = int64_t(t) * p.d_t[0] + int64_t(h) * p.d_h[0];
 #pragma unroll
-            for (int x = 0; x < kSlots; ++x) st_lane(dst[x] + off, x, buf[x]);
+            for (int x = 0; x < kSlots; ++x)
+                if (dst_ok(dst[x] + off, x, g_st)) st_lane(dst[x] + off, x, buf[x]);
         }
     };
     Vec<VW> bufs[kDepth][kSlots];
@@ -427,8 +499,10 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
                     const uint32_t h = R - t * p.Hl;
                     if (valid && t != t_cached) {
                         const float* tab = tab_lane + size_t(t) * kRowFloats;
+                        if (tab_ok(tab)) {
 #pragma unroll
-                        for (int k = 0; k < kCs; ++k) cs[k] = ld_table(tab + 4 * k);
+                            for (int k = 0; k < kCs; ++k) cs[k] = ld_table(tab + 4 * k);
+                        }
                         t_cached = t;
                     }
 #pragma unroll
@@ -437,10 +511,11 @@ __global__ void __launch_bounds__(kThreads, block_min_blocks<kCopy, kNF>())
                         Vec<VW> v;
 #pragma unroll
                         for (int k = 0; k < NP; ++k) v.w[k] = 0u;
-                        if (valid) v = ld_lane(src[x0 + f] + int64_t(t) * p.s_t[x0 + f] + int64_t(h) * p.s_h[x0 + f],
-                                               x0 + f);
+                        const uint8_t* srow = src[x0 + f] + int64_t(t) * p.s_t[x0 + f] + int64_t(h) * p.s_h[x0 + f];
+                        uint8_t* drow = dst[x0 + f] + int64_t(t) * p.d_t[0] + int64_t(h) * p.d_h[0];
+                        if (valid && src_ok(srow, x0 + f, r)) v = ld_lane(srow, x0 + f);
                         fused_row(std::true_type{}, v.w, f);
-                        if (valid) st_lane(dst[x0 + f] + int64_t(t) * p.d_t[0] + int64_t(h) * p.d_h[0], x0 + f, v);
+                        if (valid && dst_ok(drow, x0 + f, g)) st_lane(drow, x0 + f, v);
                     }
                 }
             }

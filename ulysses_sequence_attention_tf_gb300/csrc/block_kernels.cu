@@ -27,4 +27,6 @@ cudaError_t launch_blocks(const RelayoutParams& p, Fused fused, cudaStream_t str
     return cudaErrorInvalidValue;
 }
 
+cudaError_t read_block_status(unsigned* out, bool clear) { return read_this_block_status(out, clear); }
+
 }  // namespace tfu

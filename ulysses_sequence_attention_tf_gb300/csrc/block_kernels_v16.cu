@@ -15,4 +15,6 @@ cudaError_t launch_blocks_v16(const RelayoutParams& p, Fused fused, cudaStream_t
     }
 }
 
+cudaError_t read_block_status_v16(unsigned* out, bool clear) { return read_this_block_status(out, clear); }
+
 }  // namespace tfu

@@ -11,6 +11,10 @@ namespace tfu {
 
 constexpr int kMaxShards = 8;
 constexpr int kMaxSlots = 3;      // Q, K, V
+#ifndef TFU_CHECKED
+#define TFU_CHECKED 0  // 1: block kernels test their accesses against the planned buffers
+#endif
+
 constexpr int kThreads = 256;          // threads per CTA
 #ifndef TFU_CHUNK_BYTES
 #define TFU_CHUNK_BYTES 32768
@@ -98,6 +102,14 @@ struct RelayoutParams {
     uint32_t Hg;          // heads between consecutive head groups on the head-major side (scatter
                           // source, gather destination): Hl, or the whole band when a launch moves
                           // a head chunk of Hl heads out of every band
+#if TFU_CHECKED
+    // checked builds: one past the last byte each slot's buffers may be accessed
+    // at (from the plan's shapes and strides), and the table's; the block kernel
+    // tests every row and table access against [base, end) and skips any outside
+    const uint8_t* src_end[kMaxSlots][kMaxShards];
+    const uint8_t* dst_end[kMaxSlots][kMaxShards];
+    const float* table_end;
+#endif
 };
 // Field order is part of the staged kernel's speed: inserting one 4-byte field
 // before `nx` (shifting every later field by 4 bytes) measured ~1.3 % slower
@@ -123,6 +135,13 @@ inline cudaError_t launch_overlapped(void (*kernel)(Params...), unsigned grid, u
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
+
+// Checked builds (TFU_CHECKED=1): the block kernels' bounds status -- nonzero
+// once a row or table access of a block kernel fell outside the ranges in
+// RelayoutParams (the access was skipped); optionally cleared.  Always 0 in
+// other builds.  One word per translation unit: 32-byte and 16-byte forms.
+cudaError_t read_block_status(unsigned* out, bool clear);
+cudaError_t read_block_status_v16(unsigned* out, bool clear);
 
 // Launch the relayout of every plane in `p` with the register kernel (vector
 // width p.vec_bytes); pure relayouts only (fused scatters take the block

@@ -252,6 +252,27 @@ tf_status launch_planned(RelayoutParams& p, const Shape& sh, tfu::Dir dir, tfu::
     p.row_bytes = rb;
     p.plane_rows = uint32_t(rows);
     p.div_hl = tfu::make_fastdiv(p.Hl);
+#if TFU_CHECKED
+    {
+        // the last byte a kernel may touch in each slot's buffers: token rows
+        // [0, tokens), heads [0, span) of the head-major side (bands Hg apart) or
+        // [0, Hl) of the token-major side, batch rows [0, B)
+        const int64_t span_heads = int64_t(sh.P - 1) * sh.Hg + sh.Hl;
+        const bool scatter = dir == tfu::Dir::kScatter;
+        for (uint32_t x = 0; x < p.nx; ++x)
+            for (int i = 0; i < sh.P; ++i) {
+                const int64_t src_heads = scatter ? span_heads : sh.Hl;
+                const int64_t dst_heads = scatter ? sh.Hl : span_heads;
+                p.src_end[x][i] = p.src[x][i] ? p.src[x][i] + (sh.B - 1) * p.s_b[x] + (src_tokens - 1) * p.s_t[x] +
+                                                    (src_heads - 1) * p.s_h[x] + rb
+                                              : nullptr;
+                p.dst_end[x][i] = p.dst[x][i] ? p.dst[x][i] + (sh.B - 1) * p.d_b[x] + (dst_tokens - 1) * p.d_t[x] +
+                                                    (dst_heads - 1) * p.d_h[x] + rb
+                                              : nullptr;
+            }
+        p.table_end = p.table ? p.table + dst_tokens * int64_t(sh.D) : nullptr;
+    }
+#endif
     // row-unit grids (block and staged kernels): `blocks` row ranges of rpu rows
     auto plan_rows = [&](uint64_t blocks, uint32_t rpu) -> tf_status {
         const uint64_t chunks = (rows + rpu - 1) / rpu;
@@ -1091,11 +1112,13 @@ TF_API void tf_ulysses_set_allocator(tf_alloc_fn alloc, tf_free_fn release, void
 
 TF_API tf_status tf_ulysses_device_status(int clear, unsigned* status) {
     if (!status) return fail(TF_ERR_INVALID, "status is NULL");
-    unsigned staged = 0, gemm = 0;
+    unsigned staged = 0, gemm = 0, block = 0, block16 = 0;
     cudaError_t e = tfu::read_staged_status(&staged, clear != 0);
     if (e == cudaSuccess) e = tfu::read_gemm_status(&gemm, clear != 0);
+    if (e == cudaSuccess) e = tfu::read_block_status(&block, clear != 0);
+    if (e == cudaSuccess) e = tfu::read_block_status_v16(&block16, clear != 0);
     if (e != cudaSuccess) return cuda_fail(e, "reading the device status words");
-    *status = (staged ? 1u : 0u) | (gemm ? 2u : 0u);
+    *status = (staged ? 1u : 0u) | (gemm ? 2u : 0u) | ((block | block16) ? 4u : 0u);
     return TF_OK;
 }
 
