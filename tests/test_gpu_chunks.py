@@ -97,6 +97,28 @@ def test_fused_head_chunks(tf, rope):
         assert bits_equal(outs["v"][i].cpu(), want_v[i])
 
 
+@pytest.mark.parametrize("rope", ["interleaved", "neox"])
+def test_fused_head_chunks_qk_only(tf, rope):
+    """Q and K alone (V moved by another path) in head chunks: the Q/K-only launch
+    (its (cos, sin) ring and paired rows) reading head bands Hg heads apart."""
+    P, B, Sl, H, D = 4, 2, 70, 24, 128
+    Hl, S = H // P, P * Sl
+    dtype = torch.float16 if rope == "neox" else torch.bfloat16
+    d = synth.qkv_shards(P, B, Sl, H, D, dtype, seed=19, layout="v_strided", with_v=False)
+    wq, wk = synth.norm_weights(D, dtype, seed=19)
+    g = synth.move(d, "cuda")
+    outs = {k: _targets(P, B, S, Hl, D, dtype) for k in "qk"}
+    for h0, h1 in ((0, 2), (2, 5), (5, Hl)):
+        tf.scatter_qkv_heads_into(g["q"], g["k"], None, outs["q"], outs["k"], None, h0=h0, h1=h1,
+                                  norm_rope=True, q_weight=wq.cuda(), k_weight=wk.cuda(), eps=EPS, theta=THETA,
+                                  rope=rope)
+    table = oracle.rope_table(THETA, S, D)
+    for key, w in (("q", wq), ("k", wk)):
+        want = oracle.scatter_norm_rope(d[key], P, w, EPS, table, style=rope)
+        for i in range(P):
+            assert_fused_ok(outs[key][i], want[i])
+
+
 def test_head_chunks_into_fused_layout(tf):
     P, B, Sl, H, D = 2, 2, 21, 8, 64
     Hl, S = H // P, P * Sl

@@ -102,6 +102,35 @@ def test_noalloc_matches_existing_entry_point_call_after_call(tf):
                     assert_fused_ok(out[x][gi], want[gi])
 
 
+@pytest.mark.parametrize("rope", ["interleaved", "neox"])
+def test_noalloc_qk_only(tf, rope):
+    """Q and K alone through the allocation-free entry point (the Q/K-only launch
+    with its (cos, sin) ring): bit for bit what scatter_qkv_into gives, no
+    allocation."""
+    P, B, S, H, D, dtype = 4, 1, 2048, 16, 128, torch.bfloat16
+    Sl, Hl = S // P, H // P
+    d = synth.qkv_shards(P, B, Sl, H, D, dtype, seed=77, layout="v_strided", with_v=False)
+    g = synth.move(d, "cuda")
+    wq, wk = synth.norm_weights(D, dtype, seed=77)
+    kw = dict(norm_rope=True, q_weight=wq.cuda(), k_weight=wk.cuda(), eps=1e-6, theta=10000.0, rope=rope)
+    ref = [_targets(P, B, S, Hl, D, dtype, 0.0) for _ in range(2)]
+    tf.scatter_qkv_into(g["q"], g["k"], None, ref[0], ref[1], None, **kw)
+    out = [_targets(P, B, S, Hl, D, dtype, 9.0) for _ in range(2)]
+    torch.cuda.synchronize()
+    allocs = tf.alloc_count()
+    counter = _CountingAllocator(tf)
+    tf.lib().tf_ulysses_set_allocator(counter.fns[0], counter.fns[1], None)
+    try:
+        tf.scatter_qkv_noalloc(g["q"], g["k"], None, out[0], out[1], None, **kw)
+        torch.cuda.synchronize()
+    finally:
+        tf.use_torch_allocator(True)
+    assert counter.calls == 0 and tf.alloc_count() == allocs
+    for x in range(2):
+        for gi in range(P):
+            assert bits_equal(out[x][gi], ref[x][gi]), (rope, x, gi)
+
+
 def test_noalloc_rejects_sizes_beyond_the_fixed_scratch(tf):
     P, B, Sl, H, D = 2, 1, 16385, 4, 128  # P * S_local * D = 4,194,560 > 4 Mi floats
     dtype = torch.bfloat16
