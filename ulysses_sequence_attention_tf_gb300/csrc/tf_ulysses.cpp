@@ -20,6 +20,7 @@
 #include <vector>
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "gemm.h"
 #include "noalloc.h"
@@ -28,6 +29,16 @@
 #include "tma_plan.h"
 
 namespace {
+
+// A named NVTX range around each C-ABI call, so that a profiler's timeline shows
+// which library call issued which launches (header-only NVTX; a few nanoseconds
+// when no profiler is attached).
+struct CallRange {
+    explicit CallRange(const char* name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+    CallRange(const CallRange&) = delete;
+    CallRange& operator=(const CallRange&) = delete;
+};
 
 using tfu::RelayoutParams;
 
@@ -665,6 +676,7 @@ TF_API tf_status tf_ulysses_scatter_qkv(const char* tag, const void* const* q, c
                                         const void* const* v, const tf_strides* strides, int P, int B, int S_local,
                                         int H, int D, tf_dtype dtype, tf_mode mode, const tf_norm_rope* nr,
                                         void* stream, tf_targets* out) {
+    CallRange call_range("tf_ulysses_scatter_qkv");
     std::string key;
     tf_status s = check_tag(tag, &key);
     if (s != TF_OK) return s;
@@ -722,6 +734,7 @@ TF_API tf_status tf_ulysses_scatter_qkv_into(const void* const* q, const void* c
                                              tf_dtype dtype, tf_mode mode, const tf_norm_rope* nr,
                                              void* const* q_out, void* const* k_out, void* const* v_out,
                                              void* stream) {
+    CallRange call_range("tf_ulysses_scatter_qkv_into");
     ScatterPlan pl;
     tf_status s = plan_scatter(q, k, v, strides, P, B, S_local, H, D, dtype, mode, nr, &pl);
     if (s != TF_OK) return s;
@@ -747,6 +760,7 @@ TF_API tf_status tf_ulysses_scatter_qkv_noalloc(const void* const* q, const void
                                                 tf_dtype dtype, tf_mode mode, const tf_norm_rope* nr,
                                                 void* const* q_out, void* const* k_out, void* const* v_out,
                                                 void* stream) {
+    CallRange call_range("tf_ulysses_scatter_qkv_noalloc");
     ScatterPlan pl;
     tf_status s = plan_scatter(q, k, v, strides, P, B, S_local, H, D, dtype, mode, nr, &pl);
     if (s != TF_OK) return s;
@@ -781,6 +795,7 @@ TF_API tf_status tf_ulysses_scatter_qkv_heads_into(const void* const* q, const v
                                                    int D, tf_dtype dtype, tf_mode mode, const tf_norm_rope* nr,
                                                    int h0, int h1, void* const* q_out, void* const* k_out,
                                                    void* const* v_out, void* stream) {
+    CallRange call_range("tf_ulysses_scatter_qkv_heads_into");
     ScatterPlan pl;
     tf_status s = plan_scatter(q, k, v, strides, P, B, S_local, H, D, dtype, mode, nr, &pl);
     if (s != TF_OK) return s;
@@ -816,6 +831,7 @@ TF_API tf_status tf_ulysses_scatter_qkv_heads_into(const void* const* q, const v
 // stride chunk_bytes.
 TF_API tf_status tf_ulysses_exchange_chunks(const void* const* src, void* const* dst, int P, size_t chunk_bytes,
                                             void* stream) {
+    CallRange call_range("tf_ulysses_exchange_chunks");
     if (P < 1 || P > TF_ULYSSES_MAX_SHARDS) return fail(TF_ERR_INVALID, "P=%d outside [1, %d]", P, TF_ULYSSES_MAX_SHARDS);
     if (!src || !dst) return fail(TF_ERR_INVALID, "src or dst is NULL");
     if (chunk_bytes % 16 != 0) return fail(TF_ERR_ALIGNMENT, "chunk_bytes=%zu is not a multiple of 16", chunk_bytes);
@@ -868,6 +884,7 @@ TF_API tf_status tf_ulysses_project_qkv_into(const void* const* x, int64_t x_row
                                              int D, tf_dtype dtype, tf_mode mode, const tf_norm_rope* nr,
                                              void* const* q_out, void* const* k_out, void* const* v_out,
                                              void* stream) {
+    CallRange call_range("tf_ulysses_project_qkv_into");
     Shape sh;
     tf_status s = check_shape(P, B, S_local, H, D, dtype, &sh);
     if (s != TF_OK) return s;
@@ -982,6 +999,7 @@ TF_API tf_status tf_ulysses_project_qkv_into(const void* const* x, int64_t x_row
 TF_API tf_status tf_ulysses_gather_out(const char* tag, const void* const* attn, const tf_strides* attn_strides,
                                        int P, int B, int S_local, int H, int D, tf_dtype dtype, void* const* dst,
                                        const tf_strides* dst_strides, void* stream, tf_targets* out) {
+    CallRange call_range("tf_ulysses_gather_out");
     std::string key;
     tf_status s = check_tag(tag, &key);
     if (s != TF_OK) return s;
@@ -1044,6 +1062,7 @@ TF_API tf_status tf_ulysses_gather_out(const char* tag, const void* const* attn,
 }
 
 TF_API tf_status tf_ulysses_rope_table(float theta, int S, int D, void* stream, const float** table) {
+    CallRange call_range("tf_ulysses_rope_table");
     if (!table) return fail(TF_ERR_INVALID, "table is NULL");
     if (S < 0) return fail(TF_ERR_INVALID, "S must be >= 0");
     if (D < 2 || D > 256 || D % 2) return fail(TF_ERR_UNSUPPORTED, "D must be even and in [2, 256]");
@@ -1061,6 +1080,7 @@ TF_API tf_status tf_ulysses_rope_table(float theta, int S, int D, void* stream, 
 }
 
 TF_API tf_status tf_ulysses_cache_clear(void) {
+    CallRange call_range("tf_ulysses_cache_clear");
     std::lock_guard<std::mutex> lock(g_mu);
     if (g_entries.empty() && g_tables.empty()) return TF_OK;
     for (auto& e : g_entries) {
